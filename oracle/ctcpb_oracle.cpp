@@ -1,0 +1,424 @@
+// CPU oracle for batched CTC prefix beam search -- TEST INFRASTRUCTURE ONLY.
+//
+// Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+// call this library.  It shares no code, header, table or constant generator
+// with the CUDA decoder: every formula below is restated from the method's
+// description ("GPU CTC Prefix Beam Search Decoder", OASR docs, section 3) and
+// from mathematics.  It is deliberately plain and slow: every step scores the
+// whole beam x vocabulary table, merges by comparing stored prefixes, and ranks
+// with a library sort.
+//
+// Arithmetic.  The method stores its log-probabilities in float32 (log_prob is
+// float32; pprev is a float2; score is a float), so the oracle computes in
+// float32 with a fixed operation order.  Build with -ffp-contract=off and
+// without -ffast-math: fused multiply-adds appear only where fmaf() is written.
+//
+//   NEG          = -FLT_MAX, the additive identity of the log semiring
+//                  (section 3, the logsumexp definition).
+//   add(a, b)    = max(a + b, NEG)          -- a product of probabilities
+//   lse(a, b)    = max(a,b) + L(E(-|a-b|))  -- section 3's logsumexp
+//   E(x)         = exp(x) for x <= 0: Cody-Waite reduction x = n ln2 + r with
+//                  |r| <= ln2/2, degree-7 Taylor polynomial of e^r, times 2^n;
+//                  E(x) = 0 for x < -87 (below the smallest normal result).
+//   L(x)         = log(1 + x) for x in [0, 1] through the series
+//                  log(1+x) = 2 atanh(s), s = x/(2+x), summed to s^13; for
+//                  x > sqrt(2)-1 it uses log(1+x) = ln2 + 2 atanh((x-1)/(x+3)).
+//   lp read      = max(raw, NEG) + 0.0f (clamps -inf/NaN to NEG, -0 to +0).
+//
+// Decoding follows section 3 of the page:
+//   3.3   step 0 seeds the top (beam-1) non-blank labels (beam 1: one label)
+//         by (log-prob desc, id asc), then the empty prefix in the last slot;
+//         a skipped lead-in puts each label's mass in its blank slot.
+//   3.4   collapsed-blank correction when frames were skipped (t > t_prev+1):
+//         prev = (lse(pb, pnb), NEG) before the step, winners = (score, NEG)
+//         after it (3.4.5).
+//   3.4.1 non-blank extension: c != last -> lp[c] + lse(pb, pnb);
+//         c == last -> lp[c] + pb; the stay path lp[last] + pnb goes to the
+//         beam's own blank slot.
+//   3.4.2 blank slot: pb' = lp[blank] + lse(pb, pnb); pnb' = stay, or NEG for
+//         the empty prefix or after a gap.
+//   3.4.3 merge: if len_j = len_i + 1 and l_j starts with l_i, candidate
+//         (i, last_j) is folded into j's blank slot (pnb'_j = lse(pnb'_j, .))
+//         and dropped.
+//   3.4.4/5 score = lse(pb', pnb'); keep the best `beam` live candidates.
+// Readings where the page is silent or inconsistent:
+//   * ties rank by (score desc, source slot asc, token asc), blank's token is
+//     blank_id; a candidate with score <= NEG is dead and never kept;
+//   * a hypothesis whose length equals the cap max_seq_len has no non-blank
+//     extensions (its blank/stay slot still applies);
+//   * frames are kept iff lp[blank] < log(threshold) (section 3.5), threshold
+//     >= 1 keeps all frames and <= 0 keeps none (section 13);
+//   * a row with no kept frame returns the empty prefix with score 0 in slot 0
+//     and dead slots after it (section 13);
+//   * output: the first nbest slots after a stable sort by score (desc);
+//     dead slots have length 0, score NEG and tokens -1; tokens past out_len
+//     are cut while the length still reports the full count (section 13).
+
+#include <algorithm>
+#include <atomic>
+#include <cfloat>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr float NEG = -FLT_MAX;
+
+// ln 2 split for Cody-Waite: HI keeps the top 16 significant bits of ln 2, so
+// n * HI is exact for |n| <= 127; LO = ln2 - HI rounded to float.
+constexpr float LN2_HI = 0.693145751953125f;
+constexpr float LN2_LO = 1.42860682030941723212e-6f;
+constexpr float LOG2E = 1.44269504088896340736f;
+constexpr float SQRT2_M1 = 0.41421356237309504880f;
+
+float from_bits(uint32_t u) {
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+// exp(x) for x <= 0.
+float fE(float x) {
+  if (!(x >= -87.0f)) return 0.0f;
+  float t = x * LOG2E;
+  float n = std::rint(t);
+  float r = std::fmaf(n, -LN2_HI, x);
+  r = std::fmaf(n, -LN2_LO, r);
+  // Taylor series of e^r: sum_{k=0..7} r^k / k!
+  float p = (float)(1.0 / 5040.0);
+  p = std::fmaf(p, r, (float)(1.0 / 720.0));
+  p = std::fmaf(p, r, (float)(1.0 / 120.0));
+  p = std::fmaf(p, r, (float)(1.0 / 24.0));
+  p = std::fmaf(p, r, (float)(1.0 / 6.0));
+  p = std::fmaf(p, r, 0.5f);
+  p = std::fmaf(p, r, 1.0f);
+  p = std::fmaf(p, r, 1.0f);
+  int ni = (int)n;  // in [-126, 0]
+  float scale = from_bits((uint32_t)(ni + 127) << 23);
+  return p * scale;
+}
+
+// log(1 + x) for x in [0, 1].
+float fL(float x) {
+  const bool lo_half = x <= SQRT2_M1;
+  float num = lo_half ? x : x - 1.0f;
+  float den = lo_half ? 2.0f + x : x + 3.0f;
+  float hi = lo_half ? 0.0f : LN2_HI;
+  float lo = lo_half ? 0.0f : LN2_LO;
+  float s = num / den;
+  float z = s * s;
+  // 2 atanh(s) = 2s (1 + z/3 + z^2/5 + ... + z^6/13)
+  float q = (float)(1.0 / 13.0);
+  q = std::fmaf(q, z, (float)(1.0 / 11.0));
+  q = std::fmaf(q, z, (float)(1.0 / 9.0));
+  q = std::fmaf(q, z, (float)(1.0 / 7.0));
+  q = std::fmaf(q, z, (float)(1.0 / 5.0));
+  q = std::fmaf(q, z, (float)(1.0 / 3.0));
+  float w = z * q;
+  float t2 = s + s;
+  float r = std::fmaf(t2, w, t2);
+  return (r + lo) + hi;
+}
+
+float lse(float a, float b) {
+  float m = std::fmax(a, b);
+  float d = std::fabs(a - b);
+  return m + fL(fE(-d));
+}
+
+float add(float a, float b) { return std::fmax(a + b, NEG); }
+
+float rd(const float* p) { return std::fmax(*p, NEG) + 0.0f; }
+
+struct Hyp {
+  std::vector<int32_t> pre;
+  float pb, pnb;
+  float score() const { return lse(pb, pnb); }
+  int32_t last(int blank) const { return pre.empty() ? blank : pre.back(); }
+};
+
+struct Cand {
+  float score;
+  int32_t src, tok;
+  float pb, pnb;
+};
+
+// ranking: score desc, then source slot asc, then token asc
+bool better(const Cand& x, const Cand& y) {
+  if (x.score != y.score) return x.score > y.score;
+  if (x.src != y.src) return x.src < y.src;
+  return x.tok < y.tok;
+}
+
+struct Args {
+  const float* lp;
+  int64_t sb, st;
+  const int32_t* lens;
+  int B, T, V, beam, nbest, blank, cap;
+  float thr;
+  int32_t* out_tokens;
+  int32_t* out_lengths;
+  float* out_scores;
+  int out_len;
+};
+
+bool keep_frame(float lpb, float thr, float log_thr) {
+  if (thr >= 1.0f) return true;
+  if (!(thr > 0.0f)) return false;
+  return lpb < log_thr;
+}
+
+float log_threshold(float thr) {
+  if (thr >= 1.0f || !(thr > 0.0f)) return NEG;
+  return (float)std::log((double)thr);
+}
+
+// Non-blank live labels of one frame in (lp desc, id asc) order.
+void ranked_labels(const float* row, int V, int blank, std::vector<std::pair<float, int32_t>>& out) {
+  out.clear();
+  for (int c = 0; c < V; ++c) {
+    if (c == blank) continue;
+    float v = rd(row + c);
+    if (v > NEG) out.push_back({v, c});
+  }
+  std::sort(out.begin(), out.end(), [](const std::pair<float, int32_t>& a, const std::pair<float, int32_t>& b) {
+    if (a.first != b.first) return a.first > b.first;
+    return a.second < b.second;
+  });
+}
+
+void decode_row(const Args& a, int b) {
+  const float* base = a.lp + (int64_t)b * a.sb;
+  auto row = [&](int t) { return base + (int64_t)t * a.st; };
+  const float log_thr = log_threshold(a.thr);
+  int len_b = std::min(std::max(a.lens ? a.lens[b] : a.T, 0), a.T);
+
+  // section 3.5: ordered list of kept frames
+  std::vector<int> sel;
+  for (int t = 0; t < len_b; ++t)
+    if (keep_frame(rd(row(t) + a.blank), a.thr, log_thr)) sel.push_back(t);
+
+  std::vector<Hyp> beams;
+  if (sel.empty()) {
+    beams.push_back(Hyp{{}, 0.0f, NEG});
+  } else {
+    // ---- step 0 (section 3.3)
+    const int t0 = sel[0];
+    const bool gap0 = t0 > 0;
+    const int nb = a.beam > 1 ? a.beam - 1 : 1;
+    std::vector<std::pair<float, int32_t>> ranked;
+    ranked_labels(row(t0), a.V, a.blank, ranked);
+    if (a.cap >= 1) {
+      for (int k = 0; k < nb && k < (int)ranked.size(); ++k) {
+        float v = ranked[k].first;
+        Hyp h{{ranked[k].second}, gap0 ? v : NEG, gap0 ? NEG : v};
+        beams.push_back(h);
+      }
+    }
+    if (a.beam > 1) {
+      float lpb = rd(row(t0) + a.blank);
+      if (lpb > NEG) beams.push_back(Hyp{{}, lpb, NEG});
+    }
+
+    // ---- steps s >= 1 (section 3.4)
+    std::vector<Cand> cands;
+    for (size_t s = 1; s < sel.size(); ++s) {
+      const int t = sel[s];
+      const bool gap = t > sel[s - 1] + 1;
+      const float* lpt = row(t);
+      const int K = (int)beams.size();
+      if (K == 0) break;
+      // collapsed-blank correction of the previous probabilities
+      std::vector<float> pb(K), pnb(K), A(K);
+      for (int k = 0; k < K; ++k) {
+        pb[k] = beams[k].pb;
+        pnb[k] = beams[k].pnb;
+        if (gap) {
+          pb[k] = lse(pb[k], pnb[k]);
+          pnb[k] = NEG;
+        }
+        A[k] = lse(pb[k], pnb[k]);
+      }
+      // section 3.4.3 pair condition: into[j] = i when l_j = l_i + last(l_j)
+      std::vector<int> into(K, -1);
+      for (int j = 0; j < K; ++j)
+        for (int i = 0; i < K; ++i) {
+          const auto& li = beams[i].pre;
+          const auto& lj = beams[j].pre;
+          if (lj.size() == li.size() + 1 && std::equal(li.begin(), li.end(), lj.begin())) into[j] = i;
+        }
+      std::vector<std::vector<int32_t>> folded(K);  // labels of beam i folded away
+      for (int j = 0; j < K; ++j)
+        if (into[j] >= 0) folded[into[j]].push_back(beams[j].last(a.blank));
+
+      const float lpb = rd(lpt + a.blank);
+      cands.clear();
+      for (int k = 0; k < K; ++k) {
+        const Hyp& h = beams[k];
+        const int32_t last = h.last(a.blank);
+        const bool empty = h.pre.empty();
+        // section 3.4.2 blank slot, with section 3.4.1's stay contribution
+        float bpb = add(lpb, A[k]);
+        float bpnb = (!empty && !gap) ? add(rd(lpt + last), pnb[k]) : NEG;
+        if (into[k] >= 0) {
+          // section 3.4.3: fold candidate (i, last_k) into this blank slot; its
+          // value is the section 3.4.1 table entry, which takes the repeat
+          // path (pb only) when last_k is also the last label of l_i
+          int i = into[k];
+          const bool rep = !beams[i].pre.empty() && beams[i].pre.back() == last;
+          float ext = rep ? add(rd(lpt + last), pb[i]) : add(rd(lpt + last), A[i]);
+          bpnb = lse(bpnb, ext);
+        }
+        float sc = lse(bpb, bpnb);
+        if (sc > NEG) cands.push_back(Cand{sc, k, a.blank, bpb, bpnb});
+        if ((int)h.pre.size() >= a.cap) continue;
+        // section 3.4.1 non-blank extensions
+        for (int c = 0; c < a.V; ++c) {
+          if (c == a.blank) continue;
+          if (std::find(folded[k].begin(), folded[k].end(), c) != folded[k].end()) continue;
+          float v = rd(lpt + c);
+          float ext = (!empty && c == last) ? add(v, pb[k]) : add(v, A[k]);
+          if (ext > NEG) cands.push_back(Cand{ext, k, c, NEG, ext});
+        }
+      }
+      // section 3.4.4/3.4.5: keep the best `beam`
+      size_t keep = std::min(cands.size(), (size_t)a.beam);
+      if (cands.size() > keep) std::nth_element(cands.begin(), cands.begin() + keep, cands.end(), better);
+      std::sort(cands.begin(), cands.begin() + keep, better);
+      std::vector<Hyp> next;
+      next.reserve(keep);
+      for (size_t w = 0; w < keep; ++w) {
+        const Cand& c = cands[w];
+        Hyp h;
+        h.pre = beams[c.src].pre;
+        if (c.tok != a.blank) h.pre.push_back(c.tok);
+        if (gap) {
+          h.pb = c.score;
+          h.pnb = NEG;
+        } else {
+          h.pb = c.pb;
+          h.pnb = c.pnb;
+        }
+        next.push_back(std::move(h));
+      }
+      beams.swap(next);
+    }
+  }
+
+  // ---- output (sections 3.6 and 13)
+  std::vector<int> order(beams.size());
+  std::vector<float> sc(beams.size());
+  for (size_t k = 0; k < beams.size(); ++k) {
+    order[k] = (int)k;
+    sc[k] = beams[k].score();
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return sc[x] > sc[y]; });
+  for (int n = 0; n < a.nbest; ++n) {
+    int32_t* tok = a.out_tokens + ((int64_t)b * a.nbest + n) * a.out_len;
+    for (int i = 0; i < a.out_len; ++i) tok[i] = -1;
+    int64_t o = (int64_t)b * a.nbest + n;
+    if (n < (int)order.size()) {
+      const Hyp& h = beams[order[n]];
+      a.out_lengths[o] = (int32_t)h.pre.size();
+      a.out_scores[o] = sc[order[n]];
+      for (int i = 0; i < (int)h.pre.size() && i < a.out_len; ++i) tok[i] = h.pre[i];
+    } else {
+      a.out_lengths[o] = 0;
+      a.out_scores[o] = NEG;
+    }
+  }
+}
+
+void for_rows(int B, int threads, const std::function<void(int)>& fn) {
+  if (threads <= 0) threads = (int)std::thread::hardware_concurrency();
+  threads = std::max(1, std::min(threads, B));
+  std::atomic<int> next{0};
+  auto work = [&]() {
+    for (int b; (b = next.fetch_add(1)) < B;) fn(b);
+  };
+  std::vector<std::thread> pool;
+  for (int i = 1; i < threads; ++i) pool.emplace_back(work);
+  work();
+  for (auto& th : pool) th.join();
+}
+}  // namespace
+
+extern "C" {
+
+float ctcpb_oracle_E(float x) { return fE(x); }
+float ctcpb_oracle_L(float x) { return fL(x); }
+float ctcpb_oracle_lse(float a, float b) { return lse(a, b); }
+float ctcpb_oracle_add(float a, float b) { return add(a, b); }
+float ctcpb_oracle_log_threshold(float thr) { return log_threshold(thr); }
+
+void ctcpb_oracle_map(int which, const float* a, const float* b, float* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    switch (which) {
+      case 0: out[i] = fE(a[i]); break;
+      case 1: out[i] = fL(a[i]); break;
+      case 2: out[i] = lse(a[i], b[i]); break;
+      default: out[i] = add(a[i], b[i]); break;
+    }
+  }
+}
+
+// Section 3.5: kept frames of each row, in order.  sel is [B, T], nsel is [B].
+int ctcpb_oracle_select_frames(const float* lp, int64_t sb, int64_t st, const int32_t* lens, int B, int T,
+                               int blank, float thr, int32_t* sel, int32_t* nsel) {
+  const float log_thr = log_threshold(thr);
+  for (int b = 0; b < B; ++b) {
+    int len_b = std::min(std::max(lens ? lens[b] : T, 0), T);
+    int n = 0;
+    for (int t = 0; t < len_b; ++t)
+      if (keep_frame(rd(lp + b * sb + (int64_t)t * st + blank), thr, log_thr)) sel[(int64_t)b * T + n++] = t;
+    for (int i = n; i < T; ++i) sel[(int64_t)b * T + i] = -1;
+    nsel[b] = n;
+  }
+  return 0;
+}
+
+// The ranked non-blank labels of each of R frame rows ([R, V], row stride st):
+// the first C by (lp desc, id asc), their count, the blank log-prob, and the
+// next label after them (front) or (NEG, -1) when there is none.
+int ctcpb_oracle_frame_lists(const float* lp, int64_t st, int R, int V, int blank, int C, int32_t* ids,
+                             float* lps, int32_t* cnt, float* lpb, float* front_lp, int32_t* front_id) {
+  std::vector<std::pair<float, int32_t>> ranked;
+  for (int r = 0; r < R; ++r) {
+    const float* row = lp + (int64_t)r * st;
+    ranked_labels(row, V, blank, ranked);
+    int n = std::min((int)ranked.size(), C);
+    for (int i = 0; i < C; ++i) {
+      ids[(int64_t)r * C + i] = i < n ? ranked[i].second : -1;
+      lps[(int64_t)r * C + i] = i < n ? ranked[i].first : NEG;
+    }
+    cnt[r] = n;
+    lpb[r] = rd(row + blank);
+    if ((int)ranked.size() > C) {
+      front_lp[r] = ranked[C].first;
+      front_id[r] = ranked[C].second;
+    } else {
+      front_lp[r] = NEG;
+      front_id[r] = -1;
+    }
+  }
+  return 0;
+}
+
+// Offline decode of B rows.  cap >= 1 is the per-hypothesis token cap.
+// Outputs: tokens [B, nbest, out_len], lengths [B, nbest], scores [B, nbest].
+int ctcpb_oracle_decode(const float* lp, int64_t sb, int64_t st, const int32_t* lens, int B, int T, int V,
+                        int beam, int nbest, int blank, int cap, float thr, int threads, int32_t* out_tokens,
+                        int32_t* out_lengths, float* out_scores, int out_len) {
+  if (B < 0 || T < 0 || V < 2 || beam < 1 || nbest < 1 || nbest > beam || blank < 0 || blank >= V || cap < 1 ||
+      out_len < 0)
+    return -1;
+  Args a{lp, sb, st, lens, B, T, V, beam, nbest, blank, cap, thr, out_tokens, out_lengths, out_scores, out_len};
+  for_rows(B, threads, [&](int b) { decode_row(a, b); });
+  return 0;
+}
+
+}  // extern "C"
