@@ -1,0 +1,337 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 CTC prefix beam search decoder.
+
+Default workload (N=1): the offline BPE decode, B=32 utterances, T=500 frames
+(lengths uniform in [250, 500]), V=5000 labels, beam=10, N-best=10, float32
+log-probabilities of peaky synthetic logits.  One "step" is one full offline
+decode of that batch (frame selection, vocabulary pre-pass, every beam step,
+N-best gather) with the inputs already resident in HBM.
+
+Prints one JSON line (rank 0).  Metric: frames/s counted as B*T per second
+(the valid-frame rate is reported beside it), and the achieved HBM bandwidth
+of the decode against the measured GB300 copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the plain prefix beam search the
+decoder is checked against) on the host cores, on the same workload.
+Multi-GPU (torchrun, one process per GPU): every rank decodes its own batch
+of the workload (rows shard with no collective); value = all ranks' frames
+over the slowest rank's time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ctc_prefix_beam_gb300 import synth  # noqa: E402
+
+METRIC = "frames/sec (B·T/s) and achieved HBM GB/s vs roofline, 1×GB300"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def args_():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="bpe", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, index: int, enabled: bool = True):
+        self.index, self.enabled, self.proc, self.out = index, enabled, None, ""
+
+    def __enter__(self):
+        if self.enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                     "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGINT)
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ bytes
+
+def algorithmic_bytes(w, lp, lens, kept, L):
+    """Bytes the decode must move (per step of the benchmark)."""
+    V, beam, nbest = w.V, w.beam, w.nbest
+    n_kept = int(kept.sum())
+    n_valid = int(np.minimum(lens, w.T).sum())
+    rank = n_kept * (4 * V + 8 * L + 16)           # read each kept frame row, write its ranked list
+    select = 0 if w.blank_threshold >= 1.0 else n_valid * 32   # one sector per frame for the blank test
+    state = n_kept * beam * 20                      # (pb, pnb, score, last, len) per hypothesis per step
+    return dict(rank=rank, select=select, state=state, decode=n_kept * 4 * V + select + state)
+
+
+def traffic_record(kernel: str):
+    """ncu DRAM bytes per launch from profiles/traffic.json when it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        rec = d.get(kernel)
+        if rec and rec.get("sources_sha") == sources_sha():
+            return rec.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ctc_prefix_beam_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(a, w, rank, world):
+    if rank != 0:
+        return
+    import oracle as O
+    O.lib()
+    lp, lens = synth.gen_batch(w, pad="zero")
+    cores = os.cpu_count() or 1
+    T = lp.shape[1]
+
+    def one():
+        t0 = time.perf_counter()
+        O.decode(lp, lens, beam=w.beam, nbest=w.nbest, blank=w.blank_id,
+                 cap=w.max_seq_len if w.max_seq_len > 0 else T, thr=w.blank_threshold, threads=cores)
+        return time.perf_counter() - t0
+
+    for _ in range(a.warmup):
+        one()
+    ts = [one() for _ in range(a.steps)]
+    ms = 1e3 * statistics.mean(ts)
+    v = w.B * w.T / (ms / 1e3)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "frames/s", "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} T={w.T} V={w.V} beam={w.beam} nbest={w.nbest} offline",
+                   "l2": "n/a (host)"},
+        "cpu_baseline": {"value": v, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                         "sample": f"whole {w.name} batch per step on {cores} host threads"},
+        "e2e": {"value": v, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def main():
+    a = args_()
+    w = synth.WORKLOADS[a.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if a.impl == "reference":
+        return run_reference(a, w, rank, world)
+
+    import torch
+    from ctc_prefix_beam_gb300 import build as B
+    from ctc_prefix_beam_gb300 import decoder as D
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    B.build()
+    D.lib()
+
+    # rank r decodes its own batch (row seeds offset by rank)
+    wr = synth.workload(w.name, seed=w.seed + rank)
+    lp_np, lens_np = synth.gen_batch(wr, pad="zero")
+    Bn, T, V = lp_np.shape
+    cfg = D.Config(beam=w.beam, nbest=w.nbest, blank_id=w.blank_id, max_seq_len=w.max_seq_len,
+                   blank_threshold=w.blank_threshold, paged=bool(w.paged), page_size=w.page_size)
+    L = D.list_len(cfg, V)
+    lp_host = torch.from_numpy(lp_np).pin_memory()
+    lens_host = torch.from_numpy(lens_np).pin_memory()
+    lp = lp_host.to(dev)
+    lens = lens_host.to(dev)
+    ws = torch.empty(D.workspace_size(cfg, Bn, T, V), dtype=torch.uint8, device=dev)
+    out_len = min(w.max_seq_len, T) if w.max_seq_len > 0 else T
+    outs = (torch.empty((Bn, w.nbest, out_len), dtype=torch.int32, device=dev),
+            torch.empty((Bn, w.nbest), dtype=torch.int32, device=dev),
+            torch.empty((Bn, w.nbest), dtype=torch.float32, device=dev))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def decode(stages=D.STAGE_ALL):
+        D.decode_offline(cfg, lp, lens, workspace=ws, outputs=outs, out_len=out_len, stages=stages)
+
+    for _ in range(max(3, a.warmup)):
+        decode()
+    torch.cuda.synchronize(dev)
+
+    # kept frames (for the byte count), from the decoder's own selection stage
+    sel, nsel = D.select_frames(cfg, lp, lens)
+    kept = nsel.cpu().numpy()
+    stages = [("init", D.STAGE_INIT), ("select", D.STAGE_SELECT), ("rank", D.STAGE_RANK),
+              ("steps", D.STAGE_STEPS), ("output", D.STAGE_OUTPUT)]
+    kernel_of = {"init": "k_init", "select": "k_select", "rank": "k_prepass", "steps": "k_step", "output": "k_output"}
+    per_stage = {n: [] for n, _ in stages}
+    totals = []
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with Clocks(local, enabled=not a.no_clocks and rank == 0) as clk:
+        for _ in range(a.steps):
+            flush.fill_(1.0)  # evict the inputs from L2 between steps (outside the timed region)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+            ev[0].record(stream)
+            for i, (n, m) in enumerate(stages):
+                decode(m)
+                ev[i + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            for i, (n, m) in enumerate(stages):
+                per_stage[n].append(ev[i].elapsed_time(ev[i + 1]))
+            totals.append(ev[0].elapsed_time(ev[-1]))
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(totals)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public call with host buffers
+    out_host = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs)
+    h2d = lp_host.numel() * 4 + lens_host.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    e2e_ms = []
+    for i in range(a.steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        lp.copy_(lp_host, non_blocking=True)
+        lens.copy_(lens_host, non_blocking=True)
+        decode()
+        for oh, od in zip(out_host, outs):
+            oh.copy_(od, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e = statistics.mean(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    frames = world * Bn * T
+    valid = world * int(np.minimum(lens_np, T).sum())
+    peak, peak_kind = peaks()
+    by = algorithmic_bytes(w, lp_np, lens_np, kept, L)
+    stage_ms = {n: statistics.mean(v) for n, v in per_stage.items()}
+    dom = max(stage_ms, key=stage_ms.get)
+    dom_bytes = {"rank": by["rank"], "select": by["select"], "steps": by["state"], "init": 0,
+                 "output": 0}[dom]
+    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+    decode_gbs = by["decode"] / (ms / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": frames / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={Bn} T={T} V={V} beam={w.beam} nbest={w.nbest} offline, "
+                               f"lengths U[250,500], peaky logits",
+                   "l2": "flushed between steps (2x L2 write)", "parallelism": f"rows x{world}"},
+        "valid_frames_per_s": valid / (ms / 1e3),
+        "stage_ms": stage_ms,
+        "roofline": {"kernel": kernel_of[dom], "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic_record(kernel_of[dom]),
+                     "peak_kind": peak_kind},
+        "decode_roofline": {"achieved": decode_gbs, "peak": peak, "unit": "GB/s", "frac": decode_gbs / peak,
+                            "bytes_per_step": by["decode"], "peak_kind": peak_kind},
+        "e2e": {"value": frames / (e2e / 1e3), "unit": "frames/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": a.steps * len(stages),
+        "clocks": clk.summary(),
+    }
+    if not a.no_cpu_baseline and world == 1:
+        import oracle as O
+        O.lib()
+        cores = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        O.decode(lp_np, lens_np, beam=w.beam, nbest=w.nbest, blank=w.blank_id,
+                 cap=w.max_seq_len if w.max_seq_len > 0 else T, thr=w.blank_threshold, threads=cores)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": Bn * T / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                               "sample": f"whole {w.name} batch (B={Bn}) once, {cores} threads, {dt:.2f} s"}
+    print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

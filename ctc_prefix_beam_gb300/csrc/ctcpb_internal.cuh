@@ -1,0 +1,270 @@
+// Internal definitions of the GB300 CTC prefix beam search decoder:
+// workspace/state layout (host + device) and the float32 arithmetic.
+#pragma once
+
+#include <cfloat>
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "ctcpb.h"
+
+namespace ctcpb {
+
+typedef unsigned long long u64;
+typedef unsigned int u32;
+
+constexpr int kMaxBeam = 128;                 // section 11: beam 1..128
+constexpr int kMaxList = 2 * kMaxBeam + 2;    // section 3.4.6: K_all <= 2*beam+2
+constexpr int kMaxV = 1 << 20;                // labels fit the 20-bit token field of a rank key
+constexpr int kStreamTile = 64;               // frames ranked per pre-pass tile when streaming
+constexpr int kStreamDefaultCap = 4096;       // section 11: STREAMING_MAX_SEQ_LEN
+constexpr u32 kMagic = 0x42504354u;           // "TCPB"
+constexpr u32 kVersion = 1u;
+
+// ---------------------------------------------------------------- layout
+//
+// One "decode state" serves both the offline workspace (tile = T, one record
+// per decoded step) and a streaming state (tile = kStreamTile, records reused
+// per chunk tile).  Every slab is 256-byte aligned; offsets are from the base.
+struct Header {
+  u32 magic, version;
+  int32_t B, V, beam, cap, paged, page_size, blank, list_len, tile, pad0;
+  u32 status;  // CTCPB_DEV_* bits
+  u32 pad1[51];
+};
+static_assert(sizeof(Header) == 256, "header is 256 bytes");
+
+struct RowHdr {
+  int32_t step;    // decode steps done (0: the row has not decoded a frame yet)
+  int32_t tcount;  // frames consumed (streaming) -- the next frame index
+  int32_t t_prev;  // frame index of the last decoded step (-1 before the first)
+  int32_t nlive;   // live hypotheses in slots [0, nlive)
+  int32_t parity;  // token buffer holding the current hypotheses
+  int32_t pad[3];
+};
+
+struct Layout {
+  int B, V, beam, cap, paged, page_size, blank, L, Lpad, tile;
+  int ldseq;   // flat: labels per hypothesis row
+  int max_lp;  // paged: logical pages per hypothesis
+  int ppr;     // paged: physical pages per row
+  int T_sel;   // offline: frames per row of the selection list (0 when streaming)
+  size_t rec_bytes;
+  size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp;
+  size_t o_clist, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;
+  size_t o_recs, o_sel, o_nsel, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int default_list_len(int beam, int V, int list_len) {
+  int L = list_len > 0 ? list_len : 2 * beam + 2;
+  if (L > V - 1) L = V - 1;
+  if (L > kMaxList) L = kMaxList;
+  return L < 1 ? 1 : L;
+}
+
+// Build the layout.  tile = records per row; T_sel = selection list length
+// (offline T, 0 when streaming).
+inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_size, int blank, int L,
+                          int tile, int T_sel) {
+  Layout o{};
+  o.B = B; o.V = V; o.beam = beam; o.cap = cap; o.paged = paged; o.page_size = page_size;
+  o.blank = blank; o.L = L; o.Lpad = (int)align_up((size_t)L, 4); o.tile = tile; o.T_sel = T_sel;
+  o.ldseq = (int)align_up((size_t)cap, 16);
+  o.max_lp = paged ? (cap + page_size - 1) / page_size : 0;
+  o.ppr = paged ? beam * (o.max_lp + 1) : 0;
+  o.rec_bytes = align_up(32 + 8 * (size_t)o.Lpad, 32);
+  const size_t A = 256;
+  size_t off = sizeof(Header);
+  auto take = [&](size_t bytes) { size_t at = align_up(off, A); off = at + bytes; return at; };
+  const size_t nb = (size_t)B * beam;
+  o.o_rows = take(sizeof(RowHdr) * (size_t)B);
+  o.o_pb = take(4 * nb);
+  o.o_pnb = take(4 * nb);
+  o.o_sc = take(4 * nb);
+  o.o_last = take(4 * nb);
+  o.o_len = take(4 * nb);
+  o.o_h = take(8 * nb);
+  o.o_hp = take(8 * nb);
+  if (!paged) {
+    o.o_clist = take(4 * 2 * nb * (size_t)o.ldseq);
+  } else {
+    o.o_pages = take(4 * (size_t)B * o.ppr * (size_t)page_size);
+    o.o_btab = take(4 * 2 * nb * (size_t)o.max_lp);
+    o.o_refc = take(4 * (size_t)B * o.ppr);
+    o.o_pool = take(4 * (size_t)B * o.ppr);
+    o.o_ptop = take(4 * (size_t)B);
+    o.o_pnext = take(4 * (size_t)B);
+  }
+  o.o_recs = take(o.rec_bytes * (size_t)B * tile);
+  if (T_sel > 0) {
+    o.o_sel = take(4 * (size_t)B * T_sel);
+    o.o_nsel = take(4 * (size_t)B);
+  }
+  o.total = align_up(off, A);
+  return o;
+}
+
+// Typed views of a state buffer.
+struct View {
+  char* base;
+  Layout lay;
+  __host__ __device__ Header* hdr() const { return (Header*)base; }
+  __host__ __device__ RowHdr* rows() const { return (RowHdr*)(base + lay.o_rows); }
+  __host__ __device__ float* pb() const { return (float*)(base + lay.o_pb); }
+  __host__ __device__ float* pnb() const { return (float*)(base + lay.o_pnb); }
+  __host__ __device__ float* sc() const { return (float*)(base + lay.o_sc); }
+  __host__ __device__ int* last() const { return (int*)(base + lay.o_last); }
+  __host__ __device__ int* len() const { return (int*)(base + lay.o_len); }
+  __host__ __device__ u64* h() const { return (u64*)(base + lay.o_h); }
+  __host__ __device__ u64* hp() const { return (u64*)(base + lay.o_hp); }
+  // flat token rows: clist[par][b][k][ldseq]
+  __host__ __device__ int* clist(int par, int b, int k) const {
+    return (int*)(base + lay.o_clist) + (((size_t)par * lay.B + b) * lay.beam + k) * (size_t)lay.ldseq;
+  }
+  // paged storage, per-row partitions of ppr pages
+  __host__ __device__ int* page(int b, int phys) const {
+    return (int*)(base + lay.o_pages) + ((size_t)b * lay.ppr + phys) * (size_t)lay.page_size;
+  }
+  __host__ __device__ int* btab(int par, int b, int k) const {
+    return (int*)(base + lay.o_btab) + (((size_t)par * lay.B + b) * lay.beam + k) * (size_t)lay.max_lp;
+  }
+  __host__ __device__ int* refc(int b) const { return (int*)(base + lay.o_refc) + (size_t)b * lay.ppr; }
+  __host__ __device__ int* pool(int b) const { return (int*)(base + lay.o_pool) + (size_t)b * lay.ppr; }
+  __host__ __device__ int* ptop() const { return (int*)(base + lay.o_ptop); }
+  __host__ __device__ int* pnext() const { return (int*)(base + lay.o_pnext); }
+  // pre-pass records: rec(b, s)
+  __host__ __device__ char* rec(int b, int s) const {
+    return base + lay.o_recs + ((size_t)b * lay.tile + s) * lay.rec_bytes;
+  }
+  __host__ __device__ int* sel() const { return (int*)(base + lay.o_sel); }
+  __host__ __device__ int* nsel() const { return (int*)(base + lay.o_nsel); }
+};
+
+// Pre-pass record: one ranked frame.
+struct RecHdr {
+  int32_t cnt;       // labels in the list
+  int32_t front_id;  // first label after the list (-1: none live)
+  float lpb;         // blank log-prob
+  float front_lp;    // its log-prob (-FLT_MAX: none)
+  int32_t pad[4];
+};
+static_assert(sizeof(RecHdr) == 32, "record header is 32 bytes");
+__host__ __device__ inline int* rec_ids(char* r) { return (int*)(r + 32); }
+__host__ __device__ inline float* rec_lps(char* r, int Lpad) { return (float*)(r + 32 + 4 * (size_t)Lpad); }
+
+// ---------------------------------------------------------------- arithmetic
+//
+// The decoder's float32 log-semiring ("GPU CTC Prefix Beam Search Decoder",
+// section 3: logsumexp(a,b) = max + log(1 + exp(-|a-b|)), NEG_INF = -FLT_MAX),
+// written with explicit round-to-nearest intrinsics so nothing is contracted.
+//   dexp(x)   exp(x) for x <= 0: x = n*ln2 + r by Cody-Waite reduction
+//             (ln2 = HI + LO, HI with 16 significant bits so n*HI is exact),
+//             e^r by its degree-7 Taylor polynomial, times 2^n; 0 below -87.
+//   dlog1p(x) log(1+x) for x in [0,1] as 2*atanh(s), s = x/(2+x), through
+//             the odd series to s^13; above sqrt(2)-1 it evaluates
+//             ln2 + 2*atanh((x-1)/(x+3)) instead.
+//   dlse      max(a,b) + dlog1p(dexp(-|a-b|)).
+//   dadd      max(a+b, NEG): a product of probabilities, clamped to NEG.
+#define CTCPB_NEG (-FLT_MAX)
+
+__device__ __forceinline__ float dexp(float x) {
+  const float LN2_HI = 0.693145751953125f;
+  const float LN2_LO = 1.42860682030941723212e-6f;
+  const float LOG2E = 1.44269504088896340736f;
+  if (!(x >= -87.0f)) return 0.0f;
+  float n = rintf(__fmul_rn(x, LOG2E));
+  float r = __fmaf_rn(n, -LN2_HI, x);
+  r = __fmaf_rn(n, -LN2_LO, r);
+  float p = (float)(1.0 / 5040.0);
+  p = __fmaf_rn(p, r, (float)(1.0 / 720.0));
+  p = __fmaf_rn(p, r, (float)(1.0 / 120.0));
+  p = __fmaf_rn(p, r, (float)(1.0 / 24.0));
+  p = __fmaf_rn(p, r, (float)(1.0 / 6.0));
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  int ni = (int)n;
+  return __fmul_rn(p, __uint_as_float((unsigned)(ni + 127) << 23));
+}
+
+__device__ __forceinline__ float dlog1p(float x) {
+  const float LN2_HI = 0.693145751953125f;
+  const float LN2_LO = 1.42860682030941723212e-6f;
+  const bool lo_half = x <= 0.41421356237309504880f;
+  float num = lo_half ? x : __fsub_rn(x, 1.0f);
+  float den = lo_half ? __fadd_rn(2.0f, x) : __fadd_rn(x, 3.0f);
+  float hi = lo_half ? 0.0f : LN2_HI;
+  float lo = lo_half ? 0.0f : LN2_LO;
+  float s = __fdiv_rn(num, den);
+  float z = __fmul_rn(s, s);
+  float q = (float)(1.0 / 13.0);
+  q = __fmaf_rn(q, z, (float)(1.0 / 11.0));
+  q = __fmaf_rn(q, z, (float)(1.0 / 9.0));
+  q = __fmaf_rn(q, z, (float)(1.0 / 7.0));
+  q = __fmaf_rn(q, z, (float)(1.0 / 5.0));
+  q = __fmaf_rn(q, z, (float)(1.0 / 3.0));
+  float w = __fmul_rn(z, q);
+  float t2 = __fadd_rn(s, s);
+  float r = __fmaf_rn(t2, w, t2);
+  return __fadd_rn(__fadd_rn(r, lo), hi);
+}
+
+__device__ __forceinline__ float dlse(float a, float b) {
+  float m = fmaxf(a, b);
+  float d = fabsf(__fsub_rn(a, b));
+  return __fadd_rn(m, dlog1p(dexp(-d)));
+}
+
+__device__ __forceinline__ float dadd(float a, float b) { return fmaxf(__fadd_rn(a, b), CTCPB_NEG); }
+
+// Read a log-prob: NaN and -inf become NEG, -0 becomes +0.
+__device__ __forceinline__ float rdlp(float raw) { return __fadd_rn(fmaxf(raw, CTCPB_NEG), 0.0f); }
+
+// Order-preserving unsigned image of a float (larger float -> larger key).
+__host__ __device__ __forceinline__ u32 fkey(float f) {
+#ifdef __CUDA_ARCH__
+  u32 u = __float_as_uint(f);
+#else
+  u32 u;
+  memcpy(&u, &f, 4);
+#endif
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(u32 k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Rank key of a pre-pass label: larger = (higher log-prob, then smaller id).
+// 0 marks "not a live label".
+__device__ __forceinline__ u64 lab_key(float lp, int c) {
+  return ((u64)fkey(lp) << 32) | (u32)(~(u32)c);
+}
+
+// Rank key of a step candidate: larger = (higher score, then smaller source
+// slot, then smaller token); 0 marks a dead candidate.
+__device__ __forceinline__ u64 cand_key(float score, int src, int tok) {
+  return ((u64)fkey(score) << 32) | (u32)(~(((u32)src << 20) | (u32)tok));
+}
+__device__ __forceinline__ float ck_score(u64 k) { return fkey_inv((u32)(k >> 32)); }
+__device__ __forceinline__ int ck_src(u64 k) { return (int)((~(u32)k) >> 20); }
+__device__ __forceinline__ int ck_tok(u64 k) { return (int)((~(u32)k) & 0xfffffu); }
+
+// Prefix hash: h(empty) = kH0, h(l + c) = mix(h(l), c).  Used only to find
+// candidate pairs for the exact prefix comparison of section 3.4.3.
+constexpr u64 kH0 = 0x6a09e667f3bcc909ull;
+__device__ __forceinline__ u64 hmix(u64 h, int c) {
+  u64 x = h ^ ((u64)(u32)c * 0x9e3779b97f4a7c15ull + 0x632be59bd9b4e019ull);
+  x ^= x >> 30;
+  x *= 0xbf58476d1ce4e5b9ull;
+  x ^= x >> 27;
+  x *= 0x94d049bb133111ebull;
+  x ^= x >> 31;
+  return x;
+}
+
+}  // namespace ctcpb

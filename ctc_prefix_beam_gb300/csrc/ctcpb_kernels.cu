@@ -1,0 +1,953 @@
+// Kernels of the GB300 CTC prefix beam search decoder.
+//
+// Paths follow "GPU CTC Prefix Beam Search Decoder" (OASR docs):
+//   k_init      state reset (section 3.7's memsets, section 8's init)
+//   k_select    frame selection by blank threshold, ordered compaction (3.5)
+//   k_prepass   per-frame vocabulary ranking, hoisted out of the serial loop
+//               (3.4.7): the first L non-blank labels by (lp desc, id asc)
+//   k_step      one block per row: step-0 seeding (3.3), extension scoring
+//               (3.4.1-3.4.2), prefix merge (3.4.3), top-beam selection
+//               (3.4.4-3.4.5 / 3.4.6) and the token store update (flat
+//               double-buffered rows or paged prefix-shared pages, 3.4.5, 4.2)
+//   k_output    N-best gather (3.6)
+#include <cstdio>
+#include <cstring>
+
+#include "ctcpb_internal.cuh"
+#include "ctcpb_kernels.h"
+
+namespace ctcpb {
+
+#define FULL 0xffffffffu
+
+// ------------------------------------------------------------------ helpers
+
+template <int NT>
+__device__ __forceinline__ void gsync() {
+  if (NT == 32)
+    __syncwarp();
+  else
+    __syncthreads();
+}
+
+template <int NT>
+__device__ __forceinline__ bool g_any(bool p) {
+  if (NT == 32) {
+    return __any_sync(FULL, p);
+  } else {
+    return __syncthreads_or(p) != 0;
+  }
+}
+
+// Bitonic sort (descending) of P keys, P a power of two, by a group of NT
+// threads (a warp when NT == 32).  Ends with a group barrier.
+template <int NT>
+__device__ void bitonic_desc(u64* a, int P, int tid) {
+  for (int k = 2; k <= P; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P; i += NT) {
+        int ixj = i ^ j;
+        if (ixj > i) {
+          u64 x = a[i], y = a[ixj];
+          bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            a[i] = y;
+            a[ixj] = x;
+          }
+        }
+      }
+      gsync<NT>();
+    }
+}
+
+__device__ __forceinline__ u64 warp_max_u64(u64 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    u64 w = __shfl_xor_sync(FULL, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+
+__device__ __forceinline__ int pow2_at_least(int n, int lo) {
+  int p = lo;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+__device__ __forceinline__ void set_status(const View& st, u32 bit) { atomicOr(&st.hdr()->status, bit); }
+
+// ------------------------------------------------------------------ init
+
+__global__ void k_init(View st) {
+  const Layout& L = st.lay;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t nthr = (size_t)gridDim.x * blockDim.x;
+  if (tid == 0) {
+    Header* h = st.hdr();
+    h->magic = kMagic;
+    h->version = kVersion;
+    h->B = L.B; h->V = L.V; h->beam = L.beam; h->cap = L.cap; h->paged = L.paged;
+    h->page_size = L.page_size; h->blank = L.blank; h->list_len = L.L; h->tile = L.tile;
+    h->status = 0u;
+  }
+  for (size_t b = tid; b < (size_t)L.B; b += nthr) {
+    RowHdr r;
+    r.step = 0; r.tcount = 0; r.t_prev = -1; r.nlive = 0; r.parity = 0;
+    r.pad[0] = r.pad[1] = r.pad[2] = 0;
+    st.rows()[b] = r;
+    if (L.paged) {
+      st.ptop()[b] = 0;
+      st.pnext()[b] = 0;
+    }
+  }
+  if (L.paged) {
+    const size_t nt = 2 * (size_t)L.B * L.beam * L.max_lp;
+    int* bt = (int*)(st.base + L.o_btab);
+    for (size_t i = tid; i < nt; i += nthr) bt[i] = -1;
+    const size_t np = (size_t)L.B * L.ppr;
+    int* rc = (int*)(st.base + L.o_refc);
+    for (size_t i = tid; i < np; i += nthr) rc[i] = 0;
+  }
+}
+
+// ------------------------------------------------------------------ select
+// Section 3.5: keep t < len_b iff lp[b,t,blank] < log_thr (mode 1), all
+// frames (mode 0) or none (mode 2); ordered compaction with warp ballots.
+__global__ void __launch_bounds__(256) k_select(View st, const float* __restrict__ lp, long long sb, long long stt,
+                                                const int* __restrict__ lens, int T, int mode, float log_thr,
+                                                int* __restrict__ sel, int* __restrict__ nsel) {
+  __shared__ int wcount[8];
+  __shared__ int base_s;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int len_b = lens ? lens[b] : T;
+  len_b = len_b < 0 ? 0 : (len_b > T ? T : len_b);
+  const int blank = st.lay.blank;
+  if (tid == 0) base_s = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += 256) {
+    const int t = t0 + tid;
+    bool keep = false;
+    if (t < len_b) {
+      if (mode == 0)
+        keep = true;
+      else if (mode == 1)
+        keep = rdlp(lp[(long long)b * sb + (long long)t * stt + blank]) < log_thr;
+    }
+    unsigned m = __ballot_sync(FULL, keep);
+    if (lane == 0) wcount[wid] = __popc(m);
+    __syncthreads();
+    int off = base_s;
+    for (int w = 0; w < wid; ++w) off += wcount[w];
+    if (keep) sel[(size_t)b * T + off + __popc(m & ((1u << lane) - 1u))] = t;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < 8; ++w) tot += wcount[w];
+      base_s += tot;
+    }
+    __syncthreads();
+  }
+  const int n = base_s;
+  for (int i = n + tid; i < T; i += 256) sel[(size_t)b * T + i] = -1;
+  if (tid == 0) nsel[b] = n;
+}
+
+// ------------------------------------------------------------------ pre-pass
+// Rank one frame row by one warp: the first L live non-blank labels by
+// (lp desc, id asc), the blank log-prob and the label after the list.
+//
+// Exact top-(L+1) selection:
+//   1. each lane keeps its top-2 label keys over labels lane, lane+32, ...;
+//   2. the (L+1)-th largest of these 64 keys is a lower bound tau of the
+//      (L+1)-th largest key of the row (they are distinct labels);
+//   3. every label with key >= tau is compacted into shared memory and the
+//      compacted set is sorted; it contains the top L+1 by construction;
+//   4. if the compacted set would overflow `lcap`, the warp falls back to
+//      L+1 rounds of "largest key below the previous one".
+constexpr int kRankCap = 512;  // shared keys per ranking warp
+
+__device__ __forceinline__ u64 label_key_at(const float* __restrict__ row, int c, int V, int blank) {
+  if (c >= V || c == blank) return 0ull;
+  float v = rdlp(row[c]);
+  return v > CTCPB_NEG ? lab_key(v, c) : 0ull;
+}
+
+__device__ void rank_row(const float* __restrict__ row, int V, int blank, int L, u64* buf, int lane,
+                         int* o_ids, float* o_lps, int* o_cnt, float* o_lpb, float* o_flp, int* o_fid) {
+  const int K = L + 1;
+  u64 tau = 0ull;
+  if (K <= 64) {
+    u64 k1 = 0ull, k2 = 0ull;
+    for (int c = lane; c < V; c += 32) {
+      u64 key = label_key_at(row, c, V, blank);
+      if (key > k2) {
+        if (key > k1) {
+          k2 = k1;
+          k1 = key;
+        } else {
+          k2 = key;
+        }
+      }
+    }
+    buf[lane] = k1;
+    buf[lane + 32] = k2;
+    __syncwarp();
+    bitonic_desc<32>(buf, 64, lane);
+    tau = buf[K - 1];
+    __syncwarp();
+  }
+  int n = 0;
+  bool ovf = false;
+  for (int c0 = 0; c0 < V; c0 += 32) {
+    const int c = c0 + lane;
+    u64 key = label_key_at(row, c, V, blank);
+    bool take = key != 0ull && key >= tau;
+    unsigned m = __ballot_sync(FULL, take);
+    int tot = __popc(m);
+    if (n + tot > kRankCap) {
+      ovf = true;
+      break;
+    }
+    if (take) buf[n + __popc(m & ((1u << lane) - 1u))] = key;
+    n += tot;
+  }
+  __syncwarp();
+  if (!ovf) {
+    const int P = pow2_at_least(n, 32);
+    for (int i = n + lane; i < P; i += 32) buf[i] = 0ull;
+    __syncwarp();
+    bitonic_desc<32>(buf, P, lane);
+  } else {
+    u64 prev = ~0ull;
+    n = 0;
+    for (int r = 0; r < K; ++r) {
+      u64 best = 0ull;
+      for (int c = lane; c < V; c += 32) {
+        u64 key = label_key_at(row, c, V, blank);
+        if (key < prev && key > best) best = key;
+      }
+      best = warp_max_u64(best);
+      if (best == 0ull) break;
+      if (lane == 0) buf[r] = best;
+      prev = best;
+      n = r + 1;
+    }
+    __syncwarp();
+  }
+  const int cnt = n < L ? n : L;
+  for (int i = lane; i < L; i += 32) {
+    if (i < cnt) {
+      u64 kk = buf[i];
+      o_ids[i] = (int)(~(u32)kk);
+      o_lps[i] = fkey_inv((u32)(kk >> 32));
+    } else {
+      o_ids[i] = -1;
+      o_lps[i] = CTCPB_NEG;
+    }
+  }
+  if (lane == 0) {
+    *o_cnt = cnt;
+    *o_lpb = rdlp(row[blank]);
+    if (n > L) {
+      *o_flp = fkey_inv((u32)(buf[L] >> 32));
+      *o_fid = (int)(~(u32)buf[L]);
+    } else {
+      *o_flp = CTCPB_NEG;
+      *o_fid = -1;
+    }
+  }
+  __syncwarp();
+}
+
+// Records for the decode: item (b, s) ranks the frame of row b's step s.
+// mode 0 (offline): frame sel[b][s], s < nsel[b].
+// mode 1 (streaming): chunk row tile_start + s, s < frames of row b in the tile.
+__global__ void __launch_bounds__(256) k_prepass(View st, const float* __restrict__ lp, long long sb, long long stt,
+                                                 int mode, const int* __restrict__ nframes, int chunk_T,
+                                                 int tile_start, int tile_len) {
+  __shared__ u64 bufs[8][kRankCap];
+  const Layout& Ly = st.lay;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  const long long gw = (long long)blockIdx.x * nw + wid;
+  const long long tw = (long long)gridDim.x * nw;
+  const long long items = (long long)Ly.B * tile_len;
+  for (long long it = gw; it < items; it += tw) {
+    const int b = (int)(it % Ly.B);
+    const int s = (int)(it / Ly.B);
+    const float* row;
+    if (mode == 0) {
+      if (s >= st.nsel()[b]) continue;
+      const int t = st.sel()[(size_t)b * Ly.T_sel + s];
+      row = lp + (long long)b * sb + (long long)t * stt;
+    } else {
+      int nf = nframes ? nframes[b] : chunk_T;
+      nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
+      if (tile_start + s >= nf) continue;
+      row = lp + (long long)b * sb + (long long)(tile_start + s) * stt;
+    }
+    char* r = st.rec(b, s);
+    RecHdr* h = (RecHdr*)r;
+    rank_row(row, Ly.V, Ly.blank, Ly.L, bufs[wid], lane, rec_ids(r), rec_lps(r, Ly.Lpad), &h->cnt, &h->lpb,
+             &h->front_lp, &h->front_id);
+  }
+}
+
+// Stand-alone pre-pass over R rows (the ctcpb_topk_prepass entry point).
+__global__ void __launch_bounds__(256) k_prepass_rows(const float* __restrict__ lp, long long stride_r, int R, int V,
+                                                      int blank, int L, int* ids, float* lps, int* cnt, float* lpb,
+                                                      float* flp, int* fid) {
+  __shared__ u64 bufs[8][kRankCap];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  for (long long r = (long long)blockIdx.x * nw + wid; r < R; r += (long long)gridDim.x * nw) {
+    rank_row(lp + r * stride_r, V, blank, L, bufs[wid], lane, ids + r * L, lps + r * L, cnt + r, lpb + r, flp + r,
+             fid + r);
+  }
+}
+
+// ------------------------------------------------------------------ step
+//
+// One block of NT threads owns one row for the whole call.  The beam state of
+// the row lives in shared memory between steps; tokens live in the state
+// buffer (flat rows or pages).
+template <int NT>
+struct StepSmem {
+  // current hypotheses, slot order
+  float pb[NT], pnb[NT], sc[NT];
+  int last[NT], len[NT];
+  u64 h[NT], hp[NT];
+  // per step
+  float A[NT], pbg[NT], lpl[NT], bpb[NT], bpnb[NT], rep[NT];
+  int into[NT], repdead[NT];
+  // next hypotheses
+  float npb[NT], npnb[NT], nsc[NT];
+  int nlast[NT], nlen[NT], nsrc[NT], ntok[NT];
+  u64 nh[NT], nhp[NT];
+  // the frame's ranked labels
+  int ids[kMaxList + 2];
+  float lps[kMaxList + 2];
+  u32 excl[NT][(kMaxList + 31) / 32];
+  int xu_k[NT], xu_c[NT];
+  int pi[2 * NT], pj[2 * NT];
+  int dfree[NT];
+  int cnt, front_id, nw, npairs, nxu, nkeys, ndfree;
+  float lpb, front_lp;
+};
+
+template <int NT>
+size_t step_smem_bytes(int sortcap) {
+  return align_up(sizeof(StepSmem<NT>), 16) + (size_t)sortcap * sizeof(u64);
+}
+
+struct TokenStore {
+  View st;
+  int b;
+  __device__ __forceinline__ int get(int par, int k, int x) const {
+    if (!st.lay.paged) return st.clist(par, b, k)[x];
+    const int ps = st.lay.page_size;
+    const int phys = st.btab(par, b, k)[x / ps];
+    return phys >= 0 ? st.page(b, phys)[x % ps] : -1;
+  }
+};
+
+// allocate one page of row b: LIFO pool first, then the bump pointer
+__device__ int page_alloc(const View& st, int b) {
+  int* top = st.ptop() + b;
+  int cur = *((volatile int*)top);
+  if (cur > st.lay.ppr) {
+    set_status(st, CTCPB_DEV_OVERFLOW);
+    return -1;
+  }
+  while (cur > 0) {
+    int prev = atomicCAS(top, cur, cur - 1);
+    if (prev == cur) return st.pool(b)[cur - 1];
+    cur = prev;
+  }
+  int phys = atomicAdd(st.pnext() + b, 1);
+  if (phys >= st.lay.ppr) {
+    set_status(st, CTCPB_DEV_PAGES);
+    return -1;
+  }
+  return phys;
+}
+
+__device__ __forceinline__ void page_push(const View& st, int b, int phys) {
+  int pos = atomicAdd(st.ptop() + b, 1);
+  if (pos < st.lay.ppr)
+    st.pool(b)[pos] = phys;
+  else
+    set_status(st, CTCPB_DEV_OVERFLOW);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ lp, long long sb, long long stt,
+                                             int mode, const int* __restrict__ nframes, int chunk_T,
+                                             int tile_start, int tile_len, int sortcap) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  StepSmem<NT>& S = *reinterpret_cast<StepSmem<NT>*>(smem_raw);
+  u64* keys = reinterpret_cast<u64*>(smem_raw + align_up(sizeof(StepSmem<NT>), 16));
+  const Layout& Ly = st.lay;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V;
+  const float NEG = CTCPB_NEG;
+
+  if (mode == 1) {
+    const Header* hd = st.hdr();
+    bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
+              hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
+              hd->page_size == Ly.page_size && hd->blank == Ly.blank && hd->list_len == Ly.L &&
+              hd->tile == Ly.tile;
+    if (!ok) {
+      if (tid == 0) set_status(st, CTCPB_DEV_HEADER);
+      return;
+    }
+  }
+
+  RowHdr* rh = st.rows() + b;
+  int nsteps;
+  if (mode == 0) {
+    nsteps = st.nsel()[b];
+  } else {
+    int nf = nframes ? nframes[b] : chunk_T;
+    nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
+    nsteps = nf - tile_start;
+    nsteps = nsteps < 0 ? 0 : (nsteps > tile_len ? tile_len : nsteps);
+  }
+  if (nsteps == 0) return;
+
+  int step = rh->step, tcount = rh->tcount, t_prev = rh->t_prev, nlive = rh->nlive, par = rh->parity;
+  const size_t rb = (size_t)b * beam;
+  for (int k = tid; k < beam; k += NT) {
+    S.pb[k] = st.pb()[rb + k];
+    S.pnb[k] = st.pnb()[rb + k];
+    S.sc[k] = st.sc()[rb + k];
+    S.last[k] = st.last()[rb + k];
+    S.len[k] = st.len()[rb + k];
+    S.h[k] = st.h()[rb + k];
+    S.hp[k] = st.hp()[rb + k];
+  }
+  TokenStore tok{st, b};
+  const int M = sortcap - NT;  // candidates per selection chunk
+
+  for (int s = 0; s < nsteps; ++s) {
+    const int t = mode == 0 ? st.sel()[(size_t)b * Ly.T_sel + s] : tcount + s;
+    const float* row = lp + (long long)b * sb + (long long)(mode == 0 ? t : tile_start + s) * stt;
+    char* rec = st.rec(b, s);
+    {
+      const RecHdr* rhd = (const RecHdr*)rec;
+      const int cnt = rhd->cnt;
+      const int* rids = rec_ids(rec);
+      const float* rlps = rec_lps(rec, Ly.Lpad);
+      for (int i = tid; i < cnt; i += NT) {
+        S.ids[i] = rids[i];
+        S.lps[i] = rlps[i];
+      }
+      if (tid == 0) {
+        S.cnt = cnt;
+        S.front_id = rhd->front_id;
+        S.front_lp = rhd->front_lp;
+        S.lpb = rhd->lpb;
+      }
+    }
+    gsync<NT>();
+    const bool gap = t > t_prev + 1;
+    const int cnt = S.cnt;
+    const int np = par ^ 1;
+
+    if (step == 0) {
+      // ---- section 3.3: seed the top (beam-1) labels, then the empty prefix
+      const int nb = beam > 1 ? beam - 1 : 1;
+      const int ntok = cap >= 1 ? (nb < cnt ? nb : cnt) : 0;
+      const bool empty_live = beam > 1 && S.lpb > NEG;
+      for (int k = tid; k < beam; k += NT) {
+        if (k < ntok) {
+          const int c = S.ids[k];
+          const float v = S.lps[k];
+          S.npb[k] = gap ? v : NEG;
+          S.npnb[k] = gap ? NEG : v;
+          S.nsc[k] = v;
+          S.nlast[k] = c;
+          S.nlen[k] = 1;
+          S.nh[k] = hmix(kH0, c);
+          S.nhp[k] = kH0;
+          S.ntok[k] = c;
+          S.nsrc[k] = -1;
+        } else if (k == ntok && empty_live) {
+          S.npb[k] = S.lpb;
+          S.npnb[k] = NEG;
+          S.nsc[k] = S.lpb;
+          S.nlast[k] = blank;
+          S.nlen[k] = 0;
+          S.nh[k] = kH0;
+          S.nhp[k] = 0ull;
+          S.ntok[k] = blank;
+          S.nsrc[k] = -1;
+        }
+      }
+      if (tid == 0) S.nw = ntok + (empty_live ? 1 : 0);
+      gsync<NT>();
+      const int nw = S.nw;
+      if (!Ly.paged) {
+        for (int k = tid; k < ntok; k += NT) st.clist(np, b, k)[0] = S.ids[k];
+      } else {
+        for (int k = tid; k < nw; k += NT) {
+          int* bt = st.btab(np, b, k);
+          if (k < ntok) {
+            int phys = page_alloc(st, b);
+            if (phys >= 0) {
+              st.refc(b)[phys] = 1;
+              st.page(b, phys)[0] = S.ids[k];
+            }
+            bt[0] = phys;
+          }
+        }
+      }
+      gsync<NT>();
+    } else {
+      // ---- section 3.4: collapsed-blank correction, extension and blank slots
+      for (int k = tid; k < nlive; k += NT) {
+        float pb = S.pb[k], pnb = S.pnb[k];
+        if (gap) {
+          pb = dlse(pb, pnb);
+          pnb = NEG;
+        }
+        const float A = dlse(pb, pnb);
+        const int L = S.len[k];
+        const float lpl = L > 0 ? rdlp(row[S.last[k]]) : NEG;
+        S.A[k] = A;
+        S.pbg[k] = pb;
+        S.lpl[k] = lpl;
+        S.bpb[k] = dadd(S.lpb, A);
+        S.bpnb[k] = (L > 0 && !gap) ? dadd(lpl, pnb) : NEG;
+        S.rep[k] = (L > 0 && L < cap) ? dadd(lpl, pb) : NEG;
+        S.repdead[k] = 0;
+        S.into[k] = -1;
+        for (int w = 0; w < (kMaxList + 31) / 32; ++w) S.excl[k][w] = 0u;
+      }
+      if (tid == 0) {
+        S.npairs = 0;
+        S.nxu = 0;
+        S.nkeys = 0;
+      }
+      gsync<NT>();
+      // ---- section 3.4.3: pairs (i shorter, j longer) with l_j = l_i + last_j;
+      // the prefix hash proposes pairs, token comparison decides.
+      for (int j = tid; j < nlive; j += NT) {
+        for (int i = 0; i < nlive; ++i) {
+          if (S.len[j] == S.len[i] + 1 && S.hp[j] == S.h[i]) {
+            if (S.len[i] == 0) {
+              S.into[j] = i;
+            } else {
+              int p = atomicAdd(&S.npairs, 1);
+              if (p < 2 * NT) {
+                S.pi[p] = i;
+                S.pj[p] = j;
+              } else {
+                set_status(st, CTCPB_DEV_OVERFLOW);
+              }
+            }
+          }
+        }
+      }
+      gsync<NT>();
+      {
+        const int npairs = S.npairs < 2 * NT ? S.npairs : 2 * NT;
+        for (int p = 0; p < npairs; ++p) {
+          const int i = S.pi[p], j = S.pj[p];
+          const int Li = S.len[i];
+          bool mism = false;
+          for (int x = tid; x < Li; x += NT) mism |= tok.get(par, i, x) != tok.get(par, j, x);
+          const bool any = g_any<NT>(mism);
+          if (!any && tid == 0) S.into[j] = i;
+        }
+      }
+      gsync<NT>();
+      // fold (i, last_j) into j's blank slot; drop the folded candidate
+      for (int j = tid; j < nlive; j += NT) {
+        const int i = S.into[j];
+        if (i < 0) continue;
+        const int c = S.last[j];
+        const bool rep_i = S.len[i] > 0 && S.last[i] == c;
+        const float ext = rep_i ? dadd(S.lpl[j], S.pbg[i]) : dadd(S.lpl[j], S.A[i]);
+        S.bpnb[j] = dlse(S.bpnb[j], ext);
+        if (rep_i) {
+          S.repdead[i] = 1;
+        } else {
+          int p = -1;
+          for (int q = 0; q < cnt; ++q)
+            if (S.ids[q] == c) {
+              p = q;
+              break;
+            }
+          if (p >= 0) {
+            atomicOr(&S.excl[i][p >> 5], 1u << (p & 31));
+          } else {
+            int u = atomicAdd(&S.nxu, 1);
+            S.xu_k[u] = i;
+            S.xu_c[u] = c;
+          }
+        }
+      }
+      gsync<NT>();
+
+      // ---- sections 3.4.4-3.4.6: best `beam` candidates over
+      // {blank slot, repeat slot, listed labels} of every live hypothesis
+      const int stride = cnt + 2;
+      const int NC = nlive * stride;
+      for (int i = tid; i < NT; i += NT) keys[i] = 0ull;
+      for (int base = 0; base < NC; base += M) {
+        const int m = (NC - base) < M ? (NC - base) : M;
+        for (int x = tid; x < m; x += NT) {
+          const int g = base + x;
+          const int k = g / stride, r = g - k * stride;
+          u64 key = 0ull;
+          const int L = S.len[k];
+          if (r == 0) {
+            const float sc = dlse(S.bpb[k], S.bpnb[k]);
+            if (sc > NEG) key = cand_key(sc, k, blank);
+          } else if (r == 1) {
+            if (L > 0 && L < cap && !S.repdead[k] && S.rep[k] > NEG) key = cand_key(S.rep[k], k, S.last[k]);
+          } else {
+            const int p = r - 2;
+            const int c = S.ids[p];
+            if (L < cap && !(L > 0 && c == S.last[k]) && !((S.excl[k][p >> 5] >> (p & 31)) & 1u)) {
+              const float sc = dadd(S.lps[p], S.A[k]);
+              if (sc > NEG) key = cand_key(sc, k, c);
+            }
+          }
+          keys[NT + x] = key;
+        }
+        const int P = pow2_at_least(NT + m, 2 * NT);
+        for (int i = NT + m + tid; i < P; i += NT) keys[i] = 0ull;
+        gsync<NT>();
+        bitonic_desc<NT>(keys, P, tid);
+      }
+      int nw = 0;
+      for (int w = 0; w < beam; ++w) nw += keys[w] != 0ull;
+
+      // ---- the list proves the selection unless an unlisted label could
+      // reach the beam: then rank every unlisted label of this frame
+      if (S.front_lp > NEG) {
+        const u32 sstar = nw == beam ? (u32)(keys[beam - 1] >> 32) : 0u;
+        bool bad = false;
+        for (int k = tid; k < nlive; k += NT) {
+          if (S.len[k] < cap) {
+            const float u = dadd(S.front_lp, S.A[k]);
+            if (u > NEG && (nw < beam || fkey(u) >= sstar)) bad = true;
+          }
+        }
+        const bool need = g_any<NT>(bad);
+        if (need) {
+          const u64 thr = nw == beam ? (keys[beam - 1] & 0xffffffff00000000ull) : 0ull;
+          const u64 kfront = lab_key(S.front_lp, S.front_id);
+          const long long items = (long long)nlive * V;
+          for (long long base = 0; base < items; base += NT) {
+            const long long x = base + tid;
+            if (x < items) {
+              const int k = (int)(x / V), c = (int)(x - (long long)k * V);
+              const int L = S.len[k];
+              if (c != blank && L < cap && !(L > 0 && c == S.last[k])) {
+                const float v = rdlp(row[c]);
+                if (v > NEG && lab_key(v, c) <= kfront) {
+                  bool ex = false;
+                  for (int u = 0; u < S.nxu; ++u) ex |= (S.xu_k[u] == k && S.xu_c[u] == c);
+                  const float sc = dadd(v, S.A[k]);
+                  if (!ex && sc > NEG) {
+                    const u64 key = cand_key(sc, k, c);
+                    if (key >= thr) {
+                      int pos = atomicAdd(&S.nkeys, 1);
+                      keys[NT + pos] = key;
+                    }
+                  }
+                }
+              }
+            }
+            gsync<NT>();
+            const int nk = S.nkeys;
+            gsync<NT>();  // every thread has read nk before the next round adds to it
+            if (nk > M - NT || base + NT >= items) {
+              const int P = pow2_at_least(NT + nk, 2 * NT);
+              for (int i = NT + nk + tid; i < P; i += NT) keys[i] = 0ull;
+              gsync<NT>();
+              if (nk > 0) bitonic_desc<NT>(keys, P, tid);
+              if (tid == 0) S.nkeys = 0;
+              gsync<NT>();
+            }
+          }
+          nw = 0;
+          for (int w = 0; w < beam; ++w) nw += keys[w] != 0ull;
+        }
+      }
+
+      // ---- section 3.4.5: the winners become the next hypotheses
+      for (int w = tid; w < nw; w += NT) {
+        const u64 key = keys[w];
+        const float score = ck_score(key);
+        const int src = ck_src(key), tk = ck_tok(key);
+        if (tk == blank) {
+          S.npb[w] = S.bpb[src];
+          S.npnb[w] = S.bpnb[src];
+          S.nlast[w] = S.last[src];
+          S.nlen[w] = S.len[src];
+          S.nh[w] = S.h[src];
+          S.nhp[w] = S.hp[src];
+        } else {
+          S.npb[w] = NEG;
+          S.npnb[w] = score;
+          S.nlast[w] = tk;
+          S.nlen[w] = S.len[src] + 1;
+          S.nh[w] = hmix(S.h[src], tk);
+          S.nhp[w] = S.h[src];
+        }
+        if (gap) {
+          S.npb[w] = score;
+          S.npnb[w] = NEG;
+        }
+        S.nsc[w] = score;
+        S.nsrc[w] = src;
+        S.ntok[w] = tk;
+      }
+      if (tid == 0) {
+        S.nw = nw;
+        S.ndfree = 0;
+      }
+      gsync<NT>();
+
+      // ---- token store
+      if (!Ly.paged) {
+        for (int w = 0; w < nw; ++w) {
+          const int src = S.nsrc[w];
+          const int Ls = S.len[src];
+          const int* from = st.clist(par, b, src);
+          int* to = st.clist(np, b, w);
+          for (int x = tid; x < Ls; x += NT) to[x] = from[x];
+        }
+        for (int w = tid; w < nw; w += NT)
+          if (S.ntok[w] != blank) st.clist(np, b, w)[S.len[S.nsrc[w]]] = S.ntok[w];
+        gsync<NT>();
+      } else {
+        const int ps = Ly.page_size, mlp = Ly.max_lp;
+        int* refc = st.refc(b);
+        // fork, pass A: acquire the source pages of every winner
+        for (int w = 0; w < nw; ++w) {
+          const int src = S.nsrc[w];
+          const int npg = (S.len[src] + ps - 1) / ps;
+          const int* bs = st.btab(par, b, src);
+          for (int x = tid; x < npg; x += NT)
+            if (bs[x] >= 0) atomicAdd(&refc[bs[x]], 1);
+        }
+        gsync<NT>();
+        // fork, pass B: release what each destination slot held, install the
+        // source's pages
+        for (int w = tid; w < beam; w += NT) {
+          int* bd = st.btab(np, b, w);
+          for (int x = 0; x < mlp; ++x) {
+            const int phys = bd[x];
+            if (phys < 0) break;
+            if (atomicSub(&refc[phys], 1) == 1) page_push(st, b, phys);
+            bd[x] = -1;
+          }
+          if (w < nw) {
+            const int src = S.nsrc[w];
+            const int npg = (S.len[src] + ps - 1) / ps;
+            const int* bs = st.btab(par, b, src);
+            for (int x = 0; x < npg; ++x) bd[x] = bs[x];
+          }
+        }
+        gsync<NT>();
+        // append / copy-on-write; page releases here are deferred past the
+        // last allocation of the step
+        for (int w = tid; w < nw; w += NT) {
+          const int tk = S.ntok[w];
+          if (tk == blank) continue;
+          const int pos = S.len[S.nsrc[w]];
+          const int lpi = pos / ps, off = pos - lpi * ps;
+          int* bd = st.btab(np, b, w);
+          if (off == 0) {
+            const int phys = page_alloc(st, b);
+            if (phys >= 0) {
+              refc[phys] = 1;
+              st.page(b, phys)[0] = tk;
+            }
+            bd[lpi] = phys;
+          } else {
+            const int phys = bd[lpi];
+            if (phys < 0) continue;
+            if (atomicAdd(&refc[phys], 0) > 1) {
+              const int nph = page_alloc(st, b);
+              if (nph >= 0) {
+                const int* from = st.page(b, phys);
+                int* to = st.page(b, nph);
+                for (int x = 0; x < off; ++x) to[x] = from[x];
+                to[off] = tk;
+                refc[nph] = 1;
+                bd[lpi] = nph;
+                if (atomicSub(&refc[phys], 1) == 1) {
+                  int q = atomicAdd(&S.ndfree, 1);
+                  S.dfree[q] = phys;
+                }
+              }
+            } else {
+              st.page(b, phys)[off] = tk;
+            }
+          }
+        }
+        gsync<NT>();
+        for (int q = tid; q < S.ndfree; q += NT) page_push(st, b, S.dfree[q]);
+        gsync<NT>();
+      }
+    }
+
+    // ---- commit
+    const int nw = S.nw;
+    for (int k = tid; k < nw; k += NT) {
+      S.pb[k] = S.npb[k];
+      S.pnb[k] = S.npnb[k];
+      S.sc[k] = S.nsc[k];
+      S.last[k] = S.nlast[k];
+      S.len[k] = S.nlen[k];
+      S.h[k] = S.nh[k];
+      S.hp[k] = S.nhp[k];
+    }
+    gsync<NT>();
+    nlive = nw;
+    par = np;
+    t_prev = t;
+    ++step;
+  }
+
+  for (int k = tid; k < beam; k += NT) {
+    st.pb()[rb + k] = S.pb[k];
+    st.pnb()[rb + k] = S.pnb[k];
+    st.sc()[rb + k] = S.sc[k];
+    st.last()[rb + k] = S.last[k];
+    st.len()[rb + k] = S.len[k];
+    st.h()[rb + k] = S.h[k];
+    st.hp()[rb + k] = S.hp[k];
+  }
+  if (tid == 0) {
+    rh->step = step;
+    rh->tcount = mode == 1 ? tcount + nsteps : rh->tcount;
+    rh->t_prev = t_prev;
+    rh->nlive = nlive;
+    rh->parity = par;
+  }
+}
+
+// ------------------------------------------------------------------ output
+// Section 3.6: the first nbest hypotheses after a stable sort by score.
+__global__ void __launch_bounds__(128) k_output(View st, int nbest, int* __restrict__ out_tokens,
+                                                int* __restrict__ out_lengths, float* __restrict__ out_scores,
+                                                int out_len) {
+  __shared__ int order[kMaxBeam];
+  __shared__ float scs[kMaxBeam];
+  const Layout& Ly = st.lay;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const RowHdr rh = st.rows()[b];
+  const int beam = Ly.beam;
+  const bool never = rh.step == 0;
+  const int nlive = never ? 0 : rh.nlive;
+  for (int k = tid; k < nlive; k += blockDim.x) scs[k] = st.sc()[(size_t)b * beam + k];
+  __syncthreads();
+  for (int k = tid; k < nlive; k += blockDim.x) {
+    int r = 0;
+    const float v = scs[k];
+    for (int j = 0; j < nlive; ++j) r += (scs[j] > v) || (scs[j] == v && j < k);
+    order[r] = k;
+  }
+  __syncthreads();
+  TokenStore tok{st, b};
+  for (int n = 0; n < nbest; ++n) {
+    const size_t o = (size_t)b * nbest + n;
+    int* dst = out_tokens + o * (size_t)out_len;
+    if (n < nlive) {
+      const int k = order[n];
+      const int L = st.len()[(size_t)b * beam + k];
+      for (int x = tid; x < out_len; x += blockDim.x) dst[x] = x < L ? tok.get(rh.parity, k, x) : -1;
+      if (tid == 0) {
+        out_lengths[o] = L;
+        out_scores[o] = scs[k];
+      }
+    } else {
+      for (int x = tid; x < out_len; x += blockDim.x) dst[x] = -1;
+      if (tid == 0) {
+        const bool empty_row = never && n == 0;
+        out_lengths[o] = 0;
+        out_scores[o] = empty_row ? 0.0f : CTCPB_NEG;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+
+static int grid_for(long long items_per_warp_units, int warps_per_block) {
+  long long blocks = (items_per_warp_units + warps_per_block - 1) / warps_per_block;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long cap = (long long)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+cudaError_t launch_init(const View& st, cudaStream_t s) {
+  k_init<<<grid_for((long long)st.lay.B * st.lay.beam * 2 + 1, 8), 256, 0, s>>>(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
+                          int mode, float log_thr, int* sel, int* nsel, cudaStream_t s) {
+  if (st.lay.B == 0) return cudaSuccess;
+  k_select<<<st.lay.B, 256, 0, s>>>(st, lp, sb, stt, lens, T, mode, log_thr, sel, nsel);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepass(const View& st, const float* lp, long long sb, long long stt, int mode,
+                           const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  long long items = (long long)st.lay.B * tile_len;
+  if (items == 0) return cudaSuccess;
+  k_prepass<<<grid_for(items, 8), 256, 0, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepass_rows(const float* lp, long long stride_r, int R, int V, int blank, int L, int* ids,
+                                float* lps, int* cnt, float* lpb, float* flp, int* fid, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  k_prepass_rows<<<grid_for(R, 8), 256, 0, s>>>(lp, stride_r, R, V, blank, L, ids, lps, cnt, lpb, flp, fid);
+  return cudaGetLastError();
+}
+
+template <int NT>
+static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, long long stt, int mode,
+                                 const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  const int sortcap = NT == 32 ? 1024 : 4096;
+  const size_t smem = step_smem_bytes<NT>(sortcap);
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_step<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  k_step<NT><<<st.lay.B, NT, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, sortcap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
+                        int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  if (st.lay.B == 0) return cudaSuccess;
+  if (st.lay.beam <= 32) return launch_step_t<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return launch_step_t<128>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+}
+
+cudaError_t launch_output(const View& st, int nbest, int* out_tokens, int* out_lengths, float* out_scores,
+                          int out_len, cudaStream_t s) {
+  if (st.lay.B == 0) return cudaSuccess;
+  k_output<<<st.lay.B, 128, 0, s>>>(st, nbest, out_tokens, out_lengths, out_scores, out_len);
+  return cudaGetLastError();
+}
+
+}  // namespace ctcpb

@@ -1,0 +1,20 @@
+// Host-side launchers of the decoder kernels (ctcpb_kernels.cu).
+#pragma once
+
+#include "ctcpb_internal.cuh"
+
+namespace ctcpb {
+
+cudaError_t launch_init(const View& st, cudaStream_t s);
+cudaError_t launch_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
+                          int mode, float log_thr, int* sel, int* nsel, cudaStream_t s);
+cudaError_t launch_prepass(const View& st, const float* lp, long long sb, long long stt, int mode,
+                           const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+cudaError_t launch_prepass_rows(const float* lp, long long stride_r, int R, int V, int blank, int L, int* ids,
+                                float* lps, int* cnt, float* lpb, float* flp, int* fid, cudaStream_t s);
+cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
+                        int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+cudaError_t launch_output(const View& st, int nbest, int* out_tokens, int* out_lengths, float* out_scores,
+                          int out_len, cudaStream_t s);
+
+}  // namespace ctcpb

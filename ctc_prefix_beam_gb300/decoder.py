@@ -1,0 +1,265 @@
+"""Thin Python binding of the C-ABI decoder library (include/ctcpb.h).
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current CUDA stream.  The
+library is loaded on first use; if it has not been built, calls raise
+``RuntimeError`` -- there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+OK, EINVAL, ENULL, EALIGN, ESIZE, ECUDA = 0, -1, -2, -3, -4, -5
+DEV_HEADER, DEV_PAGES, DEV_TIMEOUT, DEV_OVERFLOW = 0x1, 0x2, 0x4, 0x8
+NEG = -3.4028234663852886e38
+
+
+class CtcpbError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [("beam", ctypes.c_int32), ("nbest", ctypes.c_int32), ("blank_id", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int32), ("blank_threshold", ctypes.c_float),
+                ("paged", ctypes.c_int32), ("page_size", ctypes.c_int32), ("list_len", ctypes.c_int32)]
+
+
+@dataclasses.dataclass
+class Config:
+    """Mirror of ``ctcpb_config`` (section 11 of the decoder's description)."""
+    beam: int = 10
+    nbest: Optional[int] = None
+    blank_id: int = 0
+    max_seq_len: int = 0
+    blank_threshold: float = 1.0
+    paged: bool = False
+    page_size: int = 16
+    list_len: int = 0
+
+    def c(self) -> _Cfg:
+        return _Cfg(self.beam, self.beam if self.nbest is None else self.nbest, self.blank_id,
+                    self.max_seq_len, self.blank_threshold, int(bool(self.paged)), self.page_size,
+                    self.list_len)
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load the decoder library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"decoder library not built: {path} is missing "
+                                   "(run `python -m ctc_prefix_beam_gb300.build`)")
+            L = ctypes.CDLL(path)
+            P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            cfgp = ctypes.POINTER(_Cfg)
+            sig = {
+                "ctcpb_status_string": (ctypes.c_char_p, [I]),
+                "ctcpb_list_len": (I, [cfgp, I]),
+                "ctcpb_workspace_size": (I, [cfgp, I, I, I, ctypes.POINTER(SZ)]),
+                "ctcpb_decode_offline": (I, [cfgp, P, I64, I64, P, I, I, I, P, SZ, P, P, P, I, P]),
+                "ctcpb_decode_offline_staged": (I, [cfgp, P, I64, I64, P, I, I, I, P, SZ, P, P, P, I,
+                                                    ctypes.c_uint32, P]),
+                "ctcpb_state_size": (I, [cfgp, I, I, ctypes.POINTER(SZ)]),
+                "ctcpb_stream_init": (I, [cfgp, P, SZ, I, I, P]),
+                "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
+                "ctcpb_read_state": (I, [cfgp, P, SZ, I, I, P, P, P, I, P]),
+                "ctcpb_read_status": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
+                "ctcpb_select_frames": (I, [cfgp, P, I64, I64, P, I, I, I, P, P, P]),
+                "ctcpb_topk_prepass": (I, [cfgp, P, I64, I, I, P, P, P, P, P, P, P]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype, fn.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().ctcpb_status_string(code).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise CtcpbError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _f32_3d(lp: torch.Tensor) -> torch.Tensor:
+    if lp.dtype != torch.float32 or lp.dim() != 3 or not lp.is_cuda:
+        raise ValueError("log_prob must be a CUDA float32 tensor [B, T, V]")
+    if lp.stride(2) != 1:
+        lp = lp.contiguous()
+    return lp
+
+
+def _alloc(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def list_len(cfg: Config, V: int) -> int:
+    rc = lib().ctcpb_list_len(ctypes.byref(cfg.c()), V)
+    if rc < 0:
+        raise CtcpbError(rc, "list_len")
+    return rc
+
+
+def workspace_size(cfg: Config, B: int, T: int, V: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().ctcpb_workspace_size(ctypes.byref(cfg.c()), B, T, V, ctypes.byref(n)), "workspace_size")
+    return n.value
+
+
+def state_size(cfg: Config, B: int, V: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().ctcpb_state_size(ctypes.byref(cfg.c()), B, V, ctypes.byref(n)), "state_size")
+    return n.value
+
+
+def _outputs(B, nbest, out_len, device):
+    return (torch.empty((B, nbest, out_len), dtype=torch.int32, device=device),
+            torch.empty((B, nbest), dtype=torch.int32, device=device),
+            torch.empty((B, nbest), dtype=torch.float32, device=device))
+
+
+STAGE_INIT, STAGE_SELECT, STAGE_RANK, STAGE_STEPS, STAGE_OUTPUT, STAGE_ALL = 0x1, 0x2, 0x4, 0x8, 0x10, 0x1f
+
+
+def decode_offline(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None, *,
+                   workspace: Optional[torch.Tensor] = None, out_len: Optional[int] = None, outputs=None,
+                   stages: int = STAGE_ALL):
+    """Offline decode of a CUDA float32 [B, T, V] batch.
+
+    Returns (tokens [B, nbest, out_len] int32 padded -1, lengths [B, nbest]
+    int32, scores [B, nbest] float32), all on the device.  ``out_len``
+    defaults to min(max_seq_len, T) (T when the cap is unset).
+    """
+    lp = _f32_3d(log_prob)
+    B, T, V = lp.shape
+    c = cfg.c()
+    nbest = c.nbest
+    if out_len is None:
+        out_len = min(cfg.max_seq_len, T) if cfg.max_seq_len > 0 else T
+    if seq_lengths is not None:
+        if seq_lengths.dtype != torch.int32 or not seq_lengths.is_cuda:
+            raise ValueError("seq_lengths must be a CUDA int32 tensor [B]")
+        seq_lengths = seq_lengths.contiguous()
+    need = workspace_size(cfg, B, T, V)
+    if workspace is None:
+        workspace = _alloc(need, lp.device)
+    tok, ln, sc = _outputs(B, nbest, out_len, lp.device) if outputs is None else outputs
+    if stages == STAGE_ALL:
+        rc = lib().ctcpb_decode_offline(ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
+                                        _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
+                                        _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(lp.device))
+    else:
+        rc = lib().ctcpb_decode_offline_staged(ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
+                                               _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
+                                               _ptr(tok), _ptr(ln), _ptr(sc), out_len, stages,
+                                               _stream(lp.device))
+    _check(rc, "decode_offline")
+    return tok, ln, sc
+
+
+class StreamState:
+    """A device buffer holding B streams' beam state (caller-owned memory)."""
+
+    def __init__(self, cfg: Config, B: int, V: int, device="cuda"):
+        self.cfg, self.B, self.V = cfg, B, V
+        self.nbytes = state_size(cfg, B, V)
+        self.buf = _alloc(self.nbytes, device)
+        self.init()
+
+    def init(self):
+        _check(lib().ctcpb_stream_init(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
+                                       self.V, _stream(self.buf.device)), "stream_init")
+
+    def step_chunk(self, lp_chunk: torch.Tensor, n_frames: Optional[torch.Tensor] = None):
+        lp = _f32_3d(lp_chunk)
+        if lp.shape[0] != self.B or lp.shape[2] != self.V:
+            raise ValueError("chunk must be [B, chunk_T, V] for this state")
+        if n_frames is not None:
+            if n_frames.dtype != torch.int32 or not n_frames.is_cuda:
+                raise ValueError("n_frames must be a CUDA int32 tensor [B]")
+            n_frames = n_frames.contiguous()
+        _check(lib().ctcpb_stream_step_chunk(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
+                                             self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames),
+                                             lp.shape[1], _stream(lp.device)), "stream_step_chunk")
+
+    def read(self, out_len: Optional[int] = None, outputs=None):
+        c = self.cfg.c()
+        if out_len is None:
+            out_len = self.cfg.max_seq_len if self.cfg.max_seq_len > 0 else 4096
+        tok, ln, sc = _outputs(self.B, c.nbest, out_len, self.buf.device) if outputs is None else outputs
+        _check(lib().ctcpb_read_state(ctypes.byref(c), _ptr(self.buf), self.buf.numel(), self.B, self.V,
+                                      _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(self.buf.device)),
+               "read_state")
+        return tok, ln, sc
+
+    def status(self) -> int:
+        return read_status(self.buf)
+
+
+def read_status(buf: torch.Tensor) -> int:
+    v = ctypes.c_uint32()
+    _check(lib().ctcpb_read_status(_ptr(buf), ctypes.byref(v)), "read_status")
+    return v.value
+
+
+def select_frames(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None):
+    lp = _f32_3d(log_prob)
+    B, T, V = lp.shape
+    sel = torch.empty((B, T), dtype=torch.int32, device=lp.device)
+    nsel = torch.empty((B,), dtype=torch.int32, device=lp.device)
+    _check(lib().ctcpb_select_frames(ctypes.byref(cfg.c()), _ptr(lp), lp.stride(0), lp.stride(1),
+                                     _ptr(seq_lengths), B, T, V, _ptr(sel), _ptr(nsel), _stream(lp.device)),
+           "select_frames")
+    return sel, nsel
+
+
+def topk_prepass(cfg: Config, rows: torch.Tensor):
+    """Ranked labels of each row of a CUDA float32 [R, V] tensor (section 3.4.7)."""
+    if rows.dtype != torch.float32 or rows.dim() != 2 or not rows.is_cuda or rows.stride(1) != 1:
+        raise ValueError("rows must be a CUDA float32 [R, V] tensor with V contiguous")
+    R, V = rows.shape
+    L = list_len(cfg, V)
+    dev = rows.device
+    ids = torch.empty((R, L), dtype=torch.int32, device=dev)
+    lps = torch.empty((R, L), dtype=torch.float32, device=dev)
+    cnt = torch.empty((R,), dtype=torch.int32, device=dev)
+    lpb = torch.empty((R,), dtype=torch.float32, device=dev)
+    flp = torch.empty((R,), dtype=torch.float32, device=dev)
+    fid = torch.empty((R,), dtype=torch.int32, device=dev)
+    _check(lib().ctcpb_topk_prepass(ctypes.byref(cfg.c()), _ptr(rows), rows.stride(0), R, V, _ptr(ids),
+                                    _ptr(lps), _ptr(cnt), _ptr(lpb), _ptr(flp), _ptr(fid), _stream(dev)),
+           "topk_prepass")
+    return dict(ids=ids, lps=lps, cnt=cnt, lpb=lpb, front_lp=flp, front_id=fid)

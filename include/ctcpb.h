@@ -1,0 +1,212 @@
+/*
+ * ctcpb.h -- C ABI of the GB300-native batched CTC prefix beam search decoder.
+ *
+ * What it computes ("GPU CTC Prefix Beam Search Decoder", OASR docs):
+ *   log_prob[B, T, V] (float32 log-probabilities, label 'blank_id' is the CTC
+ *   blank) -> per row the N best collapsed label sequences and their CTC
+ *   posterior log-scores, by prefix beam search (section 3): each hypothesis
+ *   keeps a blank-ending and a non-blank-ending log-probability (3.1), extends
+ *   by every non-blank label through the two paths of 3.2 / 3.4.1, keeps its
+ *   blank/stay slot (3.4.2), merges a shorter hypothesis' extension into the
+ *   longer hypothesis it equals (3.4.3) and keeps the best `beam` candidates
+ *   (3.4.4-3.4.5).  Offline decoding may skip blank-dominant frames (3.5);
+ *   streaming decoding carries the beam state across chunks (section 8).
+ *
+ * Conventions (all calls):
+ *   - Every buffer pointer is a DEVICE pointer, allocated and owned by the
+ *     caller; the library never allocates or frees memory (section 5).
+ *   - log_prob rows are float32 with V contiguous; stride_b / stride_t are in
+ *     elements (64-bit, so offsets past 2^31 elements are fine, section 13).
+ *   - Calls are asynchronous on `stream` and never synchronise with the host.
+ *   - Return value: CTCPB_OK (0) or a negative status for argument errors
+ *     found on the host (nothing is launched then).  Conditions found on the
+ *     device set bits in a status word inside the workspace / state, read with
+ *     ctcpb_read_status().
+ *   - Workspace and state buffers must be 256-byte aligned.
+ *
+ * Arithmetic: float32 with a fixed operation order and the library's own
+ * exp/log1p (Cody-Waite reduction + Taylor series; atanh series), so results
+ * are reproducible bit for bit on any launch shape.
+ */
+#ifndef CTCPB_H
+#define CTCPB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers. */
+typedef struct CUstream_st* ctcpb_stream_t;
+
+/* Host-side status codes. */
+#define CTCPB_OK 0
+#define CTCPB_EINVAL (-1)   /* a dimension or configuration value is out of range */
+#define CTCPB_ENULL (-2)    /* a required pointer is NULL */
+#define CTCPB_EALIGN (-3)   /* workspace/state pointer not 256-byte aligned */
+#define CTCPB_ESIZE (-4)    /* workspace/state buffer smaller than the size query */
+#define CTCPB_ECUDA (-5)    /* a CUDA launch failed (the runtime error is pending) */
+
+/* Device-side status bits (ctcpb_read_status). */
+#define CTCPB_DEV_HEADER 0x1u   /* state header does not match the call's dims/config: call skipped */
+#define CTCPB_DEV_PAGES 0x2u    /* paged token pool exhausted: the beam kept its prefix (section 13) */
+#define CTCPB_DEV_TIMEOUT 0x4u  /* a bounded inter-block wait gave up: results of the call are invalid */
+#define CTCPB_DEV_OVERFLOW 0x8u /* an internal candidate buffer overflowed: results are invalid */
+
+/*
+ * Decoder configuration (section 11).
+ *   beam             beam width, 1..128 (MAX_BEAM_SIZE of section 11).
+ *   nbest            hypotheses returned per row, 1..beam.
+ *   blank_id         CTC blank label, 0..V-1.
+ *   max_seq_len      cap on labels per hypothesis; a hypothesis at the cap has
+ *                    no non-blank extension (section 11).  <= 0 selects the
+ *                    default: T offline (never binds), 4096 when streaming.
+ *   blank_threshold  offline frame skip (section 3.5): frame t is decoded iff
+ *                    log_prob[b,t,blank] < log(blank_threshold); >= 1 keeps all
+ *                    frames, <= 0 keeps none (section 13).  Ignored when
+ *                    streaming.  Must not be NaN.
+ *   paged            0: flat double-buffered token rows (section 7, "Flat");
+ *                    1: paged, prefix-shared, reference-counted pages (4.2, 7).
+ *   page_size        labels per page in paged mode, 1..1024 (section 11: 16).
+ *   list_len         labels ranked per frame by the vocabulary pre-pass; 0
+ *                    selects min(2*beam+2, V-1) (section 3.4.7).  Any value in
+ *                    1..V-1 gives the same decode: when a frame's list cannot
+ *                    prove the selection, that step re-ranks the whole frame.
+ */
+typedef struct ctcpb_config {
+  int32_t beam;
+  int32_t nbest;
+  int32_t blank_id;
+  int32_t max_seq_len;
+  float blank_threshold;
+  int32_t paged;
+  int32_t page_size;
+  int32_t list_len;
+} ctcpb_config;
+
+/* Human-readable text for a host status code. */
+const char* ctcpb_status_string(int status);
+
+/*
+ * Workspace bytes for ctcpb_decode_offline on [B, T, V] (section 5,
+ * calculate_[paged_]workspace_size).  Writes *bytes; returns a status.
+ */
+int ctcpb_workspace_size(const ctcpb_config* cfg, int B, int T, int V, size_t* bytes);
+
+/*
+ * Offline decode (section 3.7 / 12.1, ctc_beam_search_decode[_paged]).
+ *   log_prob      [B, T, V] float32, element strides stride_b, stride_t (>= V).
+ *   seq_lengths   [B] int32 valid frames per row (values clamped to [0, T]);
+ *                 NULL means T for every row.  Frames t >= len_b are never read.
+ *   ws, ws_bytes  workspace of at least ctcpb_workspace_size() bytes; its
+ *                 contents need no initialisation and are overwritten.
+ *   out_tokens    [B, nbest, out_len] int32: labels of each hypothesis, padded
+ *                 with -1; a hypothesis longer than out_len is cut (its length
+ *                 still reports the full count, section 13).
+ *   out_lengths   [B, nbest] int32;  out_scores [B, nbest] float32.
+ *   Hypotheses are ordered by score (descending); a row with fewer live
+ *   hypotheses than nbest has dead slots (length 0, score -FLT_MAX, tokens -1);
+ *   a row with no decoded frame returns the empty hypothesis with score 0 in
+ *   slot 0 (section 13).  B == 0 is a no-op.
+ */
+int ctcpb_decode_offline(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                         const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                         int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                         ctcpb_stream_t stream);
+
+/*
+ * Streaming state bytes for B independent streams of vocabulary V (section 5,
+ * calculate_[paged_]state_buffer_size).  The state holds each stream's beam,
+ * its label storage and its step/frame counters (section 4.3).
+ */
+int ctcpb_state_size(const ctcpb_config* cfg, int B, int V, size_t* bytes);
+
+/*
+ * Reset a streaming state (section 8, init_streaming_state[_paged]): every
+ * stream starts before its first frame.  The state is position independent
+ * (offsets, not pointers), so it may be copied with cudaMemcpy and resumed.
+ */
+int ctcpb_stream_init(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                      ctcpb_stream_t stream);
+
+/*
+ * Decode one chunk of frames for every stream (section 8, ctc_beam_search_chunk).
+ *   lp_chunk   [B, chunk_T, V] float32 with element strides stride_b, stride_t.
+ *   n_frames   [B] int32 device array: stream b decodes its first n_frames[b]
+ *              rows of the chunk (values clamped to [0, chunk_T]); NULL means
+ *              chunk_T for every stream.
+ * Streaming never skips frames (section 3.5).  The step and frame counters
+ * live in the state on the device.  Decoding a stream in any chunking gives
+ * the same result as decoding its frames offline without skipping.
+ */
+int ctcpb_stream_step_chunk(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                            const float* lp_chunk, int64_t stride_b, int64_t stride_t, const int32_t* n_frames,
+                            int chunk_T, ctcpb_stream_t stream);
+
+/*
+ * Write the current N best of every stream (section 8, read_streaming_results)
+ * in the output layout of ctcpb_decode_offline.  Does not modify the state.
+ */
+int ctcpb_read_state(const ctcpb_config* cfg, const void* state, size_t state_bytes, int B, int V,
+                     int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                     ctcpb_stream_t stream);
+
+/*
+ * Copy the device status word of a workspace or state to *device_status.
+ * Synchronises the device (for tests and error reporting, not the hot path).
+ */
+int ctcpb_read_status(const void* ws_or_state, uint32_t* device_status);
+
+/* ---- Stage entry points (the steps of the hot path, exposed for testing
+ * and per-kernel timing). */
+
+/* Stages of ctcpb_decode_offline, in launch order. */
+#define CTCPB_STAGE_INIT 0x1u    /* reset the workspace's per-row state (section 3.7) */
+#define CTCPB_STAGE_SELECT 0x2u  /* frame selection (section 3.5) */
+#define CTCPB_STAGE_RANK 0x4u    /* vocabulary pre-pass of every kept frame (section 3.4.7) */
+#define CTCPB_STAGE_STEPS 0x8u   /* all decode steps of every row (sections 3.3-3.4) */
+#define CTCPB_STAGE_OUTPUT 0x10u /* N-best gather (section 3.6) */
+#define CTCPB_STAGE_ALL 0x1fu
+
+/*
+ * ctcpb_decode_offline restricted to the stages in stage_mask, on the same
+ * workspace and with the same arguments.  Running the five stages in order,
+ * in one call or several, is exactly ctcpb_decode_offline; a stage reads what
+ * the earlier stages left in the workspace.
+ */
+int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                                const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                                int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                                uint32_t stage_mask, ctcpb_stream_t stream);
+
+/* Number of labels the pre-pass ranks per frame for this config and V. */
+int ctcpb_list_len(const ctcpb_config* cfg, int V);
+
+/*
+ * Frame selection (section 3.5): sel [B, T] int32 receives the kept frames of
+ * each row in order (the rest of the row is -1), nsel [B] their count.
+ */
+int ctcpb_select_frames(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                        const int32_t* seq_lengths, int B, int T, int V, int32_t* sel, int32_t* nsel,
+                        ctcpb_stream_t stream);
+
+/*
+ * Vocabulary pre-pass (section 3.4.7) over R frame rows (row r at
+ * log_prob + r * stride_r): the first L = list_len non-blank live labels by
+ * (log-prob desc, label asc) -> ids [R, L] int32 / lps [R, L] float32 (padded
+ * with -1 / -FLT_MAX), cnt [R], the blank log-prob lpb [R], and the next
+ * ranked label after the list (front_id [R], front_lp [R]; -1 / -FLT_MAX when
+ * none).  A label is live iff its log-prob is > -FLT_MAX (NaN and -inf are
+ * read as -FLT_MAX).
+ */
+int ctcpb_topk_prepass(const ctcpb_config* cfg, const float* log_prob, int64_t stride_r, int R, int V,
+                       int32_t* ids, float* lps, int32_t* cnt, float* lpb, float* front_lp, int32_t* front_id,
+                       ctcpb_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTCPB_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads, exports every symbol include/ctcpb.h declares,
+and rejects bad arguments on the host (no GPU needed: nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from ctc_prefix_beam_gb300 import build as B
+from ctc_prefix_beam_gb300 import decoder as D
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return D.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ctcpb.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ctcpb_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert D.status_string(code) not in ("", "unknown status")
+    assert D.status_string(-99) == "unknown status"
+
+
+def cfg(**kw):
+    base = dict(beam=10, nbest=10, blank_id=0, max_seq_len=0, blank_threshold=1.0, paged=False,
+                page_size=16, list_len=0)
+    base.update(kw)
+    return D.Config(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(beam=0), dict(beam=129), dict(nbest=11), dict(nbest=0),
+                                 dict(blank_id=-1), dict(blank_id=5000), dict(paged=True, page_size=0),
+                                 dict(list_len=-1), dict(blank_threshold=float("nan"))])
+def test_size_query_rejects_bad_config(lib, bad):
+    with pytest.raises(D.CtcpbError) as e:
+        D.workspace_size(cfg(**bad), 4, 10, 5000)
+    assert e.value.code == D.EINVAL
+
+
+def test_size_queries(lib):
+    c = cfg()
+    a = D.workspace_size(c, 32, 500, 5000)
+    b = D.workspace_size(c, 64, 500, 5000)
+    assert 0 < a < b and a % 256 == 0
+    s1 = D.state_size(c, 128, 5000)
+    s2 = D.state_size(cfg(max_seq_len=400), 128, 5000)
+    assert s2 < s1
+    p = D.state_size(cfg(beam=128, nbest=128, paged=True, max_seq_len=400), 16, 29)
+    assert p > 0
+    with pytest.raises(D.CtcpbError):
+        D.workspace_size(c, -1, 10, 5000)
+    assert D.list_len(c, 5000) == 22
+    assert D.list_len(cfg(beam=128, nbest=128), 29) == 28
+    assert D.list_len(cfg(list_len=3), 5000) == 3
+
+
+def test_host_validation_before_any_launch(lib):
+    c = cfg().c()
+    NULL = None
+    # B = 0 is a no-op
+    assert lib.ctcpb_decode_offline(ctypes.byref(c), NULL, 5000, 5000, NULL, 0, 10, 5000, NULL, 0, NULL, NULL,
+                                    NULL, 0, NULL) == D.OK
+    # missing outputs
+    assert lib.ctcpb_decode_offline(ctypes.byref(c), ctypes.c_void_p(256), 5000, 5000, NULL, 2, 10, 5000,
+                                    ctypes.c_void_p(256), 1 << 30, NULL, NULL, NULL, 10, NULL) == D.ENULL
+    # bad stride
+    assert lib.ctcpb_decode_offline(ctypes.byref(c), ctypes.c_void_p(256), 5000, 10, NULL, 2, 10, 5000,
+                                    ctypes.c_void_p(256), 1 << 30, ctypes.c_void_p(256), ctypes.c_void_p(256),
+                                    ctypes.c_void_p(256), 10, NULL) == D.EINVAL
+    # misaligned / too small workspace
+    args = (ctypes.byref(c), ctypes.c_void_p(256), 50000, 5000, NULL, 2, 10, 5000)
+    outs = (ctypes.c_void_p(512), ctypes.c_void_p(512), ctypes.c_void_p(512), 10, NULL)
+    assert lib.ctcpb_decode_offline(*args, ctypes.c_void_p(260), 1 << 30, *outs) == D.EALIGN
+    assert lib.ctcpb_decode_offline(*args, ctypes.c_void_p(512), 1024, *outs) == D.ESIZE
+    assert lib.ctcpb_decode_offline(*args, NULL, 1 << 30, *outs) == D.ENULL
+    # streaming: bad state sizes
+    assert lib.ctcpb_stream_init(ctypes.byref(c), ctypes.c_void_p(512), 16, 4, 5000, NULL) == D.ESIZE
+    assert lib.ctcpb_stream_step_chunk(ctypes.byref(c), ctypes.c_void_p(512), 16, 4, 5000, NULL, 5000, 5000,
+                                       NULL, 16, NULL) == D.ENULL
+    assert lib.ctcpb_read_status(NULL, NULL) == D.ENULL
+    assert lib.ctcpb_topk_prepass(ctypes.byref(c), NULL, 10, 5, 5000, NULL, NULL, NULL, NULL, NULL, NULL,
+                                  NULL) == D.EINVAL
