@@ -60,8 +60,12 @@ struct Layout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Labels ranked per frame: default min(2*beam+2, V-1) (section 3.4.6's K_all
+// bound).  A requested length below `beam` is raised to `beam`, because step 0
+// seeds beam-1 labels straight from the list (section 3.3).
 inline int default_list_len(int beam, int V, int list_len) {
   int L = list_len > 0 ? list_len : 2 * beam + 2;
+  if (L < beam) L = beam;
   if (L > V - 1) L = V - 1;
   if (L > kMaxList) L = kMaxList;
   return L < 1 ? 1 : L;

@@ -67,7 +67,8 @@ def test_size_queries(lib):
         D.workspace_size(c, -1, 10, 5000)
     assert D.list_len(c, 5000) == 22
     assert D.list_len(cfg(beam=128, nbest=128), 29) == 28
-    assert D.list_len(cfg(list_len=3), 5000) == 3
+    assert D.list_len(cfg(list_len=3), 5000) == 10
+    assert D.list_len(cfg(beam=2, nbest=2, list_len=3), 5000) == 3
 
 
 def test_host_validation_before_any_launch(lib):

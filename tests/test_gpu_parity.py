@@ -48,7 +48,7 @@ def adversarial_rows(rng, R, V):
 
 
 @pytest.mark.parametrize("V,beam,list_len", [(5000, 10, 0), (1024, 16, 0), (29, 128, 0), (32, 4, 0),
-                                             (7, 4, 0), (5000, 10, 1), (5000, 10, 3), (300, 31, 0),
+                                             (7, 4, 0), (5000, 2, 3), (5000, 1, 1), (300, 31, 0),
                                              (5000, 40, 0), (2, 1, 0), (3000, 128, 0)])
 def test_prepass_lists_match_oracle(V, beam, list_len):
     rng = np.random.default_rng(V + beam)
@@ -110,7 +110,8 @@ EDGE = [
     dict(beam=10, blank_id=4),
     dict(beam=10, max_seq_len=3),          # the cap binds
     dict(beam=10, max_seq_len=1),
-    dict(beam=10, list_len=1),             # every step proves nothing: full-row re-rank
+    dict(beam=10, list_len=1),             # list of `beam` labels: frequent full-row re-ranks
+    dict(beam=3, list_len=3, V=40),        # short list on a wider vocabulary
     dict(beam=10, list_len=2, paged=True, page_size=3),
     dict(beam=6, paged=True, page_size=1),
     dict(beam=6, blank_threshold=0.0),     # no frame decoded
