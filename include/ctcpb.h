@@ -117,6 +117,29 @@ int ctcpb_decode_offline(const ctcpb_config* cfg, const float* log_prob, int64_t
                          ctcpb_stream_t stream);
 
 /*
+ * Offline decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart: it exists for code that may not call cudaMalloc (inside
+ * a stream capture that must stay allocation-free, in an engine plugin whose
+ * host owns the device heap, on a real-time path that must not block in the
+ * allocator).  Same arguments and results as ctcpb_decode_offline without the
+ * workspace: the workspace is a fixed device array of
+ * CTCPB_NOALLOC_SCRATCH_BYTES inside this library, held by every device that
+ * loads the library until the process exits.
+ *   - Returns CTCPB_ESIZE when the problem's workspace (ctcpb_workspace_size)
+ *     exceeds CTCPB_NOALLOC_SCRATCH_BYTES; nothing is launched then.
+ *   - Calls no allocator.  The first call on each device looks up the array's
+ *     device address (cudaGetSymbolAddress) with that device current; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array: calls whose work overlaps on
+ *     the GPU (different streams, or several host threads) race and corrupt
+ *     each other's results.  Serialise them, e.g. on one stream.
+ */
+#define CTCPB_NOALLOC_SCRATCH_BYTES (32u << 20)
+int ctcpb_decode_offline_noalloc(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                                 const int32_t* seq_lengths, int B, int T, int V, int32_t* out_tokens,
+                                 int32_t* out_lengths, float* out_scores, int out_len, ctcpb_stream_t stream);
+
+/*
  * Streaming state bytes for B independent streams of vocabulary V (section 5,
  * calculate_[paged_]state_buffer_size).  The state holds each stream's beam,
  * its label storage and its step/frame counters (section 4.3).
