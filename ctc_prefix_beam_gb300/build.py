@@ -19,11 +19,13 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libctcpb.so")
-SOURCES = ["ctcpb_kernels.cu", "ctcpb_api.cu", "ctcpb_noalloc.cu"]
+SOURCES = ["ctcpb_kernels.cu", "ctcpb_warp.cu", "ctcpb_api.cu", "ctcpb_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no implicit multiply-add contraction anywhere (the decoder's
 # float arithmetic is written with explicit round-to-nearest intrinsics).
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+# CTCPB_PHASE_PROF=1 in the environment builds the per-phase cycle counters.
+EXTRA = ["-DCTCPB_PHASE_PROF"] if os.environ.get("CTCPB_PHASE_PROF") == "1" else []
+FLAGS = EXTRA + ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
 
@@ -35,15 +37,20 @@ def nvcc() -> str:
 
 
 def _deps_mtime() -> float:
-    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "ctcpb.h"),
-                                                                  os.path.abspath(__file__)]
+    paths = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    paths += [os.path.join(ROOT, "include", "ctcpb.h"), os.path.abspath(__file__)]
     return max(os.path.getmtime(p) for p in paths)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
+    stamp = os.path.join(BUILD, "flags.txt")
+    flags = " ".join(EXTRA)
+    same_flags = os.path.exists(stamp) and open(stamp).read() == flags
+    if not force and same_flags and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
         return LIB
+    with open(stamp, "w") as f:
+        f.write(flags)
     cc = nvcc()
 
     def compile_one(src):

@@ -193,6 +193,15 @@ int ctcpb_read_status(const void* ws_or_state, uint32_t* device_status) {
   return CTCPB_OK;
 }
 
+int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[4]) {
+  if (!ws_or_state || !counters) return CTCPB_ENULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CTCPB_ECUDA;
+  Header h;
+  if (cudaMemcpy(&h, ws_or_state, sizeof(Header), cudaMemcpyDeviceToHost) != cudaSuccess) return CTCPB_ECUDA;
+  for (int i = 0; i < 4; ++i) counters[i] = h.counters[i];
+  return CTCPB_OK;
+}
+
 int ctcpb_select_frames(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
                         const int32_t* seq_lengths, int B, int T, int V, int32_t* sel, int32_t* nsel,
                         ctcpb_stream_t stream) {

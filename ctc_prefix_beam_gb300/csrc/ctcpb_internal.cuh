@@ -33,7 +33,10 @@ struct Header {
   u32 magic, version;
   int32_t B, V, beam, cap, paged, page_size, blank, list_len, tile, pad0;
   u32 status;  // CTCPB_DEV_* bits
-  u32 pad1[51];
+  u32 counters[4];  // decode steps, exhaustive selections, full-frame scans, hash-proposed merges
+  u32 pad2;
+  u64 phase_cycles[8];  // CTCPB_PHASE_PROF builds: clock64 cycles per step phase, summed over rows
+  u32 pad1[30];
 };
 static_assert(sizeof(Header) == 256, "header is 256 bytes");
 
@@ -53,7 +56,7 @@ struct Layout {
   int ppr;     // paged: physical pages per row
   int T_sel;   // offline: frames per row of the selection list (0 when streaming)
   size_t rec_bytes;
-  size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp;
+  size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp, o_msrc;
   size_t o_clist, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;
   size_t o_recs, o_sel, o_nsel, total;
 };
@@ -94,6 +97,7 @@ inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_s
   o.o_len = take(4 * nb);
   o.o_h = take(8 * nb);
   o.o_hp = take(8 * nb);
+  o.o_msrc = take(4 * nb);
   if (!paged) {
     o.o_clist = take(4 * 2 * nb * (size_t)o.ldseq);
   } else {
@@ -126,6 +130,8 @@ struct View {
   __host__ __device__ int* len() const { return (int*)(base + lay.o_len); }
   __host__ __device__ u64* h() const { return (u64*)(base + lay.o_h); }
   __host__ __device__ u64* hp() const { return (u64*)(base + lay.o_hp); }
+  // merge source: slot i with l_k = l_i + last(l_k), or -1 (kept by the warp kernel)
+  __host__ __device__ int* msrc() const { return (int*)(base + lay.o_msrc); }
   // flat token rows: clist[par][b][k][ldseq]
   __host__ __device__ int* clist(int par, int b, int k) const {
     return (int*)(base + lay.o_clist) + (((size_t)par * lay.B + b) * lay.beam + k) * (size_t)lay.ldseq;
@@ -155,7 +161,8 @@ struct RecHdr {
   int32_t front_id;  // first label after the list (-1: none live)
   float lpb;         // blank log-prob
   float front_lp;    // its log-prob (-FLT_MAX: none)
-  int32_t pad[4];
+  int32_t t;         // frame index of the step (offline: the kept frame)
+  int32_t pad[3];
 };
 static_assert(sizeof(RecHdr) == 32, "record header is 32 bytes");
 __host__ __device__ inline int* rec_ids(char* r) { return (int*)(r + 32); }

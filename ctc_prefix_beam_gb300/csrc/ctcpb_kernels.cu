@@ -90,6 +90,8 @@ __global__ void k_init(View st) {
     h->B = L.B; h->V = L.V; h->beam = L.beam; h->cap = L.cap; h->paged = L.paged;
     h->page_size = L.page_size; h->blank = L.blank; h->list_len = L.L; h->tile = L.tile;
     h->status = 0u;
+    for (int i = 0; i < 4; ++i) h->counters[i] = 0u;
+    for (int i = 0; i < 8; ++i) h->phase_cycles[i] = 0ull;
   }
   for (size_t b = tid; b < (size_t)L.B; b += nthr) {
     RowHdr r;
@@ -289,6 +291,7 @@ __global__ void __launch_bounds__(256) k_prepass(View st, const float* __restric
     }
     char* r = st.rec(b, s);
     RecHdr* h = (RecHdr*)r;
+    if (lane == 0) h->t = mode == 0 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
     rank_row(row, Ly.V, Ly.blank, Ly.L, bufs[wid], lane, rec_ids(r), rec_lps(r, Ly.Lpad), &h->cnt, &h->lpb,
              &h->front_lp, &h->front_id);
   }
@@ -939,6 +942,8 @@ static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, 
 cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                         int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (st.lay.B == 0) return cudaSuccess;
+  if (st.lay.beam <= 32 && !st.lay.paged)
+    return launch_step_warp(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   if (st.lay.beam <= 32) return launch_step_t<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   return launch_step_t<128>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }

@@ -1,0 +1,827 @@
+// Warp-per-row decode steps for beam <= 32 (flat token storage).
+//
+// One warp owns one row for the whole call and keeps the beam in registers:
+// lane k holds hypothesis k.  Per step ("GPU CTC Prefix Beam Search Decoder",
+// sections 3.3-3.4.6):
+//   * blank slot of every hypothesis (3.4.2) with the stay path (3.4.1) and
+//     the merge fold of 3.4.3, on lanes 0..nlive-1;
+//   * round 1: a staircase of each hypothesis' best listed labels on the other
+//     lanes (hypothesis k gets q_k labels, (k+1)(q_k+1) kept small: the best
+//     `beam` of a sum of two sorted lists lie under such a staircase), with the
+//     repeat path (c = last, pb only) in the slot of its label; the 32
+//     candidates are ranked by counting;
+//   * the ranking is PROVEN exact when every candidate left out scores below
+//     the beam-th kept one: hypothesis k's left-out labels score at most
+//     add(lp[next listed label], A_k), its unlisted ones add(front, A_k);
+//   * round 2 (the proof failed): the beam-th kept score tau is a lower bound
+//     of the true one, so the candidates that matter are exactly those scoring
+//     >= tau; each hypothesis counts its listed labels >= tau (the list is
+//     sorted) and, if they fit in 32 lanes, they are ranked again -- exact;
+//   * otherwise every candidate >= tau of the frame, unlisted labels included,
+//     is collected and sorted (warp_collect_select).
+// Prefix merges are tracked through the winners' sources (no token reads):
+// if j extends source s and i is s's blank winner, l_j = l_i + last_j; two
+// blank winners inherit their sources' relation.  The one remaining case (a
+// blank winner whose parent prefix was rebuilt by an extension) is proposed
+// by 32-bit prefix hashes and confirmed by comparing stored tokens.
+// Tokens: every step appends (source slot, token) per winner to a ring in
+// shared memory; every kRing steps (and at the end of the call) the ring is
+// materialised into the flat double-buffered rows: each hypothesis' row in the
+// other parity = its origin row's prefix + the labels it gained in the window.
+// lp[t][last] for step s+1 is gathered at the top of step s over every label
+// that can be "last" then (the current lasts and step s's list), with cp.async
+// into shared memory, so the loads overlap step s; ranked-frame records are
+// prefetched kRecRing steps ahead the same way.
+#include "ctcpb_internal.cuh"
+#include "ctcpb_kernels.h"
+
+namespace ctcpb {
+namespace {
+
+#define WFULL 0xffffffffu
+
+// Optional per-phase cycle accounting (build with -DCTCPB_PHASE_PROF).
+#ifdef CTCPB_PHASE_PROF
+#define PHASE_MARK(i)                 \
+  do {                                \
+    const long long now_ = clock64(); \
+    prof[i] += (u64)(now_ - prof_t0); \
+    prof_t0 = now_;                   \
+  } while (0)
+#else
+#define PHASE_MARK(i) \
+  do {                \
+  } while (0)
+#endif
+
+constexpr int kRing = 128;            // steps of history between materialisations
+constexpr int kRecRing = 4;           // prefetched ranked-frame records
+constexpr int kWPC = 4;               // rows (warps) per block
+constexpr int kGenCap = 512;          // keys of the exhaustive selection
+constexpr int kMaxRec = 32 + 8 * 68;  // record bytes for beam <= 32 (L <= 66)
+constexpr int kGath = 128;            // gathered log-probs per frame (beam + L <= 98)
+constexpr u32 kH32 = 2166136261u;     // prefix hash of the empty prefix
+constexpr u32 kGold = 0x9e3779b9u;
+
+struct __align__(16) WarpSmem {
+  u64 keys[kGenCap];
+  u32 hist[kRing][32];
+  char rec[kRecRing][kMaxRec];
+  float gath[2][kGath];
+  float A[32], bpb[32], bpnb[32], rep[32];
+  int last[32], len[32];
+  int bw[32];
+  float w_sc[32], w_pb[32], w_pnb[32];
+  int w_src[32], w_tok[32], w_gl[32];
+  int fold_i[32], fold_c[32];
+  int nfold, nkeys;
+};
+
+struct Tables {
+  unsigned short qmap[33][32];  // nlive -> lane -> (hyp << 8 | list position), 0xffff: none
+  unsigned char qcnt[33][32];  // nlive -> hyp -> listed labels of that hyp in the round-1 set
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  unsigned s = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// 32-bit prefix hash (FNV-1a step).  Equal prefixes hash equal; a collision
+// only costs an extra exact comparison.
+__device__ __forceinline__ u32 h32(u32 h, int c) { return (h ^ (u32)c) * 16777619u; }
+
+__device__ __forceinline__ int wpow2(int n, int lo) {
+  int p = lo;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+__device__ void warp_bitonic(u64* a, int P, int lane) {
+  for (int k = 2; k <= P; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lane; i < P; i += 32) {
+        int ixj = i ^ j;
+        if (ixj > i) {
+          u64 x = a[i], y = a[ixj];
+          bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            a[i] = y;
+            a[ixj] = x;
+          }
+        }
+      }
+      __syncwarp();
+    }
+}
+
+// Staircase tables, one lane per nlive value (lane 0 also does nlive = 32).
+__device__ void build_tables(Tables& tb, int lane) {
+  for (int n = lane; n <= 32; n += 32) {
+    unsigned char q[32];
+    for (int k = 0; k < 32; ++k) {
+      q[k] = 0;
+      tb.qmap[n][k] = 0xffff;
+    }
+    int l = n;
+    // one listed label per hypothesis first: a frame whose best label extends
+    // every hypothesis (a label frame) needs each of them in the set
+    for (int k = 0; k < n && l < 32; ++k, ++l) {
+      tb.qmap[n][l] = (unsigned short)(k << 8);
+      q[k] = 1;
+    }
+    for (; l < 32 && n > 0; ++l) {
+      int best = 0, bv = 1 << 30;
+      for (int k = 0; k < n; ++k) {
+        const int v = (k + 1) * (q[k] + 1);
+        if (v < bv) {
+          bv = v;
+          best = k;
+        }
+      }
+      tb.qmap[n][l] = (unsigned short)((best << 8) | q[best]);
+      q[best]++;
+    }
+    for (int k = 0; k < 32; ++k) tb.qcnt[n][k] = q[k];
+  }
+}
+
+// Append `key` (if nonzero and >= thr) to the candidate buffer W.keys[32 ..];
+// the first 32 entries hold the running best after each compaction.
+__device__ __forceinline__ void push_key(WarpSmem& W, u64 key, u64 thr, int lane) {
+  const bool take = key != 0ull && key >= thr;
+  const unsigned m = __ballot_sync(WFULL, take);
+  const int base = W.nkeys;
+  if (take) W.keys[32 + base + __popc(m & ((1u << lane) - 1u))] = key;
+  __syncwarp();
+  if (lane == 0) W.nkeys = base + __popc(m);
+  __syncwarp();
+  if (base + __popc(m) > kGenCap - 64) {  // compact: keep the best 32 at the front
+    warp_bitonic(W.keys, kGenCap, lane);
+    for (int i = 32 + lane; i < kGenCap; i += 32) W.keys[i] = 0ull;
+    if (lane == 0) W.nkeys = 0;
+    __syncwarp();
+  }
+}
+
+// Every candidate of the step with key >= thr, the frame's unlisted labels
+// included when the list cannot bound them, sorted; W.keys[0..beam) holds the
+// best.  Returns how many are live.
+__device__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n, int beam, int cap, int blank, int V,
+                                   const float* __restrict__ row, int lane, u64 thr, u32& scans) {
+  const RecHdr* h = (const RecHdr*)rec;
+  const int cnt = h->cnt;
+  const int* ids = (const int*)(rec + 32);
+  const float* lps = (const float*)(rec + 32 + 4 * Lpad);
+  const int nfold = W.nfold;
+  for (int i = lane; i < kGenCap; i += 32) W.keys[i] = 0ull;
+  if (lane == 0) W.nkeys = 0;
+  __syncwarp();
+  const int stride = cnt + 2;
+  const int NC = n * stride;
+  for (int base = 0; base < NC; base += 32) {
+    const int g = base + lane;
+    u64 key = 0ull;
+    if (g < NC) {
+      const int k = g / stride, r = g - k * stride;
+      const int L = W.len[k];
+      if (r == 0) {
+        const float sc = dlse(W.bpb[k], W.bpnb[k]);
+        if (sc > CTCPB_NEG) key = cand_key(sc, k, blank);
+      } else if (r == 1) {
+        if (W.rep[k] > CTCPB_NEG) key = cand_key(W.rep[k], k, W.last[k]);
+      } else {
+        const int c = ids[r - 2];
+        bool ok = L < cap && !(L > 0 && c == W.last[k]);
+        for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == k && W.fold_c[f] == c);
+        if (ok) {
+          const float sc = dadd(lps[r - 2], W.A[k]);
+          if (sc > CTCPB_NEG) key = cand_key(sc, k, c);
+        }
+      }
+    }
+    push_key(W, key, thr, lane);
+  }
+  const float front_lp = h->front_lp;
+  if (front_lp > CTCPB_NEG) {
+    // the running beam-th key so far bounds what an unlisted label must reach
+    int P = wpow2(32 + W.nkeys, 64);
+    for (int i = 32 + W.nkeys + lane; i < P; i += 32) W.keys[i] = 0ull;
+    __syncwarp();
+    warp_bitonic(W.keys, P, lane);
+    for (int i = 32 + lane; i < P; i += 32) W.keys[i] = 0ull;
+    if (lane == 0) W.nkeys = 0;
+    __syncwarp();
+    int nw = 0;
+    for (int w = 0; w < beam; ++w) nw += W.keys[w] != 0ull;
+    const u64 kb = nw == beam ? W.keys[beam - 1] : 0ull;
+    if (kb > thr) thr = kb & 0xffffffff00000000ull;
+    bool bad = false;
+    float amax = CTCPB_NEG;
+    if (lane < n && W.len[lane] < cap) {
+      const float u = dadd(front_lp, W.A[lane]);
+      bad = u > CTCPB_NEG && ((u64)fkey(u) << 32) >= thr;
+      amax = W.A[lane];
+    }
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(WFULL, amax, o));
+    if (__any_sync(WFULL, bad)) {
+      ++scans;
+      const u64 kfront = lab_key(front_lp, h->front_id);
+      for (int c0 = 0; c0 < V; c0 += 128) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u + lane;
+          v[u] = c < V ? rdlp(row[c]) : CTCPB_NEG;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u + lane;
+          // an unlisted label worth scoring: reaches thr for the best hypothesis
+          const bool q = c < V && c != blank && v[u] > CTCPB_NEG && lab_key(v[u], c) <= kfront &&
+                         ((u64)fkey(dadd(v[u], amax)) << 32) >= thr;
+          for (unsigned m = __ballot_sync(WFULL, q); m; m &= m - 1) {
+            const int src = __ffs(m) - 1;
+            const int cc = __shfl_sync(WFULL, c, src);
+            const float vv = __shfl_sync(WFULL, v[u], src);
+            u64 key = 0ull;
+            if (lane < n) {
+              const int L = W.len[lane];
+              bool ok = L < cap && !(L > 0 && cc == W.last[lane]);
+              for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == lane && W.fold_c[f] == cc);
+              const float sc = dadd(vv, W.A[lane]);
+              if (ok && sc > CTCPB_NEG) key = cand_key(sc, lane, cc);
+            }
+            push_key(W, key, thr, lane);
+          }
+        }
+      }
+    }
+  }
+  const int P = wpow2(32 + W.nkeys, 64);
+  for (int i = 32 + W.nkeys + lane; i < P; i += 32) W.keys[i] = 0ull;
+  __syncwarp();
+  warp_bitonic(W.keys, P, lane);
+  int nw = 0;
+  for (int w = 0; w < beam; ++w) nw += W.keys[w] != 0ull;
+  return nw;
+}
+
+// Rank of this lane's key among the warp's 32 keys (larger key = better).
+__device__ __forceinline__ int warp_rank(u32 hi, u32 lo, int beam) {
+  int r = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r += __shfl_sync(WFULL, hi, j) > hi;
+  // equal scores among the kept ones leave gaps in the ranks: resolve the
+  // ties on the full key (score, source slot, token)
+  const bool in = hi != 0u && r < beam;
+  const u32 orr = __reduce_or_sync(WFULL, in ? (1u << r) : 0u);
+  if (__popc(orr) != __popc(__ballot_sync(WFULL, in))) {
+    r = 0;
+#pragma unroll 4
+    for (int j = 0; j < 32; ++j) {
+      const u32 hj = __shfl_sync(WFULL, hi, j), lj = __shfl_sync(WFULL, lo, j);
+      r += (hj > hi) || (hj == hi && lj > lo);
+    }
+  }
+  return r;
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* __restrict__ lp, long long sb,
+                                                         long long stt, int mode, const int* __restrict__ nframes,
+                                                         int chunk_T, int tile_start, int tile_len) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  Tables& tb = *reinterpret_cast<Tables*>(smem);
+  WarpSmem& W = reinterpret_cast<WarpSmem*>(smem + align_up(sizeof(Tables), 16))[threadIdx.x >> 5];
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) build_tables(tb, lane);
+  __syncthreads();
+
+  const Layout& Ly = st.lay;
+  const int b = blockIdx.x * kWPC + (threadIdx.x >> 5);
+  if (b >= Ly.B) return;
+  const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V, Lpad = Ly.Lpad;
+  const float NEG = CTCPB_NEG;
+
+  if (mode == 1) {
+    const Header* hd = st.hdr();
+    bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
+              hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
+              hd->page_size == Ly.page_size && hd->blank == Ly.blank && hd->list_len == Ly.L &&
+              hd->tile == Ly.tile;
+    if (!ok) {
+      if (lane == 0) atomicOr(&st.hdr()->status, CTCPB_DEV_HEADER);
+      return;
+    }
+  }
+  int nsteps;
+  if (mode == 0) {
+    nsteps = st.nsel()[b];
+  } else {
+    int nf = nframes ? nframes[b] : chunk_T;
+    nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
+    nsteps = nf - tile_start;
+    nsteps = nsteps < 0 ? 0 : (nsteps > tile_len ? tile_len : nsteps);
+  }
+  if (nsteps == 0) return;
+
+  const RowHdr rh0 = st.rows()[b];
+  int step = rh0.step, t_prev = rh0.t_prev, nlive = rh0.nlive, par = rh0.parity;
+  const int tcount = rh0.tcount;
+  const size_t rb = (size_t)b * beam;
+  float pb = NEG, pnb = NEG, sc = NEG;
+  int last = blank, len = 0, msrc = -1;
+  u32 h = 0u, hp = 0u;
+  if (lane < nlive) {
+    pb = st.pb()[rb + lane];
+    pnb = st.pnb()[rb + lane];
+    sc = st.sc()[rb + lane];
+    last = st.last()[rb + lane];
+    len = st.len()[rb + lane];
+    h = (u32)st.h()[rb + lane];
+    hp = (u32)st.hp()[rb + lane];
+    msrc = st.msrc()[rb + lane];
+  }
+  int origin = lane, lo = len, nnew = 0, gl = -1;
+  int win0 = 0;  // call step index of the ring's first entry
+  u32 c_steps = 0, c_fb = 0, c_scan = 0, c_hash = 0;
+#ifdef CTCPB_PHASE_PROF
+  u64 prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  long long prof_t0 = clock64();
+#endif
+  const float* lpb_row = lp + (long long)b * sb;
+  const int rec_chunks = (int)(Ly.rec_bytes / 16);
+
+  auto row_of = [&](int s, const RecHdr* hd) -> const float* {
+    return lpb_row + (long long)(mode == 0 ? hd->t : tile_start + s) * stt;
+  };
+  auto prefetch_rec = [&](int s) {
+    if (s < nsteps) {
+      const char* src = st.rec(b, s);
+      char* dst = W.rec[s % kRecRing];
+      for (int c = lane; c < rec_chunks; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+    }
+  };
+
+  // Materialise the ring into the other parity of the flat rows.
+  auto flush = [&](int s_last) {
+    const int np = par ^ 1;
+    int slot = lane, rem = nnew;
+    for (int r = s_last - win0; r >= 0; --r) {
+      const u32 e = W.hist[r][slot & 31];
+      const int tk = (int)(e & 0xffffffu);
+      if (lane < nlive && tk != blank) {
+        --rem;
+        st.clist(np, b, lane)[lo + rem] = tk;
+      }
+      slot = (int)(e >> 24);
+    }
+    // origin prefixes, four rows at a time with every load issued before the stores
+    for (int w0 = 0; w0 < nlive; w0 += 4) {
+      int4 v[4][2];
+      int nv[4], o[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int w = w0 + u < nlive ? w0 + u : w0;
+        o[u] = w0 + u < nlive ? __shfl_sync(WFULL, origin, w) : -1;
+        const int c = __shfl_sync(WFULL, lo, w);
+        nv[u] = o[u] >= 0 ? (c >> 2) : 0;
+        const int4* from = o[u] >= 0 ? reinterpret_cast<const int4*>(st.clist(par, b, o[u])) : nullptr;
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (lane + 32 * i < nv[u]) v[u][i] = from[lane + 32 * i];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (o[u] < 0) continue;
+        int4* to = reinterpret_cast<int4*>(st.clist(np, b, w0 + u));
+        const int4* from = reinterpret_cast<const int4*>(st.clist(par, b, o[u]));
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (lane + 32 * i < nv[u]) to[lane + 32 * i] = v[u][i];
+        for (int x = 64 + lane; x < nv[u]; x += 32) to[x] = from[x];
+        const int c = __shfl_sync(WFULL, lo, w0 + u);
+        if (lane < (c & 3))
+          st.clist(np, b, w0 + u)[(nv[u] << 2) + lane] = st.clist(par, b, o[u])[(nv[u] << 2) + lane];
+      }
+    }
+    par = np;
+    origin = lane;
+    lo = len;
+    nnew = 0;
+    win0 = s_last + 1;
+    __syncwarp();
+  };
+
+  for (int d = 0; d < kRecRing; ++d) {
+    prefetch_rec(d);
+    cp_commit();
+  }
+
+  for (int s = 0; s < nsteps; ++s) {
+    PHASE_MARK(7);
+    cp_wait<1>();
+    __syncwarp();
+    PHASE_MARK(0);
+    const char* Rc = W.rec[s % kRecRing];
+    const RecHdr* hd = (const RecHdr*)Rc;
+    const int cnt = hd->cnt;
+    const float lpb = hd->lpb;
+    const int my_id = lane < cnt ? ((const int*)(Rc + 32))[lane] : -1;
+    const float my_lp = lane < cnt ? ((const float*)(Rc + 32 + 4 * Lpad))[lane] : NEG;
+    const int t = mode == 0 ? hd->t : tcount + s;
+    const float* row = row_of(s, hd);
+    const bool gap = t > t_prev + 1;
+    const bool live = lane < nlive;
+    W.bw[lane] = -1;
+    // lp[t_{s+1}][x] for every label x that can be "last" at step s+1: the
+    // current lasts (slots 0..beam-1) and this step's list (beam + position)
+    if (s + 1 < nsteps) {
+      const char* R1 = W.rec[(s + 1) % kRecRing];
+      const float* row1 = row_of(s + 1, (const RecHdr*)R1);
+      float* gdst = W.gath[(s + 1) & 1];
+      for (int x = lane; x < beam + cnt; x += 32) {
+        // x < beam <= 32 means x == lane: this lane's own hypothesis
+        const int lab = x < beam ? ((live && len > 0) ? last : -1) : ((const int*)(Rc + 32))[x - beam];
+        if (lab >= 0) cp_async4(gdst + x, row1 + lab);
+      }
+    }
+    cp_commit();
+
+    int nw;
+    bool isb_w = false;
+    if (step == 0) {
+      // ---- section 3.3
+      const int nb = beam > 1 ? beam - 1 : 1;
+      const int ntok = cap >= 1 ? (nb < cnt ? nb : cnt) : 0;
+      const bool empty_live = beam > 1 && lpb > NEG;
+      if (lane < ntok) {
+        pb = gap ? my_lp : NEG;
+        pnb = gap ? NEG : my_lp;
+        sc = my_lp;
+        last = my_id;
+        len = 1;
+        h = h32(kH32, my_id);
+        hp = kH32;
+        msrc = empty_live ? ntok : -1;
+        W.hist[s - win0][lane] = ((u32)lane << 24) | (u32)my_id;
+      } else if (lane == ntok && empty_live) {
+        pb = lpb;
+        pnb = NEG;
+        sc = lpb;
+        last = blank;
+        len = 0;
+        h = kH32;
+        hp = 0u;
+        msrc = -1;
+        W.hist[s - win0][lane] = ((u32)lane << 24) | (u32)blank;
+      }
+      nw = ntok + (empty_live ? 1 : 0);
+      origin = -1;
+      lo = 0;
+      nnew = lane < ntok ? 1 : 0;
+      gl = -1;
+    } else {
+      // ---- sections 3.4.1-3.4.3 on lanes 0..nlive-1
+      const float A = sc;
+      float pbx = pb, pnbx = pnb;
+      if (gap) {  // collapsed-blank correction: lse(pb, pnb) is the stored score
+        pbx = A;
+        pnbx = NEG;
+      }
+      float lpl = NEG;
+      {
+        const bool gathered = s >= 1 && gl >= 0;
+        const float g = gathered ? W.gath[s & 1][gl] : 0.0f;
+        if (live && len > 0) lpl = gathered ? rdlp(g) : rdlp(__ldg(row + last));
+      }
+      const float bpb = dadd(lpb, A);
+      const float stay = (live && len > 0 && !gap) ? dadd(lpl, pnbx) : NEG;
+      const int mi = live ? msrc : -1;
+      const int mil = mi < 0 ? 0 : mi;
+      const float A_i = __shfl_sync(WFULL, A, mil);
+      const float pb_i = __shfl_sync(WFULL, pbx, mil);
+      const int last_i = __shfl_sync(WFULL, last, mil);
+      const int len_i = __shfl_sync(WFULL, len, mil);
+      const bool rep_i = mi >= 0 && len_i > 0 && last_i == last;
+      float bpnb = stay;
+      if (mi >= 0) bpnb = dlse(stay, dadd(lpl, rep_i ? pb_i : A_i));
+      const float scB = live ? dlse(bpb, bpnb) : NEG;
+      PHASE_MARK(1);
+      // repeat candidate (k, last_k) is folded away when some j has l_j = l_k + last_k
+      int repdead = 0;
+      for (unsigned m = __ballot_sync(WFULL, rep_i); m; m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        if (__shfl_sync(WFULL, mi, j) == lane) repdead = 1;
+      }
+      const float Rrep = (live && len > 0 && len < cap && !repdead) ? dadd(lpl, pbx) : NEG;
+      // ordinary candidates (i, last_j) folded into j's blank slot, as a mask per list position
+      u32 excl = 0u;
+      const unsigned fm = __ballot_sync(WFULL, mi >= 0 && !rep_i);
+      for (unsigned m = fm; m; m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        const int ij = __shfl_sync(WFULL, mi, j);
+        const int cj = __shfl_sync(WFULL, last, j);
+        if (lane < cnt && my_id == cj) excl |= 1u << ij;
+      }
+      const int n = nlive;
+
+      // candidate of this lane: its hypothesis' blank slot (lane < n) or
+      // listed label qp of hypothesis qk
+      float cs;
+      int csrc, ctok, cgl;
+      auto make_cand = [&](bool valid, int qk, int qp) {
+        const float Ak = __shfl_sync(WFULL, A, qk);
+        const int lastk = __shfl_sync(WFULL, last, qk);
+        const int lenk = __shfl_sync(WFULL, len, qk);
+        const float Rk = __shfl_sync(WFULL, Rrep, qk);
+        const int cq = __shfl_sync(WFULL, my_id, qp);
+        const float lq = __shfl_sync(WFULL, my_lp, qp);
+        const u32 exq = __shfl_sync(WFULL, excl, qp);
+        cs = NEG;
+        csrc = 0;
+        ctok = blank;
+        cgl = -1;
+        if (lane < n) {
+          cs = scB;
+          csrc = lane;
+          cgl = lane;
+        } else if (valid && qp < cnt && lenk < cap) {
+          csrc = qk;
+          ctok = cq;
+          if (lenk > 0 && cq == lastk) {
+            cs = Rk;
+            cgl = qk;
+          } else if (!((exq >> qk) & 1u)) {
+            cs = dadd(lq, Ak);
+            cgl = beam + qp;
+          }
+        }
+      };
+
+      // ---- round 1: the staircase
+      {
+        const unsigned short qm = lane >= n ? tb.qmap[n][lane] : (unsigned short)0xffff;
+        make_cand(qm != 0xffff, qm == 0xffff ? 0 : (qm >> 8), qm == 0xffff ? 0 : (qm & 31));
+      }
+      bool clive = cs > NEG;
+      u32 hi = clive ? fkey(cs) : 0u;
+      u32 lo_k = clive ? ~(((u32)csrc << 20) | (u32)ctok) : 0u;
+      int r = warp_rank(hi, lo_k, beam);
+      nw = __popc(__ballot_sync(WFULL, clive && r < beam));
+      PHASE_MARK(2);
+      u32 sstar = 0u;
+      if (nw == beam) sstar = __shfl_sync(WFULL, hi, __ffs(__ballot_sync(WFULL, clive && r == beam - 1)) - 1);
+      bool proven;
+      {
+        const int q = live ? tb.qcnt[n][lane] : 0;
+        const float nxt = __shfl_sync(WFULL, my_lp, q & 31);
+        bool bad = false;
+        if (live && len < cap) {
+          float bnd = NEG;
+          if (q < cnt)
+            bnd = dadd(nxt, A);
+          else if (hd->front_lp > NEG)
+            bnd = dadd(hd->front_lp, A);
+          bad = bnd > NEG && (nw < beam || fkey(bnd) >= sstar);
+        }
+        proven = !__any_sync(WFULL, bad);
+      }
+      PHASE_MARK(3);
+      bool generic = false;
+      if (!proven) {
+        ++c_fb;
+        // ---- round 2: every listed candidate scoring >= tau (tau = sstar)
+        generic = nw < beam;
+        if (!generic) {
+          const int lim = cnt < 32 ? cnt : 32;
+          int ck = 0;
+          for (int k = 0; k < n; ++k) {
+            const float a = __shfl_sync(WFULL, A, k);
+            const int lk = __shfl_sync(WFULL, len, k);
+            const bool p = lane < lim && fkey(dadd(my_lp, a)) >= sstar;
+            const int c = lk < cap ? __popc(__ballot_sync(WFULL, p)) : 0;
+            if (lane == k) ck = c;
+          }
+          // the list must bound everything it leaves out
+          bool over = false;
+          if (live && ck == lim && len < cap) {
+            if (cnt > 32)
+              over = true;
+            else if (hd->front_lp > NEG && fkey(dadd(hd->front_lp, A)) >= sstar)
+              over = true;
+          }
+          int pre = ck;  // inclusive prefix over hypotheses
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(WFULL, pre, o);
+            if (lane >= o) pre += v;
+          }
+          const int total = __shfl_sync(WFULL, pre, n > 0 ? n - 1 : 0);
+          generic = __any_sync(WFULL, over) || n + total > 32;
+          if (!generic) {
+            int qk = 0, qp = 0;
+            const int idx = lane - n;
+            for (int k = 0; k < n; ++k) {
+              const int e = __shfl_sync(WFULL, pre, k);
+              const int c = __shfl_sync(WFULL, ck, k);
+              if (idx >= e - c && idx < e) {
+                qk = k;
+                qp = idx - (e - c);
+              }
+            }
+            make_cand(lane >= n && idx < total, qk, qp);
+            clive = cs > NEG;
+            hi = clive ? fkey(cs) : 0u;
+            lo_k = clive ? ~(((u32)csrc << 20) | (u32)ctok) : 0u;
+            r = warp_rank(hi, lo_k, beam);
+            nw = __popc(__ballot_sync(WFULL, clive && r < beam));
+          }
+        }
+      }
+      if (generic) {
+        if (live) {
+          W.A[lane] = A;
+          W.bpb[lane] = bpb;
+          W.bpnb[lane] = bpnb;
+          W.rep[lane] = Rrep;
+          W.last[lane] = last;
+          W.len[lane] = len;
+        }
+        const unsigned fmm = __ballot_sync(WFULL, mi >= 0 && !rep_i);
+        if (mi >= 0 && !rep_i) {
+          const int f = __popc(fmm & ((1u << lane) - 1u));
+          W.fold_i[f] = mi;
+          W.fold_c[f] = last;
+        }
+        if (lane == 0) W.nfold = __popc(fmm);
+        __syncwarp();
+        const u64 thr = nw == beam ? ((u64)sstar << 32) : 0ull;
+        nw = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr, c_scan);
+        if (lane < nw) {
+          const u64 key = W.keys[lane];
+          const int src = ck_src(key), tk = ck_tok(key);
+          const bool isb = tk == blank;
+          W.w_sc[lane] = ck_score(key);
+          W.w_src[lane] = src;
+          W.w_tok[lane] = tk;
+          W.w_pb[lane] = isb ? W.bpb[src] : NEG;
+          W.w_pnb[lane] = isb ? W.bpnb[src] : ck_score(key);
+          W.w_gl[lane] = (isb || (W.len[src] > 0 && tk == W.last[src])) ? src : -1;
+        }
+      } else if (clive && r < beam) {
+        W.w_sc[r] = cs;
+        W.w_src[r] = csrc;
+        W.w_tok[r] = ctok;
+        W.w_pb[r] = lane < n ? bpb : NEG;
+        W.w_pnb[r] = lane < n ? bpnb : cs;
+        W.w_gl[r] = cgl;
+      }
+      __syncwarp();
+      PHASE_MARK(4);
+
+      // ---- section 3.4.5: commit
+      const bool wl = lane < nw;
+      const int src = wl ? W.w_src[lane] : 0;
+      const int tk = wl ? W.w_tok[lane] : blank;
+      const float score = wl ? W.w_sc[lane] : NEG;
+      const int s_last = __shfl_sync(WFULL, last, src);
+      const int s_len = __shfl_sync(WFULL, len, src);
+      const u32 s_h = __shfl_sync(WFULL, h, src), s_hp = __shfl_sync(WFULL, hp, src);
+      const int s_origin = __shfl_sync(WFULL, origin, src);
+      const int s_lo = __shfl_sync(WFULL, lo, src);
+      const int s_nnew = __shfl_sync(WFULL, nnew, src);
+      const int s_msrc = __shfl_sync(WFULL, msrc, src);
+      const bool isb = tk == blank;
+      isb_w = isb;
+      if (wl) {
+        pb = isb ? W.w_pb[lane] : NEG;
+        pnb = isb ? W.w_pnb[lane] : score;
+        if (gap) {
+          pb = score;
+          pnb = NEG;
+        }
+        sc = score;
+        last = isb ? s_last : tk;
+        len = isb ? s_len : s_len + 1;
+        h = isb ? s_h : h32(s_h, tk);
+        hp = isb ? s_hp : s_h;
+        origin = s_origin;
+        lo = s_lo;
+        nnew = s_nnew + (isb ? 0 : 1);
+        gl = W.w_gl[lane];
+        W.hist[s - win0][lane] = ((u32)src << 24) | ((u32)tk & 0xffffffu);
+        if (isb) W.bw[src] = lane;
+      }
+      __syncwarp();
+      int nm = -1;
+      if (wl) nm = isb ? (s_msrc >= 0 ? W.bw[s_msrc] : -1) : W.bw[src];
+      msrc = nm;
+    }
+
+    // ---- the one merge relation the sources cannot show: a blank winner
+    // whose parent prefix equals an extension winner (hash proposal, exact check)
+    nlive = nw;
+    {
+      const bool wl = lane < nw;
+      const bool want = wl && step > 0 && isb_w && msrc < 0 && len >= 1;
+      if (__any_sync(WFULL, want)) {
+        const u32 key = !wl ? (0x80000000u | (u32)lane)
+                            : (isb_w ? (hp ^ ((u32)(len - 1) * kGold)) : (h ^ ((u32)len * kGold)));
+        const unsigned grp = __match_any_sync(WFULL, key);
+        const unsigned extm = __ballot_sync(WFULL, wl && !isb_w);
+        const unsigned match = want ? (grp & extm) : 0u;
+        const bool cand = want && match != 0u;
+        if (__any_sync(WFULL, cand)) {
+          ++c_hash;
+          flush(s);  // tokens of every hypothesis into the flat rows
+          for (unsigned mj = __ballot_sync(WFULL, cand); mj; mj &= mj - 1) {
+            const int j = __ffs(mj) - 1;
+            const unsigned gj = __shfl_sync(WFULL, match, j);
+            const int Lj = __shfl_sync(WFULL, len, j);
+            for (unsigned mi2 = gj; mi2; mi2 &= mi2 - 1) {
+              const int i = __ffs(mi2) - 1;
+              const int* ri = st.clist(par, b, i);
+              const int* rj = st.clist(par, b, j);
+              bool mism = false;
+              for (int x = lane; x < Lj - 1; x += 32) mism |= ri[x] != rj[x];
+              if (!__any_sync(WFULL, mism)) {
+                if (lane == j) msrc = i;
+                break;
+              }
+            }
+          }
+        }
+      }
+    }
+    PHASE_MARK(5);
+    t_prev = t;
+    ++step;
+    ++c_steps;
+    // ---- prefetch the record kRecRing steps ahead
+    prefetch_rec(s + kRecRing);
+    cp_commit();
+    PHASE_MARK(6);
+    if (s - win0 + 1 == kRing && s + 1 < nsteps) flush(s);
+  }
+  cp_wait<0>();
+  __syncwarp();
+  flush(nsteps - 1);
+
+  if (lane < beam) {
+    st.pb()[rb + lane] = pb;
+    st.pnb()[rb + lane] = pnb;
+    st.sc()[rb + lane] = sc;
+    st.last()[rb + lane] = last;
+    st.len()[rb + lane] = len;
+    st.h()[rb + lane] = h;
+    st.hp()[rb + lane] = hp;
+    st.msrc()[rb + lane] = msrc;
+  }
+  if (lane == 0) {
+    atomicAdd(&st.hdr()->counters[0], c_steps);
+    atomicAdd(&st.hdr()->counters[1], c_fb);
+    atomicAdd(&st.hdr()->counters[2], c_scan);
+    atomicAdd(&st.hdr()->counters[3], c_hash);
+#ifdef CTCPB_PHASE_PROF
+    for (int i = 0; i < 8; ++i) atomicAdd(&st.hdr()->phase_cycles[i], prof[i]);
+#endif
+    RowHdr rr = rh0;
+    rr.step = step;
+    rr.tcount = mode == 1 ? tcount + nsteps : rh0.tcount;
+    rr.t_prev = t_prev;
+    rr.nlive = nlive;
+    rr.parity = par;
+    st.rows()[b] = rr;
+  }
+}
+
+size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem); }
+
+cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
+                             const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  const size_t smem = step_warp_smem_bytes();
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_step_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int blocks = (st.lay.B + kWPC - 1) / kWPC;
+  k_step_warp<<<blocks, 32 * kWPC, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
+  return cudaGetLastError();
+}
+
+}  // namespace ctcpb

@@ -83,6 +83,7 @@ def lib():
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
                 "ctcpb_read_state": (I, [cfgp, P, SZ, I, I, P, P, P, I, P]),
                 "ctcpb_read_status": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
+                "ctcpb_read_counters": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
                 "ctcpb_select_frames": (I, [cfgp, P, I64, I64, P, I, I, I, P, P, P]),
                 "ctcpb_topk_prepass": (I, [cfgp, P, I64, I, I, P, P, P, P, P, P, P]),
             }
@@ -233,6 +234,12 @@ def read_status(buf: torch.Tensor) -> int:
     v = ctypes.c_uint32()
     _check(lib().ctcpb_read_status(_ptr(buf), ctypes.byref(v)), "read_status")
     return v.value
+
+
+def read_counters(buf: torch.Tensor) -> dict:
+    v = (ctypes.c_uint32 * 4)()
+    _check(lib().ctcpb_read_counters(_ptr(buf), v), "read_counters")
+    return dict(steps=v[0], exhaustive=v[1], frame_scans=v[2], hash_merges=v[3])
 
 
 def select_frames(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None):
