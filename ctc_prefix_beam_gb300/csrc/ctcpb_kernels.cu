@@ -155,161 +155,6 @@ __global__ void __launch_bounds__(256) k_select(View st, const float* __restrict
   if (tid == 0) nsel[b] = n;
 }
 
-// ------------------------------------------------------------------ pre-pass
-// Rank one frame row by one warp: the first L live non-blank labels by
-// (lp desc, id asc), the blank log-prob and the label after the list.
-//
-// Exact top-(L+1) selection:
-//   1. each lane keeps its top-2 label keys over labels lane, lane+32, ...;
-//   2. the (L+1)-th largest of these 64 keys is a lower bound tau of the
-//      (L+1)-th largest key of the row (they are distinct labels);
-//   3. every label with key >= tau is compacted into shared memory and the
-//      compacted set is sorted; it contains the top L+1 by construction;
-//   4. if the compacted set would overflow `lcap`, the warp falls back to
-//      L+1 rounds of "largest key below the previous one".
-constexpr int kRankCap = 512;  // shared keys per ranking warp
-
-__device__ __forceinline__ u64 label_key_at(const float* __restrict__ row, int c, int V, int blank) {
-  if (c >= V || c == blank) return 0ull;
-  float v = rdlp(row[c]);
-  return v > CTCPB_NEG ? lab_key(v, c) : 0ull;
-}
-
-__device__ void rank_row(const float* __restrict__ row, int V, int blank, int L, u64* buf, int lane,
-                         int* o_ids, float* o_lps, int* o_cnt, float* o_lpb, float* o_flp, int* o_fid) {
-  const int K = L + 1;
-  u64 tau = 0ull;
-  if (K <= 64) {
-    u64 k1 = 0ull, k2 = 0ull;
-    for (int c = lane; c < V; c += 32) {
-      u64 key = label_key_at(row, c, V, blank);
-      if (key > k2) {
-        if (key > k1) {
-          k2 = k1;
-          k1 = key;
-        } else {
-          k2 = key;
-        }
-      }
-    }
-    buf[lane] = k1;
-    buf[lane + 32] = k2;
-    __syncwarp();
-    bitonic_desc<32>(buf, 64, lane);
-    tau = buf[K - 1];
-    __syncwarp();
-  }
-  int n = 0;
-  bool ovf = false;
-  for (int c0 = 0; c0 < V; c0 += 32) {
-    const int c = c0 + lane;
-    u64 key = label_key_at(row, c, V, blank);
-    bool take = key != 0ull && key >= tau;
-    unsigned m = __ballot_sync(FULL, take);
-    int tot = __popc(m);
-    if (n + tot > kRankCap) {
-      ovf = true;
-      break;
-    }
-    if (take) buf[n + __popc(m & ((1u << lane) - 1u))] = key;
-    n += tot;
-  }
-  __syncwarp();
-  if (!ovf) {
-    const int P = pow2_at_least(n, 32);
-    for (int i = n + lane; i < P; i += 32) buf[i] = 0ull;
-    __syncwarp();
-    bitonic_desc<32>(buf, P, lane);
-  } else {
-    u64 prev = ~0ull;
-    n = 0;
-    for (int r = 0; r < K; ++r) {
-      u64 best = 0ull;
-      for (int c = lane; c < V; c += 32) {
-        u64 key = label_key_at(row, c, V, blank);
-        if (key < prev && key > best) best = key;
-      }
-      best = warp_max_u64(best);
-      if (best == 0ull) break;
-      if (lane == 0) buf[r] = best;
-      prev = best;
-      n = r + 1;
-    }
-    __syncwarp();
-  }
-  const int cnt = n < L ? n : L;
-  for (int i = lane; i < L; i += 32) {
-    if (i < cnt) {
-      u64 kk = buf[i];
-      o_ids[i] = (int)(~(u32)kk);
-      o_lps[i] = fkey_inv((u32)(kk >> 32));
-    } else {
-      o_ids[i] = -1;
-      o_lps[i] = CTCPB_NEG;
-    }
-  }
-  if (lane == 0) {
-    *o_cnt = cnt;
-    *o_lpb = rdlp(row[blank]);
-    if (n > L) {
-      *o_flp = fkey_inv((u32)(buf[L] >> 32));
-      *o_fid = (int)(~(u32)buf[L]);
-    } else {
-      *o_flp = CTCPB_NEG;
-      *o_fid = -1;
-    }
-  }
-  __syncwarp();
-}
-
-// Records for the decode: item (b, s) ranks the frame of row b's step s.
-// mode 0 (offline): frame sel[b][s], s < nsel[b].
-// mode 1 (streaming): chunk row tile_start + s, s < frames of row b in the tile.
-__global__ void __launch_bounds__(256) k_prepass(View st, const float* __restrict__ lp, long long sb, long long stt,
-                                                 int mode, const int* __restrict__ nframes, int chunk_T,
-                                                 int tile_start, int tile_len) {
-  __shared__ u64 bufs[8][kRankCap];
-  const Layout& Ly = st.lay;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  const long long gw = (long long)blockIdx.x * nw + wid;
-  const long long tw = (long long)gridDim.x * nw;
-  const long long items = (long long)Ly.B * tile_len;
-  for (long long it = gw; it < items; it += tw) {
-    const int b = (int)(it % Ly.B);
-    const int s = (int)(it / Ly.B);
-    const float* row;
-    if (mode == 0) {
-      if (s >= st.nsel()[b]) continue;
-      const int t = st.sel()[(size_t)b * Ly.T_sel + s];
-      row = lp + (long long)b * sb + (long long)t * stt;
-    } else {
-      int nf = nframes ? nframes[b] : chunk_T;
-      nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
-      if (tile_start + s >= nf) continue;
-      row = lp + (long long)b * sb + (long long)(tile_start + s) * stt;
-    }
-    char* r = st.rec(b, s);
-    RecHdr* h = (RecHdr*)r;
-    if (lane == 0) h->t = mode == 0 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
-    rank_row(row, Ly.V, Ly.blank, Ly.L, bufs[wid], lane, rec_ids(r), rec_lps(r, Ly.Lpad), &h->cnt, &h->lpb,
-             &h->front_lp, &h->front_id);
-  }
-}
-
-// Stand-alone pre-pass over R rows (the ctcpb_topk_prepass entry point).
-__global__ void __launch_bounds__(256) k_prepass_rows(const float* __restrict__ lp, long long stride_r, int R, int V,
-                                                      int blank, int L, int* ids, float* lps, int* cnt, float* lpb,
-                                                      float* flp, int* fid) {
-  __shared__ u64 bufs[8][kRankCap];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  for (long long r = (long long)blockIdx.x * nw + wid; r < R; r += (long long)gridDim.x * nw) {
-    rank_row(lp + r * stride_r, V, blank, L, bufs[wid], lane, ids + r * L, lps + r * L, cnt + r, lpb + r, flp + r,
-             fid + r);
-  }
-}
-
 // ------------------------------------------------------------------ step
 //
 // One block of NT threads owns one row for the whole call.  The beam state of
@@ -906,21 +751,6 @@ cudaError_t launch_select(const View& st, const float* lp, long long sb, long lo
                           int mode, float log_thr, int* sel, int* nsel, cudaStream_t s) {
   if (st.lay.B == 0) return cudaSuccess;
   k_select<<<st.lay.B, 256, 0, s>>>(st, lp, sb, stt, lens, T, mode, log_thr, sel, nsel);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prepass(const View& st, const float* lp, long long sb, long long stt, int mode,
-                           const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
-  long long items = (long long)st.lay.B * tile_len;
-  if (items == 0) return cudaSuccess;
-  k_prepass<<<grid_for(items, 8), 256, 0, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prepass_rows(const float* lp, long long stride_r, int R, int V, int blank, int L, int* ids,
-                                float* lps, int* cnt, float* lpb, float* flp, int* fid, cudaStream_t s) {
-  if (R == 0) return cudaSuccess;
-  k_prepass_rows<<<grid_for(R, 8), 256, 0, s>>>(lp, stride_r, R, V, blank, L, ids, lps, cnt, lpb, flp, fid);
   return cudaGetLastError();
 }
 
