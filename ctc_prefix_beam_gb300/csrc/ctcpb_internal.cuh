@@ -187,7 +187,9 @@ __device__ __forceinline__ float dexp(float x) {
   const float LN2_HI = 0.693145751953125f;
   const float LN2_LO = 1.42860682030941723212e-6f;
   const float LOG2E = 1.44269504088896340736f;
-  if (!(x >= -87.0f)) return 0.0f;
+  // branch-free: the reduction runs on a clamped argument, the result is selected
+  const bool under = !(x >= -87.0f);
+  x = under ? -87.0f : x;
   float n = rintf(__fmul_rn(x, LOG2E));
   float r = __fmaf_rn(n, -LN2_HI, x);
   r = __fmaf_rn(n, -LN2_LO, r);
@@ -200,7 +202,7 @@ __device__ __forceinline__ float dexp(float x) {
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
   int ni = (int)n;
-  return __fmul_rn(p, __uint_as_float((unsigned)(ni + 127) << 23));
+  return under ? 0.0f : __fmul_rn(p, __uint_as_float((unsigned)(ni + 127) << 23));
 }
 
 __device__ __forceinline__ float dlog1p(float x) {

@@ -71,10 +71,12 @@ struct __align__(16) WarpSmem {
   float A[32], bpb[32], bpnb[32], rep[32];
   int last[32], len[32];
   int bw[32];
-  float w_sc[32], w_pb[32], w_pnb[32];
-  int w_src[32], w_tok[32], w_gl[32];
   int fold_i[32], fold_c[32];
   int nfold, nkeys;
+  int4 st[32][2];   // bookkeeping of hypothesis k, read by the candidates extending it
+  int4 nst[32][4];  // the new hypothesis of slot r, written by the candidate ranked r
+  u32 fk[32];       // fold key of slot j: (i << 20 | last_j) when l_j = l_i + last_j
+  u32 hk[32];       // prefix hash keys of the extension winners
 };
 
 struct Tables {
@@ -198,7 +200,9 @@ __device__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n
         const float sc = dlse(W.bpb[k], W.bpnb[k]);
         if (sc > CTCPB_NEG) key = cand_key(sc, k, blank);
       } else if (r == 1) {
-        if (W.rep[k] > CTCPB_NEG) key = cand_key(W.rep[k], k, W.last[k]);
+        bool ok = W.rep[k] > CTCPB_NEG;
+        for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == k && W.fold_c[f] == W.last[k]);
+        if (ok) key = cand_key(W.rep[k], k, W.last[k]);
       } else {
         const int c = ids[r - 2];
         bool ok = L < cap && !(L > 0 && c == W.last[k]);
@@ -276,24 +280,41 @@ __device__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n
   return nw;
 }
 
-// Rank of this lane's key among the warp's 32 keys (larger key = better).
-__device__ __forceinline__ int warp_rank(u32 hi, u32 lo, int beam) {
-  int r = 0;
+// Rank of this lane's key among the warp's 32 keys (larger key = better),
+// counting the larger score keys; equal scores among the kept ones are
+// resolved on the full key (score, source slot, token).
+__device__ __forceinline__ int warp_rank(u32 hi, u32 lo, bool live, int beam) {
+  int gt = 0, ge = 0;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) r += __shfl_sync(WFULL, hi, j) > hi;
-  // equal scores among the kept ones leave gaps in the ranks: resolve the
-  // ties on the full key (score, source slot, token)
-  const bool in = hi != 0u && r < beam;
-  const u32 orr = __reduce_or_sync(WFULL, in ? (1u << r) : 0u);
-  if (__popc(orr) != __popc(__ballot_sync(WFULL, in))) {
+  for (int j = 0; j < 32; ++j) {
+    const u32 x = __shfl_sync(WFULL, hi, j);
+    gt += (int)(x > hi);
+    ge += (int)(x >= hi);
+  }
+  int r = gt;
+  if (__any_sync(WFULL, live && gt < beam && ge - gt > 1)) {
     r = 0;
 #pragma unroll 4
     for (int j = 0; j < 32; ++j) {
       const u32 hj = __shfl_sync(WFULL, hi, j), lj = __shfl_sync(WFULL, lo, j);
-      r += (hj > hi) || (hj == hi && lj > lo);
+      r += (int)((hj > hi) || (hj == hi && lj > lo));
     }
   }
   return r;
+}
+
+// Bit j set when a[j] == key, for the 32 words of a (16-byte aligned shared
+// memory), read as eight broadcasts.
+__device__ __forceinline__ unsigned smem_match(const u32* a, u32 key) {
+  const uint4* a4 = reinterpret_cast<const uint4*>(a);
+  unsigned m = 0u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 v = a4[q];
+    m |= ((unsigned)(v.x == key) << (4 * q)) | ((unsigned)(v.y == key) << (4 * q + 1)) |
+         ((unsigned)(v.z == key) << (4 * q + 2)) | ((unsigned)(v.w == key) << (4 * q + 3));
+  }
+  return m;
 }
 
 }  // namespace
@@ -445,7 +466,6 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
     const float* row = row_of(s, hd);
     const bool gap = t > t_prev + 1;
     const bool live = lane < nlive;
-    W.bw[lane] = -1;
     // lp[t_{s+1}][x] for every label x that can be "last" at step s+1: the
     // current lasts (slots 0..beam-1) and this step's list (beam + position)
     if (s + 1 < nsteps) {
@@ -496,11 +516,8 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
     } else {
       // ---- sections 3.4.1-3.4.3 on lanes 0..nlive-1
       const float A = sc;
-      float pbx = pb, pnbx = pnb;
-      if (gap) {  // collapsed-blank correction: lse(pb, pnb) is the stored score
-        pbx = A;
-        pnbx = NEG;
-      }
+      const float pbx = gap ? A : pb;  // collapsed-blank correction: lse(pb, pnb) is the stored score
+      const float pnbx = gap ? NEG : pnb;
       float lpl = NEG;
       {
         const bool gathered = s >= 1 && gl >= 0;
@@ -516,27 +533,34 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
       const int last_i = __shfl_sync(WFULL, last, mil);
       const int len_i = __shfl_sync(WFULL, len, mil);
       const bool rep_i = mi >= 0 && len_i > 0 && last_i == last;
-      float bpnb = stay;
-      if (mi >= 0) bpnb = dlse(stay, dadd(lpl, rep_i ? pb_i : A_i));
-      const float scB = live ? dlse(bpb, bpnb) : NEG;
-      PHASE_MARK(1);
-      // repeat candidate (k, last_k) is folded away when some j has l_j = l_k + last_k
-      int repdead = 0;
-      for (unsigned m = __ballot_sync(WFULL, rep_i); m; m &= m - 1) {
-        const int j = __ffs(m) - 1;
-        if (__shfl_sync(WFULL, mi, j) == lane) repdead = 1;
+      // the extension of l_i folded into this blank slot (NEG when there is none)
+      const float mterm = mi >= 0 ? dadd(lpl, rep_i ? pb_i : A_i) : NEG;
+      const float Rrep = (live && len > 0 && len < cap) ? dadd(lpl, pbx) : NEG;
+      // (i, last) names the candidate this slot absorbs; a unique dummy otherwise
+      const u32 foldk = mi >= 0 ? (((u32)mi << 20) | (u32)last) : (0x80000000u | (u32)lane);
+      if (live) {
+        W.st[lane][0] = make_int4(last, len, (int)h, (int)hp);
+        W.st[lane][1] = make_int4(origin, lo, nnew, msrc);
       }
-      const float Rrep = (live && len > 0 && len < cap && !repdead) ? dadd(lpl, pbx) : NEG;
-      // ordinary candidates (i, last_j) folded into j's blank slot, as a mask per list position
-      u32 excl = 0u;
-      const unsigned fm = __ballot_sync(WFULL, mi >= 0 && !rep_i);
-      for (unsigned m = fm; m; m &= m - 1) {
-        const int j = __ffs(m) - 1;
-        const int ij = __shfl_sync(WFULL, mi, j);
-        const int cj = __shfl_sync(WFULL, last, j);
-        if (lane < cnt && my_id == cj) excl |= 1u << ij;
-      }
+      W.fk[lane] = foldk;
       const int n = nlive;
+      // proof bound of this hypothesis: what its best label outside the set scores
+      float bnd = NEG;
+      {
+        const int q = live ? tb.qcnt[n][lane] : 0;
+        const float nxt = __shfl_sync(WFULL, my_lp, q & 31);
+        if (live && len < cap) {
+          if (q < cnt)
+            bnd = dadd(nxt, A);
+          else if (hd->front_lp > NEG)
+            bnd = dadd(hd->front_lp, A);
+        }
+      }
+      __syncwarp();
+      PHASE_MARK(1);
+      // blank slot (3.4.1-3.4.3), branch-free so it overlaps the candidates below
+      const float bpnb = __any_sync(WFULL, mi >= 0) ? dlse(stay, mterm) : stay;  // dlse(stay, NEG) == stay
+      const float scB = live ? dlse(bpb, bpnb) : NEG;
 
       // candidate of this lane: its hypothesis' blank slot (lane < n) or
       // listed label qp of hypothesis qk
@@ -549,26 +573,23 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
         const float Rk = __shfl_sync(WFULL, Rrep, qk);
         const int cq = __shfl_sync(WFULL, my_id, qp);
         const float lq = __shfl_sync(WFULL, my_lp, qp);
-        const u32 exq = __shfl_sync(WFULL, excl, qp);
         cs = NEG;
-        csrc = 0;
+        csrc = lane < n ? lane : 0;
         ctok = blank;
-        cgl = -1;
-        if (lane < n) {
-          cs = scB;
-          csrc = lane;
-          cgl = lane;
-        } else if (valid && qp < cnt && lenk < cap) {
+        cgl = lane < n ? lane : -1;
+        if (lane >= n && valid && qp < cnt && lenk < cap) {
           csrc = qk;
           ctok = cq;
           if (lenk > 0 && cq == lastk) {
             cs = Rk;
             cgl = qk;
-          } else if (!((exq >> qk) & 1u)) {
+          } else {
             cs = dadd(lq, Ak);
             cgl = beam + qp;
           }
         }
+        // a candidate (k, c) with l_k + c == l_j of a live j is folded into j's blank slot
+        if (lane >= n && cs > NEG && smem_match(W.fk, ((u32)csrc << 20) | (u32)ctok) != 0u) cs = NEG;
       };
 
       // ---- round 1: the staircase
@@ -576,28 +597,20 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
         const unsigned short qm = lane >= n ? tb.qmap[n][lane] : (unsigned short)0xffff;
         make_cand(qm != 0xffff, qm == 0xffff ? 0 : (qm >> 8), qm == 0xffff ? 0 : (qm & 31));
       }
+      if (lane < n) cs = scB;
       bool clive = cs > NEG;
       u32 hi = clive ? fkey(cs) : 0u;
       u32 lo_k = clive ? ~(((u32)csrc << 20) | (u32)ctok) : 0u;
-      int r = warp_rank(hi, lo_k, beam);
-      nw = __popc(__ballot_sync(WFULL, clive && r < beam));
+      int r = warp_rank(hi, lo_k, clive, beam);
+      bool won = clive && r < beam;
+      nw = __popc(__ballot_sync(WFULL, won));
       PHASE_MARK(2);
-      u32 sstar = 0u;
-      if (nw == beam) sstar = __shfl_sync(WFULL, hi, __ffs(__ballot_sync(WFULL, clive && r == beam - 1)) - 1);
       bool proven;
+      u32 sstar;
       {
-        const int q = live ? tb.qcnt[n][lane] : 0;
-        const float nxt = __shfl_sync(WFULL, my_lp, q & 31);
-        bool bad = false;
-        if (live && len < cap) {
-          float bnd = NEG;
-          if (q < cnt)
-            bnd = dadd(nxt, A);
-          else if (hd->front_lp > NEG)
-            bnd = dadd(hd->front_lp, A);
-          bad = bnd > NEG && (nw < beam || fkey(bnd) >= sstar);
-        }
-        proven = !__any_sync(WFULL, bad);
+        const unsigned lastm = __ballot_sync(WFULL, won && r == beam - 1);
+        sstar = __shfl_sync(WFULL, hi, lastm ? __ffs(lastm) - 1 : 0);
+        proven = !__any_sync(WFULL, bnd > NEG && (nw < beam || fkey(bnd) >= sstar));
       }
       PHASE_MARK(3);
       bool generic = false;
@@ -643,11 +656,13 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
               }
             }
             make_cand(lane >= n && idx < total, qk, qp);
+            if (lane < n) cs = scB;
             clive = cs > NEG;
             hi = clive ? fkey(cs) : 0u;
             lo_k = clive ? ~(((u32)csrc << 20) | (u32)ctok) : 0u;
-            r = warp_rank(hi, lo_k, beam);
-            nw = __popc(__ballot_sync(WFULL, clive && r < beam));
+            r = warp_rank(hi, lo_k, clive, beam);
+            won = clive && r < beam;
+            nw = __popc(__ballot_sync(WFULL, won));
           }
         }
       }
@@ -660,75 +675,82 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
           W.last[lane] = last;
           W.len[lane] = len;
         }
-        const unsigned fmm = __ballot_sync(WFULL, mi >= 0 && !rep_i);
-        if (mi >= 0 && !rep_i) {
+        const unsigned fmm = __ballot_sync(WFULL, mi >= 0);
+        if (mi >= 0) {
           const int f = __popc(fmm & ((1u << lane) - 1u));
           W.fold_i[f] = mi;
           W.fold_c[f] = last;
         }
         if (lane == 0) W.nfold = __popc(fmm);
+        W.bw[lane] = -1;
         __syncwarp();
         const u64 thr = nw == beam ? ((u64)sstar << 32) : 0ull;
         nw = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr, c_scan);
+        const u64 key = lane < nw ? W.keys[lane] : 0ull;
+        const int gsrc = ck_src(key), gtk = ck_tok(key);
+        const bool gisb = gtk == blank;
+        if (lane < nw && gisb) W.bw[gsrc] = lane;
+        __syncwarp();
         if (lane < nw) {
-          const u64 key = W.keys[lane];
-          const int src = ck_src(key), tk = ck_tok(key);
-          const bool isb = tk == blank;
-          W.w_sc[lane] = ck_score(key);
-          W.w_src[lane] = src;
-          W.w_tok[lane] = tk;
-          W.w_pb[lane] = isb ? W.bpb[src] : NEG;
-          W.w_pnb[lane] = isb ? W.bpnb[src] : ck_score(key);
-          W.w_gl[lane] = (isb || (W.len[src] > 0 && tk == W.last[src])) ? src : -1;
+          const int4 s0 = W.st[gsrc][0], s1 = W.st[gsrc][1];
+          const float gsc = ck_score(key);
+          float npb = gisb ? W.bpb[gsrc] : NEG, npnb = gisb ? W.bpnb[gsrc] : gsc;
+          if (gap) {
+            npb = gsc;
+            npnb = NEG;
+          }
+          const int gm = gisb ? (s1.w >= 0 ? W.bw[s1.w] : -1) : W.bw[gsrc];
+          const int ggl = (gisb || (s0.y > 0 && gtk == s0.x)) ? gsrc : -1;
+          W.hist[s - win0][lane] = ((u32)gsrc << 24) | ((u32)gtk & 0xffffffu);
+          W.nst[lane][0] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(gsc), gisb ? s0.x : gtk);
+          W.nst[lane][1] = make_int4(gisb ? s0.y : s0.y + 1, gisb ? s0.z : (int)h32((u32)s0.z, gtk),
+                                     gisb ? s0.w : s0.z, s1.x);
+          W.nst[lane][2] = make_int4(s1.y, s1.z + (gisb ? 0 : 1), ggl, gm);
+          W.nst[lane][3] = make_int4(gisb ? 1 : 0, 0, 0, 0);
         }
-      } else if (clive && r < beam) {
-        W.w_sc[r] = cs;
-        W.w_src[r] = csrc;
-        W.w_tok[r] = ctok;
-        W.w_pb[r] = lane < n ? bpb : NEG;
-        W.w_pnb[r] = lane < n ? bpnb : cs;
-        W.w_gl[r] = cgl;
+      } else {
+        // ---- section 3.4.5: the candidate ranked r writes new slot r
+        // merge source of the new slot: the blank winner of this slot's merge
+        // source (a blank slot) or of its source (an extension)
+        const int rw = won ? r : -1;
+        const int mq = lane < n ? mi : csrc;
+        const int nm0 = __shfl_sync(WFULL, rw, mq < 0 ? 0 : mq);
+        if (won) {
+          const bool isb = lane < n;
+          const int4 s0 = W.st[csrc][0], s1 = W.st[csrc][1];
+          float npb = isb ? bpb : NEG, npnb = isb ? bpnb : cs;
+          if (gap) {
+            npb = cs;
+            npnb = NEG;
+          }
+          W.hist[s - win0][r] = ((u32)csrc << 24) | ((u32)ctok & 0xffffffu);
+          W.nst[r][0] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(cs), isb ? s0.x : ctok);
+          W.nst[r][1] = make_int4(isb ? s0.y : s0.y + 1, isb ? s0.z : (int)h32((u32)s0.z, ctok), isb ? s0.w : s0.z,
+                                  s1.x);
+          W.nst[r][2] = make_int4(s1.y, s1.z + (isb ? 0 : 1), cgl, mq < 0 ? -1 : nm0);
+          W.nst[r][3] = make_int4(isb ? 1 : 0, 0, 0, 0);
+        }
       }
       __syncwarp();
       PHASE_MARK(4);
-
-      // ---- section 3.4.5: commit
-      const bool wl = lane < nw;
-      const int src = wl ? W.w_src[lane] : 0;
-      const int tk = wl ? W.w_tok[lane] : blank;
-      const float score = wl ? W.w_sc[lane] : NEG;
-      const int s_last = __shfl_sync(WFULL, last, src);
-      const int s_len = __shfl_sync(WFULL, len, src);
-      const u32 s_h = __shfl_sync(WFULL, h, src), s_hp = __shfl_sync(WFULL, hp, src);
-      const int s_origin = __shfl_sync(WFULL, origin, src);
-      const int s_lo = __shfl_sync(WFULL, lo, src);
-      const int s_nnew = __shfl_sync(WFULL, nnew, src);
-      const int s_msrc = __shfl_sync(WFULL, msrc, src);
-      const bool isb = tk == blank;
-      isb_w = isb;
-      if (wl) {
-        pb = isb ? W.w_pb[lane] : NEG;
-        pnb = isb ? W.w_pnb[lane] : score;
-        if (gap) {
-          pb = score;
-          pnb = NEG;
-        }
-        sc = score;
-        last = isb ? s_last : tk;
-        len = isb ? s_len : s_len + 1;
-        h = isb ? s_h : h32(s_h, tk);
-        hp = isb ? s_hp : s_h;
-        origin = s_origin;
-        lo = s_lo;
-        nnew = s_nnew + (isb ? 0 : 1);
-        gl = W.w_gl[lane];
-        W.hist[s - win0][lane] = ((u32)src << 24) | ((u32)tk & 0xffffffu);
-        if (isb) W.bw[src] = lane;
+      if (lane < nw) {
+        const int4 n0 = W.nst[lane][0], n1 = W.nst[lane][1], n2 = W.nst[lane][2], n3 = W.nst[lane][3];
+        pb = __int_as_float(n0.x);
+        pnb = __int_as_float(n0.y);
+        sc = __int_as_float(n0.z);
+        last = n0.w;
+        len = n1.x;
+        h = (u32)n1.y;
+        hp = (u32)n1.z;
+        origin = n1.w;
+        lo = n2.x;
+        nnew = n2.y;
+        gl = n2.z;
+        msrc = n2.w;
+        isb_w = n3.x != 0;
+      } else {
+        msrc = -1;
       }
-      __syncwarp();
-      int nm = -1;
-      if (wl) nm = isb ? (s_msrc >= 0 ? W.bw[s_msrc] : -1) : W.bw[src];
-      msrc = nm;
     }
 
     // ---- the one merge relation the sources cannot show: a blank winner
@@ -738,11 +760,10 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
       const bool wl = lane < nw;
       const bool want = wl && step > 0 && isb_w && msrc < 0 && len >= 1;
       if (__any_sync(WFULL, want)) {
-        const u32 key = !wl ? (0x80000000u | (u32)lane)
-                            : (isb_w ? (hp ^ ((u32)(len - 1) * kGold)) : (h ^ ((u32)len * kGold)));
-        const unsigned grp = __match_any_sync(WFULL, key);
+        W.hk[lane] = h ^ ((u32)len * kGold);
         const unsigned extm = __ballot_sync(WFULL, wl && !isb_w);
-        const unsigned match = want ? (grp & extm) : 0u;
+        __syncwarp();
+        const unsigned match = want ? (smem_match(W.hk, hp ^ ((u32)(len - 1) * kGold)) & extm) : 0u;
         const bool cand = want && match != 0u;
         if (__any_sync(WFULL, cand)) {
           ++c_hash;
