@@ -193,12 +193,12 @@ int ctcpb_read_status(const void* ws_or_state, uint32_t* device_status) {
   return CTCPB_OK;
 }
 
-int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[4]) {
+int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[5]) {
   if (!ws_or_state || !counters) return CTCPB_ENULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return CTCPB_ECUDA;
   Header h;
   if (cudaMemcpy(&h, ws_or_state, sizeof(Header), cudaMemcpyDeviceToHost) != cudaSuccess) return CTCPB_ECUDA;
-  for (int i = 0; i < 4; ++i) counters[i] = h.counters[i];
+  for (int i = 0; i < 5; ++i) counters[i] = h.counters[i];
   return CTCPB_OK;
 }
 

@@ -33,8 +33,8 @@ struct Header {
   u32 magic, version;
   int32_t B, V, beam, cap, paged, page_size, blank, list_len, tile, pad0;
   u32 status;  // CTCPB_DEV_* bits
-  u32 counters[4];  // decode steps, exhaustive selections, full-frame scans, hash-proposed merges
-  u32 pad2;
+  u32 counters[5];  // decode steps, unproven first sets, exhaustive selections, full-frame scans,
+                    // hash-proposed merges
   u64 phase_cycles[8];  // CTCPB_PHASE_PROF builds: clock64 cycles per step phase, summed over rows
   u32 pad1[30];
 };

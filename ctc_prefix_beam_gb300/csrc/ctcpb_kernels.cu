@@ -90,7 +90,7 @@ __global__ void k_init(View st) {
     h->B = L.B; h->V = L.V; h->beam = L.beam; h->cap = L.cap; h->paged = L.paged;
     h->page_size = L.page_size; h->blank = L.blank; h->list_len = L.L; h->tile = L.tile;
     h->status = 0u;
-    for (int i = 0; i < 4; ++i) h->counters[i] = 0u;
+    for (int i = 0; i < 5; ++i) h->counters[i] = 0u;
     for (int i = 0; i < 8; ++i) h->phase_cycles[i] = 0ull;
   }
   for (size_t b = tid; b < (size_t)L.B; b += nthr) {
@@ -772,7 +772,7 @@ static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, 
 cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                         int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (st.lay.B == 0) return cudaSuccess;
-  if (st.lay.beam <= 32 && !st.lay.paged)
+  if (st.lay.beam <= 32 && !st.lay.paged && step_warp_fits(st.lay))
     return launch_step_warp(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   if (st.lay.beam <= 32) return launch_step_t<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   return launch_step_t<128>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);

@@ -14,6 +14,9 @@ cudaError_t launch_prepass_rows(const float* lp, long long stride_r, int R, int 
                                 float* lps, int* cnt, float* lpb, float* flp, int* fid, cudaStream_t s);
 cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                         int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+// The warp-per-row step kernel takes flat storage, beam <= 32 and a ranked
+// record of at most 32 + 8*68 bytes (list length <= 66).
+bool step_warp_fits(const Layout& lay);
 cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s);
 cudaError_t launch_output(const View& st, int nbest, int* out_tokens, int* out_lengths, float* out_scores,

@@ -16,6 +16,8 @@
 // Rows that are not 16-byte aligned, lists longer than 63 labels, and
 // compactions past the buffer use the plain per-warp ranking (rank_row).
 #include "ctcpb_internal.cuh"
+#include "ctcpb_async.cuh"
+#include "ctcpb_sort.cuh"
 #include "ctcpb_kernels.h"
 
 namespace ctcpb {
@@ -232,44 +234,6 @@ namespace {
 
 #define RFULL 0xffffffffu
 constexpr int kCandCap = 512;          // compacted labels per warp (= rank_row's buffer)
-constexpr long long kWaitSpins = 1ll << 18;  // bounded mbarrier wait (each try sleeps <= 2 us)
-
-__device__ __forceinline__ unsigned saddr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(u64* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(saddr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(u64* bar, unsigned bytes) {
-  asm volatile(
-      "{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(saddr(bar)),
-      "r"(bytes)
-      : "memory");
-}
-// bulk copy of one row into shared memory, completing on the barrier
-__device__ __forceinline__ void tma_row(void* dst, const void* src, unsigned bytes, u64* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(saddr(dst)),
-      "l"(src), "r"(bytes), "r"(saddr(bar))
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_test(u64* bar, unsigned parity) {
-  unsigned ok;
-  // the suspend hint lets the warp sleep in the barrier until the copy lands
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 2000;\n selp.u32 %0, 1, 0, "
-      "p;\n}\n"
-      : "=r"(ok)
-      : "r"(saddr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait for a phase of a barrier; false if it gave up
-__device__ __forceinline__ bool mbar_wait(u64* bar, unsigned parity) {
-  for (long long i = 0; i < kWaitSpins; ++i) {
-    if (mbar_test(bar, parity)) return true;
-  }
-  return false;
-}
-
 // Where one ranked row goes.
 struct RankDst {
   int* ids;
@@ -334,41 +298,6 @@ struct RowItems {
   }
 };
 
-
-// Bitonic sort, descending, of 32*E keys held E per lane (element i = lane +
-// 32*e); one shuffle per element per stage for strides below 32.
-template <int E, class T>
-__device__ __forceinline__ void warp_sort_desc(T (&v)[E], int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32 * E; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j >= 32) {
-        const int je = j >> 5;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          if ((e & je) == 0) {
-            const int i = lane + 32 * e;
-            const bool desc = (i & k) == 0;
-            const T a = v[e], b = v[e + je];
-            const bool sw = desc ? (a < b) : (a > b);
-            v[e] = sw ? b : a;
-            v[e + je] = sw ? a : b;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int i = lane + 32 * e;
-          const T p = __shfl_xor_sync(RFULL, v[e], j);
-          const bool desc = (i & k) == 0, lower = (i & j) == 0;
-          const bool keep_max = lower == desc;
-          v[e] = keep_max ? (p > v[e] ? p : v[e]) : (p < v[e] ? p : v[e]);
-        }
-      }
-    }
-  }
-}
 
 // Passes 1-3 over one staged row (all lanes): compacts every label that can
 // be in the top L+1 into `cand`; returns their count, or -1 when they
@@ -547,7 +476,7 @@ __global__ void __launch_bounds__(512, 1) k_rank_tma(Items items, int V, int bla
   bool have = advance(&it, &row, &t);
   if (have && lane == 0) {
     mbar_arrive_tx(bar, bytes);
-    tma_row(buf, row, bytes, bar);
+    bulk_g2s(buf, row, bytes, bar);
   }
   while (have) {
     if (!mbar_wait(bar, phase)) {
@@ -574,7 +503,7 @@ __global__ void __launch_bounds__(512, 1) k_rank_tma(Items items, int V, int bla
     if (have && lane == 0) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_arrive_tx(bar, bytes);
-      tma_row(buf, row, bytes, bar);
+      bulk_g2s(buf, row, bytes, bar);
     }
     if (n >= 0) rank_finish(cand, n, L, lpb, lane, dc);
     __syncwarp();

@@ -29,11 +29,14 @@
 // materialised into the flat double-buffered rows: each hypothesis' row in the
 // other parity = its origin row's prefix + the labels it gained in the window.
 // lp[t][last] for step s+1 is gathered at the top of step s over every label
-// that can be "last" then (the current lasts and step s's list), with cp.async
-// into shared memory, so the loads overlap step s; ranked-frame records are
-// prefetched kRecRing steps ahead the same way.
+// that can be "last" then (the current lasts and step s's list) into
+// shared memory by 4-byte asynchronous copies, so the loads overlap step s; ranked-frame
+// records arrive kRecGrp at a time by bulk copies into two alternating
+// shared-memory groups, one group ahead.
+#include "ctcpb_async.cuh"
 #include "ctcpb_internal.cuh"
 #include "ctcpb_kernels.h"
+#include "ctcpb_sort.cuh"
 
 namespace ctcpb {
 namespace {
@@ -55,20 +58,19 @@ namespace {
 #endif
 
 constexpr int kRing = 128;            // steps of history between materialisations
-constexpr int kRecRing = 4;           // prefetched ranked-frame records
+constexpr int kRecGrp = 4;            // ranked-frame records per bulk copy (two groups in flight)
 constexpr int kWPC = 4;               // rows (warps) per block
 constexpr int kGenCap = 512;          // keys of the exhaustive selection
-constexpr int kMaxRec = 32 + 8 * 68;  // record bytes for beam <= 32 (L <= 66)
 constexpr int kGath = 128;            // gathered log-probs per frame (beam + L <= 98)
+constexpr int kMaxRec = 32 + 8 * 68;  // record bytes for beam <= 32 (L <= 66)
 constexpr u32 kH32 = 2166136261u;     // prefix hash of the empty prefix
 constexpr u32 kGold = 0x9e3779b9u;
 
 struct __align__(16) WarpSmem {
   u64 keys[kGenCap];
   u32 hist[kRing][32];
-  char rec[kRecRing][kMaxRec];
-  float gath[2][kGath];
-  float A[32], bpb[32], bpnb[32], rep[32];
+  char rec[2][kRecGrp * kMaxRec];  // two groups of records, rec_bytes apart
+  float A[32], bpb[32], bpnb[32], scb[32], rep[32];
   int last[32], len[32];
   int bw[32];
   int fold_i[32], fold_c[32];
@@ -77,6 +79,8 @@ struct __align__(16) WarpSmem {
   int4 nst[32][4];  // the new hypothesis of slot r, written by the candidate ranked r
   u32 fk[32];       // fold key of slot j: (i << 20 | last_j) when l_j = l_i + last_j
   u32 hk[32];       // prefix hash keys of the extension winners
+  u64 rbar[2];      // completion of the record groups
+  float gath[2][kGath];  // lp[t][slot] of the next step, slot = hypothesis or beam + list position
 };
 
 struct Tables {
@@ -84,19 +88,12 @@ struct Tables {
   unsigned char qcnt[33][32];  // nlive -> hyp -> listed labels of that hyp in the round-1 set
 };
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  unsigned s = (unsigned)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
-}
+// 4-byte asynchronous copy global -> shared (completes at cp_wait_all)
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  unsigned s = (unsigned)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(src) : "memory");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(saddr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // 32-bit prefix hash (FNV-1a step).  Equal prefixes hash equal; a collision
 // only costs an extra exact comparison.
@@ -108,7 +105,7 @@ __device__ __forceinline__ int wpow2(int n, int lo) {
   return p;
 }
 
-__device__ void warp_bitonic(u64* a, int P, int lane) {
+__device__ __noinline__ void warp_bitonic(u64* a, int P, int lane) {
   for (int k = 2; k <= P; k <<= 1)
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = lane; i < P; i += 32) {
@@ -124,6 +121,31 @@ __device__ void warp_bitonic(u64* a, int P, int lane) {
       }
       __syncwarp();
     }
+}
+
+// Sort W.keys[0 .. m) descending, m = 32 + W.nkeys (the keys after m, up to
+// the next power of two, are zero): in registers up to 128 keys, else in
+// shared memory.
+__device__ __noinline__ void sort_keys(WarpSmem& W, int m, int lane) {
+  if (m <= 64) {
+    u64 v[2] = {W.keys[lane], W.keys[32 + lane]};
+    warp_sort_desc<2>(v, lane);
+    W.keys[lane] = v[0];
+    W.keys[32 + lane] = v[1];
+  } else if (m <= 128) {
+    u64 v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = W.keys[lane + 32 * e];
+    warp_sort_desc<4>(v, lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) W.keys[lane + 32 * e] = v[e];
+  } else {
+    const int P = wpow2(m, 64);
+    for (int i = m + lane; i < P; i += 32) W.keys[i] = 0ull;
+    __syncwarp();
+    warp_bitonic(W.keys, P, lane);
+  }
+  __syncwarp();
 }
 
 // Staircase tables, one lane per nlive value (lane 0 also does nlive = 32).
@@ -177,51 +199,54 @@ __device__ __forceinline__ void push_key(WarpSmem& W, u64 key, u64 thr, int lane
 
 // Every candidate of the step with key >= thr, the frame's unlisted labels
 // included when the list cannot bound them, sorted; W.keys[0..beam) holds the
-// best.  Returns how many are live.
-__device__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n, int beam, int cap, int blank, int V,
-                                   const float* __restrict__ row, int lane, u64 thr, u32& scans) {
+// best.  Returns how many are live, plus 1 << 16 when the frame's unlisted
+// labels were scanned.
+__device__ __noinline__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n, int beam, int cap,
+                                                int blank, int V, const float* __restrict__ row, int lane, u64 thr) {
   const RecHdr* h = (const RecHdr*)rec;
   const int cnt = h->cnt;
   const int* ids = (const int*)(rec + 32);
   const float* lps = (const float*)(rec + 32 + 4 * Lpad);
   const int nfold = W.nfold;
+  int scanned = 0;
   for (int i = lane; i < kGenCap; i += 32) W.keys[i] = 0ull;
   if (lane == 0) W.nkeys = 0;
   __syncwarp();
-  const int stride = cnt + 2;
-  const int NC = n * stride;
-  for (int base = 0; base < NC; base += 32) {
-    const int g = base + lane;
-    u64 key = 0ull;
-    if (g < NC) {
-      const int k = g / stride, r = g - k * stride;
-      const int L = W.len[k];
-      if (r == 0) {
-        const float sc = dlse(W.bpb[k], W.bpnb[k]);
-        if (sc > CTCPB_NEG) key = cand_key(sc, k, blank);
-      } else if (r == 1) {
-        bool ok = W.rep[k] > CTCPB_NEG;
-        for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == k && W.fold_c[f] == W.last[k]);
-        if (ok) key = cand_key(W.rep[k], k, W.last[k]);
-      } else {
-        const int c = ids[r - 2];
-        bool ok = L < cap && !(L > 0 && c == W.last[k]);
-        for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == k && W.fold_c[f] == c);
-        if (ok) {
-          const float sc = dadd(lps[r - 2], W.A[k]);
-          if (sc > CTCPB_NEG) key = cand_key(sc, k, c);
-        }
-      }
+  // blank slots and repeat candidates, one hypothesis per lane
+  for (int k0 = 0; k0 < n; k0 += 32) {
+    const int k = k0 + lane;
+    u64 kb = 0ull, kr = 0ull;
+    if (k < n) {
+      if (W.scb[k] > CTCPB_NEG) kb = cand_key(W.scb[k], k, blank);
+      bool ok = W.rep[k] > CTCPB_NEG;
+      for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == k && W.fold_c[f] == W.last[k]);
+      if (ok) kr = cand_key(W.rep[k], k, W.last[k]);
     }
-    push_key(W, key, thr, lane);
+    push_key(W, kb, thr, lane);
+    push_key(W, kr, thr, lane);
+  }
+  // listed labels, one hypothesis at a time, one list position per lane
+  for (int k = 0; k < n; ++k) {
+    const int L = W.len[k], lastk = W.last[k];
+    const float Ak = W.A[k];
+    for (int p0 = 0; p0 < cnt; p0 += 32) {
+      const int p = p0 + lane;
+      u64 key = 0ull;
+      if (p < cnt && L < cap) {
+        const int c = ids[p];
+        bool ok = !(L > 0 && c == lastk);
+        for (int f = 0; f < nfold && ok; ++f) ok = !(W.fold_i[f] == k && W.fold_c[f] == c);
+        const float sc = dadd(lps[p], Ak);
+        if (ok && sc > CTCPB_NEG) key = cand_key(sc, k, c);
+      }
+      push_key(W, key, thr, lane);
+    }
   }
   const float front_lp = h->front_lp;
   if (front_lp > CTCPB_NEG) {
     // the running beam-th key so far bounds what an unlisted label must reach
-    int P = wpow2(32 + W.nkeys, 64);
-    for (int i = 32 + W.nkeys + lane; i < P; i += 32) W.keys[i] = 0ull;
-    __syncwarp();
-    warp_bitonic(W.keys, P, lane);
+    const int P = wpow2(32 + W.nkeys, 64);
+    sort_keys(W, 32 + W.nkeys, lane);
     for (int i = 32 + lane; i < P; i += 32) W.keys[i] = 0ull;
     if (lane == 0) W.nkeys = 0;
     __syncwarp();
@@ -238,7 +263,7 @@ __device__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n
     }
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(WFULL, amax, o));
     if (__any_sync(WFULL, bad)) {
-      ++scans;
+      scanned = 1;
       const u64 kfront = lab_key(front_lp, h->front_id);
       for (int c0 = 0; c0 < V; c0 += 128) {
         float v[4];
@@ -271,28 +296,22 @@ __device__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n
       }
     }
   }
-  const int P = wpow2(32 + W.nkeys, 64);
-  for (int i = 32 + W.nkeys + lane; i < P; i += 32) W.keys[i] = 0ull;
-  __syncwarp();
-  warp_bitonic(W.keys, P, lane);
+  sort_keys(W, 32 + W.nkeys, lane);
   int nw = 0;
   for (int w = 0; w < beam; ++w) nw += W.keys[w] != 0ull;
-  return nw;
+  return nw | (scanned << 16);
 }
 
 // Rank of this lane's key among the warp's 32 keys (larger key = better),
-// counting the larger score keys; equal scores among the kept ones are
-// resolved on the full key (score, source slot, token).
+// counting the larger score keys; equal scores among the kept ones (two kept
+// lanes with one rank) are resolved on the full key (score, source slot, token).
 __device__ __forceinline__ int warp_rank(u32 hi, u32 lo, bool live, int beam) {
-  int gt = 0, ge = 0;
+  int r = 0;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const u32 x = __shfl_sync(WFULL, hi, j);
-    gt += (int)(x > hi);
-    ge += (int)(x >= hi);
-  }
-  int r = gt;
-  if (__any_sync(WFULL, live && gt < beam && ge - gt > 1)) {
+  for (int j = 0; j < 32; ++j) r += (int)(__shfl_sync(WFULL, hi, j) > hi);
+  const bool in = live && r < beam;
+  const u32 orr = __reduce_or_sync(WFULL, in ? (1u << r) : 0u);
+  if (__popc(orr) != __popc(__ballot_sync(WFULL, in))) {
     r = 0;
 #pragma unroll 4
     for (int j = 0; j < 32; ++j) {
@@ -303,24 +322,250 @@ __device__ __forceinline__ int warp_rank(u32 hi, u32 lo, bool live, int beam) {
   return r;
 }
 
-// Bit j set when a[j] == key, for the 32 words of a (16-byte aligned shared
-// memory), read as eight broadcasts.
-__device__ __forceinline__ unsigned smem_match(const u32* a, u32 key) {
+// Bit j set when a[j] == key, for j < cnt (<= KB) of the words of a (16-byte
+// aligned shared memory): KB/4 broadcast reads, no branches.
+template <int KB>
+__device__ __forceinline__ unsigned smem_match(const u32* a, u32 key, int cnt) {
   const uint4* a4 = reinterpret_cast<const uint4*>(a);
   unsigned m = 0u;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < KB / 4; ++q) {
     const uint4 v = a4[q];
     m |= ((unsigned)(v.x == key) << (4 * q)) | ((unsigned)(v.y == key) << (4 * q + 1)) |
          ((unsigned)(v.z == key) << (4 * q + 2)) | ((unsigned)(v.w == key) << (4 * q + 3));
   }
-  return m;
+  return cnt >= 32 ? m : (m & ((1u << cnt) - 1u));
+}
+
+// Round 2 of the step selection: hypothesis k's first ck_k listed labels are
+// every listed candidate of k scoring >= sstar (the list is sorted).  Returns
+// -1 when they do not fit the lanes after the n blank slots or the list cannot
+// bound what it leaves out; else this lane's candidate as
+// (valid << 16 | k << 8 | list position).
+__device__ __noinline__ int round2_plan(float A, int len, bool live, float my_lp, int cnt, int n, int cap,
+                                        float front_lp, u32 sstar, int lane) {
+  const int lim = cnt < 32 ? cnt : 32;
+  int ck = 0;
+  for (int k = 0; k < n; ++k) {
+    const float a = __shfl_sync(WFULL, A, k);
+    const int lk = __shfl_sync(WFULL, len, k);
+    const bool p = lane < lim && fkey(dadd(my_lp, a)) >= sstar;
+    const int c = lk < cap ? __popc(__ballot_sync(WFULL, p)) : 0;
+    if (lane == k) ck = c;
+  }
+  // the list must bound everything it leaves out
+  bool over = false;
+  if (live && ck == lim && len < cap) {
+    if (cnt > 32)
+      over = true;
+    else if (front_lp > CTCPB_NEG && fkey(dadd(front_lp, A)) >= sstar)
+      over = true;
+  }
+  int pre = ck;  // inclusive prefix over hypotheses
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(WFULL, pre, o);
+    if (lane >= o) pre += v;
+  }
+  const int total = __shfl_sync(WFULL, pre, n > 0 ? n - 1 : 0);
+  if (__any_sync(WFULL, over) || n + total > 32) return -1;
+  int qk = 0, qp = 0;
+  const int idx = lane - n;
+  for (int k = 0; k < n; ++k) {
+    const int e = __shfl_sync(WFULL, pre, k);
+    const int c = __shfl_sync(WFULL, ck, k);
+    if (idx >= e - c && idx < e) {
+      qk = k;
+      qp = idx - (e - c);
+    }
+  }
+  const bool valid = lane >= n && idx < total;
+  return ((valid ? 1 : 0) << 16) | (qk << 8) | qp;
+}
+
+// Materialise the history ring (steps win0..s_last) into the other parity of
+// the flat rows: each hypothesis' row = its origin row's first lo labels + the
+// nnew labels it gained in the window.  rows[p]: this row's hypotheses in
+// parity p, ldseq labels apart.
+__device__ __noinline__ void flush_rows(WarpSmem& W, int* rows0, int* rows1, int ldseq, int lane, int nlive, int blank,
+                                        int par, int win0, int s_last, int origin, int lo, int nnew) {
+  int* const from_rows = par ? rows1 : rows0;
+  int* const to_rows = par ? rows0 : rows1;
+  int slot = lane, rem = nnew;
+  for (int r = s_last - win0; r >= 0; --r) {
+    const u32 e = W.hist[r][slot & 31];
+    const int tk = (int)(e & 0xffffffu);
+    if (lane < nlive && tk != blank) {
+      --rem;
+      to_rows[(size_t)lane * ldseq + lo + rem] = tk;
+    }
+    slot = (int)(e >> 24);
+  }
+  // origin prefixes, four rows at a time with every load issued before the stores
+  for (int w0 = 0; w0 < nlive; w0 += 4) {
+    int4 v[4][2];
+    int nv[4], o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int w = w0 + u < nlive ? w0 + u : w0;
+      o[u] = w0 + u < nlive ? __shfl_sync(WFULL, origin, w) : -1;
+      const int c = __shfl_sync(WFULL, lo, w);
+      nv[u] = o[u] >= 0 ? (c >> 2) : 0;
+      const int4* from = o[u] >= 0 ? reinterpret_cast<const int4*>(from_rows + (size_t)o[u] * ldseq) : nullptr;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (lane + 32 * i < nv[u]) v[u][i] = from[lane + 32 * i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (o[u] < 0) continue;
+      int4* to = reinterpret_cast<int4*>(to_rows + (size_t)(w0 + u) * ldseq);
+      const int4* from = reinterpret_cast<const int4*>(from_rows + (size_t)o[u] * ldseq);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (lane + 32 * i < nv[u]) to[lane + 32 * i] = v[u][i];
+      for (int x = 64 + lane; x < nv[u]; x += 32) to[x] = from[x];
+      const int c = __shfl_sync(WFULL, lo, w0 + u);
+      if (lane < (c & 3))
+        to_rows[(size_t)(w0 + u) * ldseq + (nv[u] << 2) + lane] = from_rows[(size_t)o[u] * ldseq + (nv[u] << 2) + lane];
+    }
+  }
+  __syncwarp();
+}
+
+// A step candidate: score, source slot, token, gathered-slot index of its
+// next-step lp[last] (-1: read it directly).
+struct Cand {
+  float cs;
+  int src, tok, gl;
+};
+
+// This lane's candidate: its hypothesis' blank slot (lane < n, score scB) or
+// listed label qp of hypothesis qk; folded candidates (some live j has
+// l_j = l_k + c) are dead.
+template <int KB>
+__device__ __forceinline__ Cand make_cand(const WarpSmem& W, bool valid, int qk, int qp, float A, int last, int len,
+                                          float Rrep, int my_id, float my_lp, float scB, int n, int cnt, int cap,
+                                          int beam, int blank, bool anyfold, int lane) {
+  const float Ak = __shfl_sync(WFULL, A, qk);
+  const int lastk = __shfl_sync(WFULL, last, qk);
+  const int lenk = __shfl_sync(WFULL, len, qk);
+  const float Rk = __shfl_sync(WFULL, Rrep, qk);
+  const int cq = __shfl_sync(WFULL, my_id, qp);
+  const float lq = __shfl_sync(WFULL, my_lp, qp);
+  Cand c;
+  c.cs = lane < n ? scB : CTCPB_NEG;
+  c.src = lane < n ? lane : 0;
+  c.tok = blank;
+  c.gl = lane < n ? lane : -1;
+  if (lane >= n && valid && qp < cnt && lenk < cap) {
+    c.src = qk;
+    c.tok = cq;
+    if (lenk > 0 && cq == lastk) {  // the repeat path: pb only
+      c.cs = Rk;
+      c.gl = qk;
+    } else {
+      c.cs = dadd(lq, Ak);
+      c.gl = beam + qp < kGath ? beam + qp : -1;
+    }
+    if (anyfold && c.cs > CTCPB_NEG && smem_match<KB>(W.fk, ((u32)c.src << 20) | (u32)c.tok, n) != 0u)
+      c.cs = CTCPB_NEG;
+  }
+  return c;
+}
+
+// New slot r := candidate c (source bookkeeping from W.st), its history entry
+// in ring row hrow.  nm: the new slot's merge source.
+__device__ __forceinline__ void commit_slot(WarpSmem& W, int r, const Cand& c, bool isb, float bpb, float bpnb,
+                                            bool gap, int nm, int hrow) {
+  const int4 s0 = W.st[c.src][0], s1 = W.st[c.src][1];
+  float npb = isb ? bpb : CTCPB_NEG, npnb = isb ? bpnb : c.cs;
+  if (gap) {
+    npb = c.cs;
+    npnb = CTCPB_NEG;
+  }
+  W.hist[hrow][r] = ((u32)c.src << 24) | ((u32)c.tok & 0xffffffu);
+  W.nst[r][0] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(c.cs), isb ? s0.x : c.tok);
+  W.nst[r][1] = make_int4(isb ? s0.y : s0.y + 1, isb ? s0.z : (int)h32((u32)s0.z, c.tok), isb ? s0.w : s0.z, s1.x);
+  W.nst[r][2] = make_int4(s1.y, s1.z + (isb ? 0 : 1), c.gl, nm);
+  W.nst[r][3] = make_int4(isb ? 1 : 0, 0, 0, 0);
+  // prefix key of an extension winner for the merge check (a blank winner's
+  // dummy can only cause an extra exact comparison)
+  W.hk[r] = isb ? 0xffffffffu : (h32((u32)s0.z, c.tok) ^ ((u32)(s0.y + 1) * kGold));
+}
+
+// The selection when the first candidate set did not prove it: round 2 (every
+// listed candidate scoring >= sstar, when they fit the warp), else the
+// exhaustive selection.  Writes the winners' new slots like the fast path.
+// Returns nw | exhaustive << 8 | frame scanned << 9.
+template <int KB>
+__device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const float* row, u32 sstar, int nw1, float A,
+                                        int last, int len, bool live, float Rrep, int my_id, float my_lp, float scB,
+                                        float bpb, float bpnb, int mi, bool anyfold, int n, int cnt, int cap, int beam,
+                                        int blank, int V, int Lpad, bool gap, int hrow, int lane) {
+  const RecHdr* hd = (const RecHdr*)Rc;
+  if (nw1 == beam) {
+    const int plan = round2_plan(A, len, live, my_lp, cnt, n, cap, hd->front_lp, sstar, lane);
+    if (plan >= 0) {
+      const Cand c = make_cand<KB>(W, (plan >> 16) != 0, (plan >> 8) & 0xff, plan & 0xff, A, last, len, Rrep, my_id,
+                                   my_lp, scB, n, cnt, cap, beam, blank, anyfold, lane);
+      const bool clive = c.cs > CTCPB_NEG;
+      const u32 hi = clive ? fkey(c.cs) : 0u;
+      const int r = warp_rank(hi, clive ? ~(((u32)c.src << 20) | (u32)c.tok) : 0u, clive, beam);
+      const bool won = clive && r < beam;
+      const int nw = __popc(__ballot_sync(WFULL, won));
+      const int mq = lane < n ? mi : c.src;
+      const int nm = __shfl_sync(WFULL, won ? r : -1, mq < 0 ? 0 : mq);
+      if (won) commit_slot(W, r, c, lane < n, bpb, bpnb, gap, mq < 0 ? -1 : nm, hrow);
+      return nw;
+    }
+  }
+  // ---- exhaustive selection over the frame's list
+  if (live) {
+    W.A[lane] = A;
+    W.bpb[lane] = bpb;
+    W.bpnb[lane] = bpnb;
+    W.scb[lane] = scB;
+    W.rep[lane] = Rrep;
+    W.last[lane] = last;
+    W.len[lane] = len;
+  }
+  const unsigned fmm = __ballot_sync(WFULL, mi >= 0);
+  if (mi >= 0) {
+    const int f = __popc(fmm & ((1u << lane) - 1u));
+    W.fold_i[f] = mi;
+    W.fold_c[f] = last;
+  }
+  if (lane == 0) W.nfold = __popc(fmm);
+  W.bw[lane] = -1;
+  __syncwarp();
+  const u64 thr = nw1 == beam ? ((u64)sstar << 32) : 0ull;
+  const int res = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr);
+  const int nw = res & 0xffff;
+  const u64 key = lane < nw ? W.keys[lane] : 0ull;
+  const int gsrc = ck_src(key), gtk = ck_tok(key);
+  const bool gisb = gtk == blank;
+  if (lane < nw && gisb) W.bw[gsrc] = lane;
+  __syncwarp();
+  if (lane < nw) {
+    Cand c;
+    c.cs = ck_score(key);
+    c.src = gsrc;
+    c.tok = gtk;
+    const int4 s0 = W.st[gsrc][0], s1 = W.st[gsrc][1];
+    c.gl = (gisb || (s0.y > 0 && gtk == s0.x)) ? gsrc : -1;
+    const int gm = gisb ? (s1.w >= 0 ? W.bw[s1.w] : -1) : W.bw[gsrc];
+    commit_slot(W, lane, c, gisb, gisb ? W.bpb[gsrc] : CTCPB_NEG, gisb ? W.bpnb[gsrc] : CTCPB_NEG, gap, gm, hrow);
+  }
+  return nw | (1 << 8) | ((res >> 16) << 9);
 }
 
 }  // namespace
 
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* __restrict__ lp, long long sb,
+// KB: beam bucket (8, 16 or 32), the bound of the per-hypothesis compares.
+template <int KB>
+__global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float* __restrict__ lp, long long sb,
                                                          long long stt, int mode, const int* __restrict__ nframes,
                                                          int chunk_T, int tile_start, int tile_len) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -377,86 +622,76 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
   }
   int origin = lane, lo = len, nnew = 0, gl = -1;
   int win0 = 0;  // call step index of the ring's first entry
-  u32 c_steps = 0, c_fb = 0, c_scan = 0, c_hash = 0;
+  u32 c_steps = 0, c_fb = 0, c_gen = 0, c_scan = 0, c_hash = 0;
 #ifdef CTCPB_PHASE_PROF
   u64 prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   long long prof_t0 = clock64();
 #endif
   const float* lpb_row = lp + (long long)b * sb;
-  const int rec_chunks = (int)(Ly.rec_bytes / 16);
-
   auto row_of = [&](int s, const RecHdr* hd) -> const float* {
     return lpb_row + (long long)(mode == 0 ? hd->t : tile_start + s) * stt;
   };
-  auto prefetch_rec = [&](int s) {
-    if (s < nsteps) {
-      const char* src = st.rec(b, s);
-      char* dst = W.rec[s % kRecRing];
-      for (int c = lane; c < rec_chunks; c += 32) cp_async16(dst + 16 * c, src + 16 * c);
+  char* const rec_g = st.rec(b, 0);  // this row's records, rec_bytes apart
+  const unsigned rbytes = (unsigned)Ly.rec_bytes;
+  auto rec_of = [&](int s) -> const char* { return W.rec[(s / kRecGrp) & 1] + (s % kRecGrp) * rbytes; };
+  int g_issued = 0, g_waited = 0;
+  // lane 0: bulk copy of record group g (steps g*kRecGrp ...) into its half
+  auto fetch_group = [&](int g) {
+    const int s0 = g * kRecGrp;
+    if (s0 < nsteps) {
+      const unsigned nb = (unsigned)(nsteps - s0 < kRecGrp ? nsteps - s0 : kRecGrp) * rbytes;
+      mbar_arrive_tx(&W.rbar[g & 1], nb);
+      bulk_g2s(W.rec[g & 1], rec_g + (size_t)s0 * rbytes, nb, &W.rbar[g & 1]);
     }
+  };
+  // all lanes: wait for group g (the (g/2)-th use of its barrier)
+  auto wait_group = [&](int g) -> bool {
+    const bool ok = mbar_wait(&W.rbar[g & 1], (unsigned)((g >> 1) & 1));
+    g_waited = g + 1;
+    return ok;
+  };
+  // a wait ran out: report it, give the copies in flight a last bounded wait
+  auto bail = [&]() {
+    if (lane == 0) atomicOr(&st.hdr()->status, CTCPB_DEV_TIMEOUT);
+    for (int g = g_waited; g < g_issued; ++g) mbar_wait(&W.rbar[g & 1], (unsigned)((g >> 1) & 1));
+    cp_wait_all();
   };
 
   // Materialise the ring into the other parity of the flat rows.
+  int* const rows0 = st.clist(0, b, 0);
+  int* const rows1 = st.clist(1, b, 0);
   auto flush = [&](int s_last) {
-    const int np = par ^ 1;
-    int slot = lane, rem = nnew;
-    for (int r = s_last - win0; r >= 0; --r) {
-      const u32 e = W.hist[r][slot & 31];
-      const int tk = (int)(e & 0xffffffu);
-      if (lane < nlive && tk != blank) {
-        --rem;
-        st.clist(np, b, lane)[lo + rem] = tk;
-      }
-      slot = (int)(e >> 24);
-    }
-    // origin prefixes, four rows at a time with every load issued before the stores
-    for (int w0 = 0; w0 < nlive; w0 += 4) {
-      int4 v[4][2];
-      int nv[4], o[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int w = w0 + u < nlive ? w0 + u : w0;
-        o[u] = w0 + u < nlive ? __shfl_sync(WFULL, origin, w) : -1;
-        const int c = __shfl_sync(WFULL, lo, w);
-        nv[u] = o[u] >= 0 ? (c >> 2) : 0;
-        const int4* from = o[u] >= 0 ? reinterpret_cast<const int4*>(st.clist(par, b, o[u])) : nullptr;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (lane + 32 * i < nv[u]) v[u][i] = from[lane + 32 * i];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (o[u] < 0) continue;
-        int4* to = reinterpret_cast<int4*>(st.clist(np, b, w0 + u));
-        const int4* from = reinterpret_cast<const int4*>(st.clist(par, b, o[u]));
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (lane + 32 * i < nv[u]) to[lane + 32 * i] = v[u][i];
-        for (int x = 64 + lane; x < nv[u]; x += 32) to[x] = from[x];
-        const int c = __shfl_sync(WFULL, lo, w0 + u);
-        if (lane < (c & 3))
-          st.clist(np, b, w0 + u)[(nv[u] << 2) + lane] = st.clist(par, b, o[u])[(nv[u] << 2) + lane];
-      }
-    }
-    par = np;
+    flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par, win0, s_last, origin, lo, nnew);
+    par ^= 1;
     origin = lane;
     lo = len;
     nnew = 0;
     win0 = s_last + 1;
-    __syncwarp();
   };
 
-  for (int d = 0; d < kRecRing; ++d) {
-    prefetch_rec(d);
-    cp_commit();
+  if (lane == 0) {
+    mbar_init(&W.rbar[0]);
+    mbar_init(&W.rbar[1]);
+    mbar_init_fence();
+    fetch_group(0);
+    fetch_group(1);
+  }
+  g_issued = nsteps > kRecGrp ? 2 : 1;
+  __syncwarp();
+  if (!wait_group(0)) {
+    bail();
+    return;
   }
 
   for (int s = 0; s < nsteps; ++s) {
     PHASE_MARK(7);
-    cp_wait<1>();
-    __syncwarp();
+    // step s+1 opens the next group: its record is read by this step's gather
+    if ((s + 1) % kRecGrp == 0 && s + 1 < nsteps && !wait_group((s + 1) / kRecGrp)) {
+      bail();
+      return;
+    }
     PHASE_MARK(0);
-    const char* Rc = W.rec[s % kRecRing];
+    const char* Rc = rec_of(s);
     const RecHdr* hd = (const RecHdr*)Rc;
     const int cnt = hd->cnt;
     const float lpb = hd->lpb;
@@ -466,19 +701,23 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
     const float* row = row_of(s, hd);
     const bool gap = t > t_prev + 1;
     const bool live = lane < nlive;
+    // lp[t][last] of this lane's hypothesis, gathered by the previous step
+    cp_wait_all();
+    __syncwarp();
+    const float gcur = gl >= 0 ? W.gath[s & 1][gl] : 0.0f;
     // lp[t_{s+1}][x] for every label x that can be "last" at step s+1: the
     // current lasts (slots 0..beam-1) and this step's list (beam + position)
     if (s + 1 < nsteps) {
-      const char* R1 = W.rec[(s + 1) % kRecRing];
-      const float* row1 = row_of(s + 1, (const RecHdr*)R1);
+      const float* row1 = row_of(s + 1, (const RecHdr*)rec_of(s + 1));
+      const int* ids = (const int*)(Rc + 32);
       float* gdst = W.gath[(s + 1) & 1];
-      for (int x = lane; x < beam + cnt; x += 32) {
+      for (int x = lane; x < beam + cnt && x < kGath; x += 32) {
         // x < beam <= 32 means x == lane: this lane's own hypothesis
-        const int lab = x < beam ? ((live && len > 0) ? last : -1) : ((const int*)(Rc + 32))[x - beam];
+        const int lab = x < beam ? ((live && len > 0) ? last : -1) : ids[x - beam];
         if (lab >= 0) cp_async4(gdst + x, row1 + lab);
       }
+      cp_commit();
     }
-    cp_commit();
 
     int nw;
     bool isb_w = false;
@@ -515,18 +754,26 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
       gl = -1;
     } else {
       // ---- sections 3.4.1-3.4.3 on lanes 0..nlive-1
+      const int mi = live ? msrc : -1;
+      // (i, last) names the candidate this slot absorbs; a unique dummy otherwise
+      const u32 foldk = mi >= 0 ? (((u32)mi << 20) | (u32)last) : (0x80000000u | (u32)lane);
+      if (live) {
+        W.st[lane][0] = make_int4(last, len, (int)h, (int)hp);
+        W.st[lane][1] = make_int4(origin, lo, nnew, msrc);
+      }
+      W.fk[lane] = foldk;
+      __syncwarp();
+      PHASE_MARK(1);
       const float A = sc;
       const float pbx = gap ? A : pb;  // collapsed-blank correction: lse(pb, pnb) is the stored score
       const float pnbx = gap ? NEG : pnb;
       float lpl = NEG;
       {
         const bool gathered = s >= 1 && gl >= 0;
-        const float g = gathered ? W.gath[s & 1][gl] : 0.0f;
-        if (live && len > 0) lpl = gathered ? rdlp(g) : rdlp(__ldg(row + last));
+        if (live && len > 0) lpl = gathered ? rdlp(gcur) : rdlp(__ldg(row + last));
       }
       const float bpb = dadd(lpb, A);
       const float stay = (live && len > 0 && !gap) ? dadd(lpl, pnbx) : NEG;
-      const int mi = live ? msrc : -1;
       const int mil = mi < 0 ? 0 : mi;
       const float A_i = __shfl_sync(WFULL, A, mil);
       const float pb_i = __shfl_sync(WFULL, pbx, mil);
@@ -536,14 +783,11 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
       // the extension of l_i folded into this blank slot (NEG when there is none)
       const float mterm = mi >= 0 ? dadd(lpl, rep_i ? pb_i : A_i) : NEG;
       const float Rrep = (live && len > 0 && len < cap) ? dadd(lpl, pbx) : NEG;
-      // (i, last) names the candidate this slot absorbs; a unique dummy otherwise
-      const u32 foldk = mi >= 0 ? (((u32)mi << 20) | (u32)last) : (0x80000000u | (u32)lane);
-      if (live) {
-        W.st[lane][0] = make_int4(last, len, (int)h, (int)hp);
-        W.st[lane][1] = make_int4(origin, lo, nnew, msrc);
-      }
-      W.fk[lane] = foldk;
       const int n = nlive;
+      // blank slot (3.4.1-3.4.3), branch-free so it overlaps the candidates below
+      const bool anyfold = __any_sync(WFULL, mi >= 0);
+      const float bpnb = anyfold ? dlse(stay, mterm) : stay;  // dlse(stay, NEG) == stay
+      const float scB = live ? dlse(bpb, bpnb) : NEG;
       // proof bound of this hypothesis: what its best label outside the set scores
       float bnd = NEG;
       {
@@ -556,180 +800,36 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
             bnd = dadd(hd->front_lp, A);
         }
       }
-      __syncwarp();
-      PHASE_MARK(1);
-      // blank slot (3.4.1-3.4.3), branch-free so it overlaps the candidates below
-      const float bpnb = __any_sync(WFULL, mi >= 0) ? dlse(stay, mterm) : stay;  // dlse(stay, NEG) == stay
-      const float scB = live ? dlse(bpb, bpnb) : NEG;
-
-      // candidate of this lane: its hypothesis' blank slot (lane < n) or
-      // listed label qp of hypothesis qk
-      float cs;
-      int csrc, ctok, cgl;
-      auto make_cand = [&](bool valid, int qk, int qp) {
-        const float Ak = __shfl_sync(WFULL, A, qk);
-        const int lastk = __shfl_sync(WFULL, last, qk);
-        const int lenk = __shfl_sync(WFULL, len, qk);
-        const float Rk = __shfl_sync(WFULL, Rrep, qk);
-        const int cq = __shfl_sync(WFULL, my_id, qp);
-        const float lq = __shfl_sync(WFULL, my_lp, qp);
-        cs = NEG;
-        csrc = lane < n ? lane : 0;
-        ctok = blank;
-        cgl = lane < n ? lane : -1;
-        if (lane >= n && valid && qp < cnt && lenk < cap) {
-          csrc = qk;
-          ctok = cq;
-          if (lenk > 0 && cq == lastk) {
-            cs = Rk;
-            cgl = qk;
-          } else {
-            cs = dadd(lq, Ak);
-            cgl = beam + qp;
-          }
-        }
-        // a candidate (k, c) with l_k + c == l_j of a live j is folded into j's blank slot
-        if (lane >= n && cs > NEG && smem_match(W.fk, ((u32)csrc << 20) | (u32)ctok) != 0u) cs = NEG;
-      };
 
       // ---- round 1: the staircase
-      {
-        const unsigned short qm = lane >= n ? tb.qmap[n][lane] : (unsigned short)0xffff;
-        make_cand(qm != 0xffff, qm == 0xffff ? 0 : (qm >> 8), qm == 0xffff ? 0 : (qm & 31));
-      }
-      if (lane < n) cs = scB;
-      bool clive = cs > NEG;
-      u32 hi = clive ? fkey(cs) : 0u;
-      u32 lo_k = clive ? ~(((u32)csrc << 20) | (u32)ctok) : 0u;
-      int r = warp_rank(hi, lo_k, clive, beam);
-      bool won = clive && r < beam;
+      const unsigned short qm = lane >= n ? tb.qmap[n][lane] : (unsigned short)0xffff;
+      const Cand c = make_cand<KB>(W, qm != 0xffff, qm == 0xffff ? 0 : (qm >> 8), qm == 0xffff ? 0 : (qm & 31), A,
+                                   last, len, Rrep, my_id, my_lp, scB, n, cnt, cap, beam, blank, anyfold, lane);
+      const bool clive = c.cs > NEG;
+      const u32 hi = clive ? fkey(c.cs) : 0u;
+      const int r = warp_rank(hi, clive ? ~(((u32)c.src << 20) | (u32)c.tok) : 0u, clive, beam);
+      const bool won = clive && r < beam;
       nw = __popc(__ballot_sync(WFULL, won));
       PHASE_MARK(2);
-      bool proven;
-      u32 sstar;
+      // ---- section 3.4.5: the candidate ranked r writes new slot r, before
+      // the proof is known (an unproven step rewrites the slots)
       {
-        const unsigned lastm = __ballot_sync(WFULL, won && r == beam - 1);
-        sstar = __shfl_sync(WFULL, hi, lastm ? __ffs(lastm) - 1 : 0);
-        proven = !__any_sync(WFULL, bnd > NEG && (nw < beam || fkey(bnd) >= sstar));
+        const int mq = lane < n ? mi : c.src;
+        const int nm = __shfl_sync(WFULL, won ? r : -1, mq < 0 ? 0 : mq);
+        if (won) commit_slot(W, r, c, lane < n, bpb, bpnb, gap, mq < 0 ? -1 : nm, s - win0);
       }
+      const unsigned lastm = __ballot_sync(WFULL, won && r == beam - 1);
+      const u32 sstar = __shfl_sync(WFULL, hi, lastm ? __ffs(lastm) - 1 : 0);
+      const bool proven = !__any_sync(WFULL, bnd > NEG && (nw < beam || fkey(bnd) >= sstar));
       PHASE_MARK(3);
-      bool generic = false;
       if (!proven) {
+        __syncwarp();  // the optimistic slots are written before they are rewritten
         ++c_fb;
-        // ---- round 2: every listed candidate scoring >= tau (tau = sstar)
-        generic = nw < beam;
-        if (!generic) {
-          const int lim = cnt < 32 ? cnt : 32;
-          int ck = 0;
-          for (int k = 0; k < n; ++k) {
-            const float a = __shfl_sync(WFULL, A, k);
-            const int lk = __shfl_sync(WFULL, len, k);
-            const bool p = lane < lim && fkey(dadd(my_lp, a)) >= sstar;
-            const int c = lk < cap ? __popc(__ballot_sync(WFULL, p)) : 0;
-            if (lane == k) ck = c;
-          }
-          // the list must bound everything it leaves out
-          bool over = false;
-          if (live && ck == lim && len < cap) {
-            if (cnt > 32)
-              over = true;
-            else if (hd->front_lp > NEG && fkey(dadd(hd->front_lp, A)) >= sstar)
-              over = true;
-          }
-          int pre = ck;  // inclusive prefix over hypotheses
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(WFULL, pre, o);
-            if (lane >= o) pre += v;
-          }
-          const int total = __shfl_sync(WFULL, pre, n > 0 ? n - 1 : 0);
-          generic = __any_sync(WFULL, over) || n + total > 32;
-          if (!generic) {
-            int qk = 0, qp = 0;
-            const int idx = lane - n;
-            for (int k = 0; k < n; ++k) {
-              const int e = __shfl_sync(WFULL, pre, k);
-              const int c = __shfl_sync(WFULL, ck, k);
-              if (idx >= e - c && idx < e) {
-                qk = k;
-                qp = idx - (e - c);
-              }
-            }
-            make_cand(lane >= n && idx < total, qk, qp);
-            if (lane < n) cs = scB;
-            clive = cs > NEG;
-            hi = clive ? fkey(cs) : 0u;
-            lo_k = clive ? ~(((u32)csrc << 20) | (u32)ctok) : 0u;
-            r = warp_rank(hi, lo_k, clive, beam);
-            won = clive && r < beam;
-            nw = __popc(__ballot_sync(WFULL, won));
-          }
-        }
-      }
-      if (generic) {
-        if (live) {
-          W.A[lane] = A;
-          W.bpb[lane] = bpb;
-          W.bpnb[lane] = bpnb;
-          W.rep[lane] = Rrep;
-          W.last[lane] = last;
-          W.len[lane] = len;
-        }
-        const unsigned fmm = __ballot_sync(WFULL, mi >= 0);
-        if (mi >= 0) {
-          const int f = __popc(fmm & ((1u << lane) - 1u));
-          W.fold_i[f] = mi;
-          W.fold_c[f] = last;
-        }
-        if (lane == 0) W.nfold = __popc(fmm);
-        W.bw[lane] = -1;
-        __syncwarp();
-        const u64 thr = nw == beam ? ((u64)sstar << 32) : 0ull;
-        nw = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr, c_scan);
-        const u64 key = lane < nw ? W.keys[lane] : 0ull;
-        const int gsrc = ck_src(key), gtk = ck_tok(key);
-        const bool gisb = gtk == blank;
-        if (lane < nw && gisb) W.bw[gsrc] = lane;
-        __syncwarp();
-        if (lane < nw) {
-          const int4 s0 = W.st[gsrc][0], s1 = W.st[gsrc][1];
-          const float gsc = ck_score(key);
-          float npb = gisb ? W.bpb[gsrc] : NEG, npnb = gisb ? W.bpnb[gsrc] : gsc;
-          if (gap) {
-            npb = gsc;
-            npnb = NEG;
-          }
-          const int gm = gisb ? (s1.w >= 0 ? W.bw[s1.w] : -1) : W.bw[gsrc];
-          const int ggl = (gisb || (s0.y > 0 && gtk == s0.x)) ? gsrc : -1;
-          W.hist[s - win0][lane] = ((u32)gsrc << 24) | ((u32)gtk & 0xffffffu);
-          W.nst[lane][0] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(gsc), gisb ? s0.x : gtk);
-          W.nst[lane][1] = make_int4(gisb ? s0.y : s0.y + 1, gisb ? s0.z : (int)h32((u32)s0.z, gtk),
-                                     gisb ? s0.w : s0.z, s1.x);
-          W.nst[lane][2] = make_int4(s1.y, s1.z + (gisb ? 0 : 1), ggl, gm);
-          W.nst[lane][3] = make_int4(gisb ? 1 : 0, 0, 0, 0);
-        }
-      } else {
-        // ---- section 3.4.5: the candidate ranked r writes new slot r
-        // merge source of the new slot: the blank winner of this slot's merge
-        // source (a blank slot) or of its source (an extension)
-        const int rw = won ? r : -1;
-        const int mq = lane < n ? mi : csrc;
-        const int nm0 = __shfl_sync(WFULL, rw, mq < 0 ? 0 : mq);
-        if (won) {
-          const bool isb = lane < n;
-          const int4 s0 = W.st[csrc][0], s1 = W.st[csrc][1];
-          float npb = isb ? bpb : NEG, npnb = isb ? bpnb : cs;
-          if (gap) {
-            npb = cs;
-            npnb = NEG;
-          }
-          W.hist[s - win0][r] = ((u32)csrc << 24) | ((u32)ctok & 0xffffffu);
-          W.nst[r][0] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(cs), isb ? s0.x : ctok);
-          W.nst[r][1] = make_int4(isb ? s0.y : s0.y + 1, isb ? s0.z : (int)h32((u32)s0.z, ctok), isb ? s0.w : s0.z,
-                                  s1.x);
-          W.nst[r][2] = make_int4(s1.y, s1.z + (isb ? 0 : 1), cgl, mq < 0 ? -1 : nm0);
-          W.nst[r][3] = make_int4(isb ? 1 : 0, 0, 0, 0);
-        }
+        const int res = slow_select<KB>(W, Rc, row, sstar, nw, A, last, len, live, Rrep, my_id, my_lp, scB, bpb, bpnb,
+                                        mi, anyfold, n, cnt, cap, beam, blank, V, Lpad, gap, s - win0, lane);
+        nw = res & 0xff;
+        c_gen += (u32)((res >> 8) & 1);
+        c_scan += (u32)((res >> 9) & 1);
       }
       __syncwarp();
       PHASE_MARK(4);
@@ -760,10 +860,7 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
       const bool wl = lane < nw;
       const bool want = wl && step > 0 && isb_w && msrc < 0 && len >= 1;
       if (__any_sync(WFULL, want)) {
-        W.hk[lane] = h ^ ((u32)len * kGold);
-        const unsigned extm = __ballot_sync(WFULL, wl && !isb_w);
-        __syncwarp();
-        const unsigned match = want ? (smem_match(W.hk, hp ^ ((u32)(len - 1) * kGold)) & extm) : 0u;
+        const unsigned match = want ? smem_match<KB>(W.hk, hp ^ ((u32)(len - 1) * kGold), nw) : 0u;
         const bool cand = want && match != 0u;
         if (__any_sync(WFULL, cand)) {
           ++c_hash;
@@ -791,13 +888,20 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
     t_prev = t;
     ++step;
     ++c_steps;
-    // ---- prefetch the record kRecRing steps ahead
-    prefetch_rec(s + kRecRing);
-    cp_commit();
+    // ---- the group of step s is used up: refill its half two groups ahead
+    if (s % kRecGrp == kRecGrp - 1) {
+      __syncwarp();
+      const int g = s / kRecGrp + 2;
+      if (lane == 0 && g * kRecGrp < nsteps) {
+        fence_proxy_async();
+        fetch_group(g);
+      }
+      if (g * kRecGrp < nsteps) g_issued = g + 1;
+    }
     PHASE_MARK(6);
     if (s - win0 + 1 == kRing && s + 1 < nsteps) flush(s);
   }
-  cp_wait<0>();
+  cp_wait_all();
   __syncwarp();
   flush(nsteps - 1);
 
@@ -814,8 +918,9 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
   if (lane == 0) {
     atomicAdd(&st.hdr()->counters[0], c_steps);
     atomicAdd(&st.hdr()->counters[1], c_fb);
-    atomicAdd(&st.hdr()->counters[2], c_scan);
-    atomicAdd(&st.hdr()->counters[3], c_hash);
+    atomicAdd(&st.hdr()->counters[2], c_gen);
+    atomicAdd(&st.hdr()->counters[3], c_scan);
+    atomicAdd(&st.hdr()->counters[4], c_hash);
 #ifdef CTCPB_PHASE_PROF
     for (int i = 0; i < 8; ++i) atomicAdd(&st.hdr()->phase_cycles[i], prof[i]);
 #endif
@@ -829,20 +934,32 @@ __global__ void __launch_bounds__(32 * kWPC) k_step_warp(View st, const float* _
   }
 }
 
+bool step_warp_fits(const Layout& lay) {
+  return lay.beam <= 32 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
+}
+
 size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem); }
 
-cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
+template <int KB>
+static cudaError_t launch_kb(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   const size_t smem = step_warp_smem_bytes();
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_step_warp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_step_warp<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int blocks = (st.lay.B + kWPC - 1) / kWPC;
-  k_step_warp<<<blocks, 32 * kWPC, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
+  k_step_warp<KB><<<blocks, 32 * kWPC, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
   return cudaGetLastError();
+}
+
+cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
+                             const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  if (st.lay.beam <= 8) return launch_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  if (st.lay.beam <= 16) return launch_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return launch_kb<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }
 
 }  // namespace ctcpb

@@ -88,12 +88,13 @@ typedef struct ctcpb_config {
 
 /*
  * Diagnostic counters of the last call on a workspace or state (synchronises
- * the device): [0] decode steps of the warp path, [1] steps whose fast
- * candidate set could not prove the selection (exhaustive selection over the
- * frame's list), [2] steps that also scored every unlisted label of the
- * frame, [3] merges proposed by prefix hashes and checked on stored tokens.
+ * the device): [0] decode steps of the warp path, [1] steps whose first
+ * candidate set could not prove the selection, [2] of those, steps that fell
+ * back to an exhaustive selection over the frame's list, [3] steps that also
+ * scored every unlisted label of the frame, [4] merges proposed by prefix
+ * hashes and checked on stored tokens.
  */
-int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[4]);
+int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[5]);
 
 /* Human-readable text for a host status code. */
 const char* ctcpb_status_string(int status);

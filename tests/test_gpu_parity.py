@@ -112,6 +112,8 @@ EDGE = [
     dict(beam=10, max_seq_len=1),
     dict(beam=10, list_len=1),             # list of `beam` labels: frequent full-row re-ranks
     dict(beam=3, list_len=3, V=40),        # short list on a wider vocabulary
+    dict(beam=4, list_len=66, V=100),      # longest list the warp-per-row kernel takes
+    dict(beam=10, list_len=80, V=200),     # a longer list goes to the block kernel
     dict(beam=10, list_len=2, paged=True, page_size=3),
     dict(beam=6, paged=True, page_size=1),
     dict(beam=6, blank_threshold=0.0),     # no frame decoded
