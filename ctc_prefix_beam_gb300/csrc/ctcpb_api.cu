@@ -2,6 +2,7 @@
 // workspace/state layout, and the launch sequence of each call.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 #include "ctcpb.h"
 #include "ctcpb_internal.cuh"
@@ -60,6 +61,20 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? CTCPB_OK : CTCPB_ECUDA; }
     if (e_ != cudaSuccess) return CTCPB_ECUDA; \
   } while (0)
 
+// Pre-pass and steps of one tile in one cooperative launch when the device and
+// the problem allow it; CTCPB_NO_FUSE=1 in the environment turns it off.
+bool try_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
+               int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  static const bool off = [] {
+    const char* e = std::getenv("CTCPB_NO_FUSE");
+    return e && e[0] == '1';
+  }();
+  if (off) return false;
+  if (launch_fused(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s) == cudaSuccess) return true;
+  cudaGetLastError();  // a refused cooperative launch: take the two-kernel path
+  return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -113,8 +128,11 @@ int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, 
     const float log_thr = mode == 1 ? (float)std::log((double)thr) : 0.0f;
     if (stage_mask & CTCPB_STAGE_SELECT)
       TRY(launch_select(st, log_prob, stride_b, stride_t, seq_lengths, T, mode, log_thr, st.sel(), st.nsel(), s));
-    if (stage_mask & CTCPB_STAGE_RANK) TRY(launch_prepass(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s));
-    if (stage_mask & CTCPB_STAGE_STEPS) TRY(launch_step(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s));
+    const bool both = (stage_mask & CTCPB_STAGE_RANK) && (stage_mask & CTCPB_STAGE_STEPS);
+    if (!(both && try_fused(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s))) {
+      if (stage_mask & CTCPB_STAGE_RANK) TRY(launch_prepass(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s));
+      if (stage_mask & CTCPB_STAGE_STEPS) TRY(launch_step(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s));
+    }
   }
   if (stage_mask & CTCPB_STAGE_OUTPUT)
     TRY(launch_output(st, cfg->nbest, out_tokens, out_lengths, out_scores, out_len, s));
@@ -164,6 +182,7 @@ int ctcpb_stream_step_chunk(const ctcpb_config* cfg, void* state, size_t state_b
   cudaStream_t s = (cudaStream_t)stream;
   for (int t0 = 0; t0 < chunk_T; t0 += kStreamTile) {
     const int tl = chunk_T - t0 < kStreamTile ? chunk_T - t0 : kStreamTile;
+    if (try_fused(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s)) continue;
     TRY(launch_prepass(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s));
     TRY(launch_step(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s));
   }
@@ -193,12 +212,13 @@ int ctcpb_read_status(const void* ws_or_state, uint32_t* device_status) {
   return CTCPB_OK;
 }
 
-int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[5]) {
+int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[6]) {
   if (!ws_or_state || !counters) return CTCPB_ENULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return CTCPB_ECUDA;
   Header h;
   if (cudaMemcpy(&h, ws_or_state, sizeof(Header), cudaMemcpyDeviceToHost) != cudaSuccess) return CTCPB_ECUDA;
   for (int i = 0; i < 5; ++i) counters[i] = h.counters[i];
+  counters[5] = h.fused_launches;
   return CTCPB_OK;
 }
 

@@ -52,4 +52,19 @@ __device__ __forceinline__ void mbar_init_fence() {
 // its later bulk copies into it
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// release store / acquire load of a flag in global memory (device scope)
+__device__ __forceinline__ void st_release_u32(u32* p, u32 v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ u32 ld_acquire_u32(const u32* p) {
+  u32 v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// order generic-proxy accesses of global memory (made visible by an acquire)
+// before this thread's later bulk copies that read it
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+
 }  // namespace ctcpb

@@ -36,7 +36,8 @@ struct Header {
   u32 counters[5];  // decode steps, unproven first sets, exhaustive selections, full-frame scans,
                     // hash-proposed merges
   u64 phase_cycles[8];  // CTCPB_PHASE_PROF builds: clock64 cycles per step phase, summed over rows
-  u32 pad1[30];
+  u32 fused_launches;   // pre-pass + steps launches made as one cooperative kernel
+  u32 pad1[29];
 };
 static_assert(sizeof(Header) == 256, "header is 256 bytes");
 
@@ -58,7 +59,7 @@ struct Layout {
   size_t rec_bytes;
   size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp, o_msrc;
   size_t o_clist, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;
-  size_t o_recs, o_sel, o_nsel, total;
+  size_t o_recs, o_rflag, o_sel, o_nsel, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -109,6 +110,7 @@ inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_s
     o.o_pnext = take(4 * (size_t)B);
   }
   o.o_recs = take(o.rec_bytes * (size_t)B * tile);
+  o.o_rflag = take(4 * (size_t)B * tile);
   if (T_sel > 0) {
     o.o_sel = take(4 * (size_t)B * T_sel);
     o.o_nsel = take(4 * (size_t)B);
@@ -151,6 +153,9 @@ struct View {
   __host__ __device__ char* rec(int b, int s) const {
     return base + lay.o_recs + ((size_t)b * lay.tile + s) * lay.rec_bytes;
   }
+  // record ready flags [B][tile]: set by the pre-pass, cleared by the step
+  // kernel once it has copied the record (only when the two run concurrently)
+  __host__ __device__ u32* rflag() const { return (u32*)(base + lay.o_rflag); }
   __host__ __device__ int* sel() const { return (int*)(base + lay.o_sel); }
   __host__ __device__ int* nsel() const { return (int*)(base + lay.o_nsel); }
 };

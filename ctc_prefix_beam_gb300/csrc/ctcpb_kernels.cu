@@ -92,6 +92,7 @@ __global__ void k_init(View st) {
     h->status = 0u;
     for (int i = 0; i < 5; ++i) h->counters[i] = 0u;
     for (int i = 0; i < 8; ++i) h->phase_cycles[i] = 0ull;
+    h->fused_launches = 0u;
   }
   for (size_t b = tid; b < (size_t)L.B; b += nthr) {
     RowHdr r;
@@ -102,6 +103,11 @@ __global__ void k_init(View st) {
       st.ptop()[b] = 0;
       st.pnext()[b] = 0;
     }
+  }
+  {
+    const size_t nf = (size_t)L.B * L.tile;
+    u32* rf = st.rflag();
+    for (size_t i = tid; i < nf; i += nthr) rf[i] = 0u;
   }
   if (L.paged) {
     const size_t nt = 2 * (size_t)L.B * L.beam * L.max_lp;

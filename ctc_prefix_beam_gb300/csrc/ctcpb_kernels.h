@@ -14,6 +14,15 @@ cudaError_t launch_prepass_rows(const float* lp, long long stride_r, int R, int 
                                 float* lps, int* cnt, float* lpb, float* flp, int* fid, cudaStream_t s);
 cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                         int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+// Pre-pass and steps of one tile in a single cooperative launch (the pre-pass
+// publishes records that the step warps consume as they arrive).  Returns
+// cudaErrorNotSupported when the problem or the device does not allow it;
+// the caller then launches the two kernels one after the other.
+cudaError_t launch_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
+                         int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+bool rank_tma_ok(const float* lp, long long s1, long long s2, int V, int L);
+int rank_tma_warps(int V);
+
 // The warp-per-row step kernel takes flat storage, beam <= 32 and a ranked
 // record of at most 32 + 8*68 bytes (list length <= 66).
 bool step_warp_fits(const Layout& lay);

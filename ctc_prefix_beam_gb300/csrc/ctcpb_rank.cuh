@@ -1,0 +1,454 @@
+// Vocabulary pre-pass building blocks ("GPU CTC Prefix Beam Search Decoder",
+// section 3.4.7), shared by the stand-alone pre-pass kernels and the fused
+// pre-pass + step kernel: the plain per-warp ranking and the staged ranking
+// of one shared-memory row per warp.
+#pragma once
+
+#include "ctcpb_async.cuh"
+#include "ctcpb_internal.cuh"
+#include "ctcpb_sort.cuh"
+
+namespace ctcpb {
+namespace {
+
+#define FULL 0xffffffffu
+template <int NT>
+__device__ __forceinline__ void gsync() {
+  if (NT == 32)
+    __syncwarp();
+  else
+    __syncthreads();
+}
+template <int NT>
+__device__ void bitonic_desc(u64* a, int P, int tid) {
+  for (int k = 2; k <= P; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P; i += NT) {
+        int ixj = i ^ j;
+        if (ixj > i) {
+          u64 x = a[i], y = a[ixj];
+          bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            a[i] = y;
+            a[ixj] = x;
+          }
+        }
+      }
+      gsync<NT>();
+    }
+}
+__device__ __forceinline__ u64 warp_max_u64(u64 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    u64 w = __shfl_xor_sync(FULL, v, o);
+    v = w > v ? w : v;
+  }
+  return v;
+}
+__device__ __forceinline__ int pow2_at_least(int n, int lo) {
+  int p = lo;
+  while (p < n) p <<= 1;
+  return p;
+}
+// ---- plain per-warp ranking (any alignment, any list length)
+// Rank one frame row by one warp: the first L live non-blank labels by
+// (lp desc, id asc), the blank log-prob and the label after the list.
+//
+// Exact top-(L+1) selection:
+//   1. each lane keeps its top-2 label keys over labels lane, lane+32, ...;
+//   2. the (L+1)-th largest of these 64 keys is a lower bound tau of the
+//      (L+1)-th largest key of the row (they are distinct labels);
+//   3. every label with key >= tau is compacted into shared memory and the
+//      compacted set is sorted; it contains the top L+1 by construction;
+//   4. if the compacted set would overflow `lcap`, the warp falls back to
+//      L+1 rounds of "largest key below the previous one".
+constexpr int kRankCap = 512;  // shared keys per ranking warp
+
+__device__ __forceinline__ u64 label_key_at(const float* __restrict__ row, int c, int V, int blank) {
+  if (c >= V || c == blank) return 0ull;
+  float v = rdlp(row[c]);
+  return v > CTCPB_NEG ? lab_key(v, c) : 0ull;
+}
+
+__device__ void rank_row(const float* __restrict__ row, int V, int blank, int L, u64* buf, int lane,
+                         int* o_ids, float* o_lps, int* o_cnt, float* o_lpb, float* o_flp, int* o_fid) {
+  const int K = L + 1;
+  u64 tau = 0ull;
+  if (K <= 64) {
+    u64 k1 = 0ull, k2 = 0ull;
+    for (int c = lane; c < V; c += 32) {
+      u64 key = label_key_at(row, c, V, blank);
+      if (key > k2) {
+        if (key > k1) {
+          k2 = k1;
+          k1 = key;
+        } else {
+          k2 = key;
+        }
+      }
+    }
+    buf[lane] = k1;
+    buf[lane + 32] = k2;
+    __syncwarp();
+    bitonic_desc<32>(buf, 64, lane);
+    tau = buf[K - 1];
+    __syncwarp();
+  }
+  int n = 0;
+  bool ovf = false;
+  for (int c0 = 0; c0 < V; c0 += 32) {
+    const int c = c0 + lane;
+    u64 key = label_key_at(row, c, V, blank);
+    bool take = key != 0ull && key >= tau;
+    unsigned m = __ballot_sync(FULL, take);
+    int tot = __popc(m);
+    if (n + tot > kRankCap) {
+      ovf = true;
+      break;
+    }
+    if (take) buf[n + __popc(m & ((1u << lane) - 1u))] = key;
+    n += tot;
+  }
+  __syncwarp();
+  if (!ovf) {
+    const int P = pow2_at_least(n, 32);
+    for (int i = n + lane; i < P; i += 32) buf[i] = 0ull;
+    __syncwarp();
+    bitonic_desc<32>(buf, P, lane);
+  } else {
+    u64 prev = ~0ull;
+    n = 0;
+    for (int r = 0; r < K; ++r) {
+      u64 best = 0ull;
+      for (int c = lane; c < V; c += 32) {
+        u64 key = label_key_at(row, c, V, blank);
+        if (key < prev && key > best) best = key;
+      }
+      best = warp_max_u64(best);
+      if (best == 0ull) break;
+      if (lane == 0) buf[r] = best;
+      prev = best;
+      n = r + 1;
+    }
+    __syncwarp();
+  }
+  const int cnt = n < L ? n : L;
+  for (int i = lane; i < L; i += 32) {
+    if (i < cnt) {
+      u64 kk = buf[i];
+      o_ids[i] = (int)(~(u32)kk);
+      o_lps[i] = fkey_inv((u32)(kk >> 32));
+    } else {
+      o_ids[i] = -1;
+      o_lps[i] = CTCPB_NEG;
+    }
+  }
+  if (lane == 0) {
+    *o_cnt = cnt;
+    *o_lpb = rdlp(row[blank]);
+    if (n > L) {
+      *o_flp = fkey_inv((u32)(buf[L] >> 32));
+      *o_fid = (int)(~(u32)buf[L]);
+    } else {
+      *o_flp = CTCPB_NEG;
+      *o_fid = -1;
+    }
+  }
+  __syncwarp();
+}
+
+#define RFULL 0xffffffffu
+constexpr int kCandCap = 512;          // compacted labels per warp (= rank_row's buffer)
+// Where one ranked row goes.
+struct RankDst {
+  int* ids;
+  float* lps;
+  int* cnt;
+  float* lpb;
+  float* flp;
+  int* fid;
+  int* tout;
+  int t;
+  u32* flag;  // set (release) once the record is complete; null: none
+};
+
+// Items of the decode: (row b, step s), frame-major, records in the state.
+struct RecItems {
+  View st;
+  const float* lp;
+  long long sb, stt;
+  int mode;
+  const int* nframes;
+  int chunk_T, tile_start, tile_len;
+  u32* flags;  // per-record ready flags [B][tile] when a consumer runs concurrently, else null
+  __device__ long long count() const { return (long long)st.lay.B * tile_len; }
+  // is item `it` a decoded frame? then its row and frame index
+  __device__ bool probe(long long it, const float** row, int* t) const {
+    const int B = st.lay.B;
+    const int b = (int)(it % B), s = (int)(it / B);
+    if (mode == 0) {
+      if (s >= st.nsel()[b]) return false;
+      *t = st.sel()[(size_t)b * st.lay.T_sel + s];
+    } else {
+      int nf = nframes ? nframes[b] : chunk_T;
+      nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
+      if (tile_start + s >= nf) return false;
+      *t = tile_start + s;
+    }
+    *row = lp + (long long)b * sb + (long long)(*t) * stt;
+    return true;
+  }
+  __device__ RankDst dst(long long it, int t) const {
+    const int B = st.lay.B;
+    const int b = (int)(it % B), s = (int)(it / B);
+    char* r = st.rec(b, s);
+    RecHdr* h = (RecHdr*)r;
+    return RankDst{rec_ids(r),  rec_lps(r, st.lay.Lpad), &h->cnt, &h->lpb, &h->front_lp, &h->front_id, &h->t, t,
+                   flags ? flags + (size_t)b * st.lay.tile + s : nullptr};
+  }
+};
+
+// Independent rows (the ctcpb_topk_prepass entry point).
+struct RowItems {
+  const float* lp;
+  long long stride;
+  int R, L;
+  int *ids, *cnt, *fid;
+  float *lps, *lpb, *flp;
+  __device__ long long count() const { return R; }
+  __device__ bool probe(long long r, const float** row, int* t) const {
+    *row = lp + r * stride;
+    *t = 0;
+    return true;
+  }
+  __device__ RankDst dst(long long r, int t) const {
+    return RankDst{ids + r * L, lps + r * L, cnt + r, lpb + r, flp + r, fid + r, nullptr, t, nullptr};
+  }
+};
+
+// Passes 1-3 over one staged row (all lanes): compacts every label that can
+// be in the top L+1 into `cand`; returns their count, or -1 when they
+// overflow the buffer.  `row`: 16-byte aligned shared memory, V % 4 == 0, the
+// blank already replaced by -inf.
+__device__ int rank_gather(const float* __restrict__ row, int V, int L, u64* cand, int lane) {
+  const int K = L + 1;
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int V4 = V >> 2;
+  // 1. maxima of the x,y and z,w halves of this lane's labels (four chains)
+  float mx = -INFINITY, my = -INFINITY, mz = -INFINITY, mw = -INFINITY;
+#pragma unroll 4
+  for (int q = lane; q < V4; q += 32) {
+    const float4 x = r4[q];
+    mx = fmaxf(mx, x.x);
+    my = fmaxf(my, x.y);
+    mz = fmaxf(mz, x.z);
+    mw = fmaxf(mw, x.w);
+  }
+  const float hA = fmaxf(mx, my) + 0.0f, hB = fmaxf(mz, mw) + 0.0f;
+  // 2. tau: the K-th largest of these 64 values
+  u32 pool[2] = {hA > CTCPB_NEG ? fkey(hA) : 0u, hB > CTCPB_NEG ? fkey(hB) : 0u};
+  warp_sort_desc<2>(pool, lane);
+  const u32 kth = __shfl_sync(RFULL, K > 32 ? pool[1] : pool[0], (K - 1) & 31);
+  const float tauf = kth != 0u ? fkey_inv(kth) : -FLT_MAX;
+  // 3. every live label >= tau, four float4 per lane per round, compacted by
+  // an exclusive scan of the lanes' hit counts
+  int n = 0;
+  for (int q0 = 0; q0 < V4; q0 += 128) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int qq = q0 + 32 * u + lane;
+      x[u] = qq < V4 ? r4[qq] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+    u32 hit = 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      hit |= (u32)(x[u].x >= tauf && x[u].x > CTCPB_NEG) << (4 * u);
+      hit |= (u32)(x[u].y >= tauf && x[u].y > CTCPB_NEG) << (4 * u + 1);
+      hit |= (u32)(x[u].z >= tauf && x[u].z > CTCPB_NEG) << (4 * u + 2);
+      hit |= (u32)(x[u].w >= tauf && x[u].w > CTCPB_NEG) << (4 * u + 3);
+    }
+    if (!__any_sync(RFULL, hit != 0u)) continue;
+    const int cntl = __popc(hit);
+    int incl = cntl;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(RFULL, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(RFULL, incl, 31);
+    if (n + total > kCandCap) return -1;
+    int pos = n + incl - cntl;
+    if (hit != 0u) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int b = (q0 + 32 * u + lane) << 2;
+        if (hit & (1u << (4 * u))) cand[pos++] = lab_key(x[u].x + 0.0f, b);
+        if (hit & (2u << (4 * u))) cand[pos++] = lab_key(x[u].y + 0.0f, b + 1);
+        if (hit & (4u << (4 * u))) cand[pos++] = lab_key(x[u].z + 0.0f, b + 2);
+        if (hit & (8u << (4 * u))) cand[pos++] = lab_key(x[u].w + 0.0f, b + 3);
+      }
+    }
+    n += total;
+  }
+  __syncwarp();
+  return n;
+}
+
+// Write rank r's label (r < L: list, r == L: front).
+__device__ __forceinline__ void put_ranked(u64 key, int r, int L, const RankDst& d) {
+  if (key == 0ull) return;
+  if (r < L) {
+    d.ids[r] = (int)(~(u32)key);
+    d.lps[r] = fkey_inv((u32)(key >> 32));
+  } else if (r == L) {
+    *d.fid = (int)(~(u32)key);
+    *d.flp = fkey_inv((u32)(key >> 32));
+  }
+}
+
+// Pass 4 (all lanes): rank the n compacted labels and write the row's list.
+__device__ void rank_finish(const u64* cand, int n, int L, float lpb, int lane, const RankDst& d) {
+  const int cnt = n < L ? n : L;
+  if (n <= 64) {
+    u64 v[2] = {lane < n ? cand[lane] : 0ull, lane + 32 < n ? cand[lane + 32] : 0ull};
+    warp_sort_desc<2>(v, lane);
+    put_ranked(v[0], lane, L, d);
+    put_ranked(v[1], lane + 32, L, d);
+  } else if (n <= 128) {
+    u64 v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = lane + 32 * e < n ? cand[lane + 32 * e] : 0ull;
+    warp_sort_desc<4>(v, lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) put_ranked(v[e], lane + 32 * e, L, d);
+  } else {
+    for (int e = lane; e < n; e += 32) {
+      const u64 me = cand[e];
+      int rk = 0, rk2 = 0;
+      int j = 0;
+      for (; j + 1 < n; j += 2) {
+        rk += cand[j] > me;
+        rk2 += cand[j + 1] > me;
+      }
+      if (j < n) rk += cand[j] > me;
+      put_ranked(me, rk + rk2, L, d);
+    }
+  }
+  for (int i = cnt + lane; i < L; i += 32) {
+    d.ids[i] = -1;
+    d.lps[i] = CTCPB_NEG;
+  }
+  if (lane == 0) {
+    *d.cnt = cnt;
+    *d.lpb = lpb;
+    if (n <= L) {
+      *d.flp = CTCPB_NEG;
+      *d.fid = -1;
+    }
+    if (d.tout) *d.tout = d.t;
+  }
+  __syncwarp();
+}
+
+__host__ __device__ inline size_t rank_tma_per_warp(int V) {
+  return align_up((size_t)V * 4, 128) + (size_t)kCandCap * 8 + 16;
+}
+
+// The ranking of one block: warps 0..nwb-1 each own a row buffer in `smem`;
+// (vblock, nvblocks) is this block's place among the blocks that rank.  The
+// next row's bulk copy is issued as soon as the current row's passes have read
+// the buffer, so it overlaps pass 4.
+template <class Items>
+__device__ __forceinline__ void rank_tma_body(const Items& items, int V, int blank, int L, u32* status,
+                                              unsigned char* smem, int vblock, int nvblocks, int nwb) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (wid >= nwb) return;
+  const size_t per_warp = align_up((size_t)V * 4, 128) + (size_t)kCandCap * 8 + 16;
+  unsigned char* base = smem + per_warp * wid;
+  float* buf = reinterpret_cast<float*>(base);
+  u64* cand = reinterpret_cast<u64*>(base + align_up((size_t)V * 4, 128));
+  u64* bar = cand + kCandCap;
+  if (lane == 0) {
+    mbar_init(bar);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncwarp();
+  const unsigned bytes = (unsigned)V * 4u;
+  const long long total = items.count();
+  const long long stride = (long long)nvblocks * nwb;
+  unsigned phase = 0u;
+  // This warp's items are it0, it0 + stride, ...; lane j resolves the j-th of
+  // the next 32 in parallel, so finding the next row costs no dependent loads.
+  long long batch = (long long)vblock * nwb + wid;
+  long long my_it = 0;
+  const float* my_row = nullptr;
+  int my_t = 0;
+  unsigned vmask = 0u;
+  auto refill = [&]() {
+    while (vmask == 0u && batch < total) {
+      my_it = batch + (long long)lane * stride;
+      const bool ok = my_it < total && items.probe(my_it, &my_row, &my_t);
+      vmask = __ballot_sync(RFULL, ok);
+      batch += 32 * stride;
+    }
+  };
+  // next valid item (all lanes): returns false when the warp's items are done
+  auto advance = [&](long long* it, const float** row, int* t) -> bool {
+    refill();
+    if (vmask == 0u) return false;
+    const int j = __ffs(vmask) - 1;
+    vmask &= vmask - 1u;
+    *it = __shfl_sync(RFULL, my_it, j);
+    *row = reinterpret_cast<const float*>(__shfl_sync(RFULL, reinterpret_cast<unsigned long long>(my_row), j));
+    *t = __shfl_sync(RFULL, my_t, j);
+    return true;
+  };
+  long long it = 0;
+  const float* row = nullptr;
+  int t = 0;
+  bool have = advance(&it, &row, &t);
+  if (have && lane == 0) {
+    mbar_arrive_tx(bar, bytes);
+    bulk_g2s(buf, row, bytes, bar);
+  }
+  while (have) {
+    if (!mbar_wait(bar, phase)) {
+      if (lane == 0 && status) atomicOr(status, CTCPB_DEV_TIMEOUT);
+      mbar_wait(bar, phase);  // a last bounded chance for the copy in flight
+      return;
+    }
+    phase ^= 1u;
+    const RankDst dc = items.dst(it, t);
+    const float rawb = buf[blank];
+    const float lpb = rdlp(rawb);
+    __syncwarp();
+    if (lane == 0) buf[blank] = -INFINITY;  // the blank is not a label of the list
+    __syncwarp();
+    const int n = rank_gather(buf, V, L, cand, lane);
+    if (n < 0) {  // constant or near-constant row: plain ranking of the staged row
+      if (lane == 0) buf[blank] = rawb;
+      __syncwarp();
+      rank_row(buf, V, blank, L, cand, lane, dc.ids, dc.lps, dc.cnt, dc.lpb, dc.flp, dc.fid);
+      if (dc.tout && lane == 0) *dc.tout = dc.t;
+    }
+    __syncwarp();  // every lane is done reading the buffer
+    have = advance(&it, &row, &t);
+    if (have && lane == 0) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      mbar_arrive_tx(bar, bytes);
+      bulk_g2s(buf, row, bytes, bar);
+    }
+    if (n >= 0) rank_finish(cand, n, L, lpb, lane, dc);
+    if (dc.flag) {  // publish the record: every lane's stores, then the flag
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release_u32(dc.flag, 1u);
+    }
+    __syncwarp();
+  }
+}
+
+
+}  // namespace
+}  // namespace ctcpb

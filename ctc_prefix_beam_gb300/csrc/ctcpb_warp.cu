@@ -36,6 +36,7 @@
 #include "ctcpb_async.cuh"
 #include "ctcpb_internal.cuh"
 #include "ctcpb_kernels.h"
+#include "ctcpb_rank.cuh"
 #include "ctcpb_sort.cuh"
 
 namespace ctcpb {
@@ -563,21 +564,27 @@ __device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const fl
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// KB: beam bucket (8, 16 or 32), the bound of the per-hypothesis compares.
+constexpr long long kFlagSpins = 1ll << 20;  // bounded wait for published records (about 1 s)
+
+// The steps of rows row_block*kWPC + warp (warps 0..kWPC-1 of the block; the
+// block's other warps only help build the tables).  KB: beam bucket (8, 16 or
+// 32), the bound of the per-hypothesis compares.  flags: the records' ready
+// flags when the pre-pass runs concurrently (null: the records are complete).
 template <int KB>
-__global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float* __restrict__ lp, long long sb,
-                                                         long long stt, int mode, const int* __restrict__ nframes,
-                                                         int chunk_T, int tile_start, int tile_len) {
-  extern __shared__ __align__(16) unsigned char smem[];
+__device__ __forceinline__ void step_warp_body(const View& st, const float* __restrict__ lp, long long sb,
+                                               long long stt, int mode, const int* __restrict__ nframes,
+                                               int chunk_T, int tile_start, int tile_len, unsigned char* smem,
+                                               int row_block, u32* flags) {
   Tables& tb = *reinterpret_cast<Tables*>(smem);
-  WarpSmem& W = reinterpret_cast<WarpSmem*>(smem + align_up(sizeof(Tables), 16))[threadIdx.x >> 5];
+  const int wid = threadIdx.x >> 5;
+  WarpSmem& W = reinterpret_cast<WarpSmem*>(smem + align_up(sizeof(Tables), 16))[wid < kWPC ? wid : 0];
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) build_tables(tb, lane);
   __syncthreads();
 
   const Layout& Ly = st.lay;
-  const int b = blockIdx.x * kWPC + (threadIdx.x >> 5);
-  if (b >= Ly.B) return;
+  const int b = row_block * kWPC + wid;
+  if (wid >= kWPC || b >= Ly.B) return;
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V, Lpad = Ly.Lpad;
   const float NEG = CTCPB_NEG;
 
@@ -635,19 +642,47 @@ __global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float
   const unsigned rbytes = (unsigned)Ly.rec_bytes;
   auto rec_of = [&](int s) -> const char* { return W.rec[(s / kRecGrp) & 1] + (s % kRecGrp) * rbytes; };
   int g_issued = 0, g_waited = 0;
-  // lane 0: bulk copy of record group g (steps g*kRecGrp ...) into its half
-  auto fetch_group = [&](int g) {
-    const int s0 = g * kRecGrp;
-    if (s0 < nsteps) {
-      const unsigned nb = (unsigned)(nsteps - s0 < kRecGrp ? nsteps - s0 : kRecGrp) * rbytes;
-      mbar_arrive_tx(&W.rbar[g & 1], nb);
-      bulk_g2s(W.rec[g & 1], rec_g + (size_t)s0 * rbytes, nb, &W.rbar[g & 1]);
+  u32* const rflags = flags ? flags + (size_t)b * Ly.tile : nullptr;
+  int s_pub = rflags ? 0 : nsteps;  // records [0, s_pub) are known to be published
+  // all lanes: make sure records [s0, s_end) are published.  Lane j acquires
+  // the flag of record s_pub + j, so one pass covers up to 32 records; the
+  // barrier orders those acquires before lane 0's bulk copies.
+  auto await_records = [&](int s_end) -> bool {
+    for (long long spin = 0; s_pub < s_end; ++spin) {
+      if (spin >= kFlagSpins) return false;
+      const int r = s_pub + lane;
+      const bool set = r >= nsteps || ld_acquire_u32(rflags + r) != 0u;
+      const unsigned m = __ballot_sync(WFULL, set);
+      s_pub += (m == WFULL) ? 32 : __ffs(~m) - 1;
+      if (s_pub < s_end) __nanosleep(64);
     }
+    __syncwarp();
+    return true;
   };
-  // all lanes: wait for group g (the (g/2)-th use of its barrier)
+  // all lanes: bulk copy of record group g (steps g*kRecGrp ...) into its
+  // half, once its records are published; false if that wait ran out
+  auto issue_group = [&](int g) -> bool {
+    const int s0 = g * kRecGrp;
+    if (s0 >= nsteps) return true;
+    const int nr = nsteps - s0 < kRecGrp ? nsteps - s0 : kRecGrp;
+    const bool fresh = s_pub < s0 + nr;
+    if (fresh && !await_records(s0 + nr)) return false;
+    if (lane == 0) {
+      if (fresh) fence_proxy_async_global();
+      fence_proxy_async();  // this half's earlier reads come before the copy's writes
+      mbar_arrive_tx(&W.rbar[g & 1], (unsigned)nr * rbytes);
+      bulk_g2s(W.rec[g & 1], rec_g + (size_t)s0 * rbytes, (unsigned)nr * rbytes, &W.rbar[g & 1]);
+    }
+    g_issued = g + 1;
+    return true;
+  };
+  // all lanes: wait for group g (the (g/2)-th use of its barrier), then clear
+  // its records' flags for the next use of the slots
   auto wait_group = [&](int g) -> bool {
     const bool ok = mbar_wait(&W.rbar[g & 1], (unsigned)((g >> 1) & 1));
     g_waited = g + 1;
+    const int s0 = g * kRecGrp;
+    if (ok && rflags && lane < kRecGrp && s0 + lane < nsteps) rflags[s0 + lane] = 0u;
     return ok;
   };
   // a wait ran out: report it, give the copies in flight a last bounded wait
@@ -673,12 +708,9 @@ __global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float
     mbar_init(&W.rbar[0]);
     mbar_init(&W.rbar[1]);
     mbar_init_fence();
-    fetch_group(0);
-    fetch_group(1);
   }
-  g_issued = nsteps > kRecGrp ? 2 : 1;
   __syncwarp();
-  if (!wait_group(0)) {
+  if (!issue_group(0) || !issue_group(1) || !wait_group(0)) {
     bail();
     return;
   }
@@ -891,12 +923,10 @@ __global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float
     // ---- the group of step s is used up: refill its half two groups ahead
     if (s % kRecGrp == kRecGrp - 1) {
       __syncwarp();
-      const int g = s / kRecGrp + 2;
-      if (lane == 0 && g * kRecGrp < nsteps) {
-        fence_proxy_async();
-        fetch_group(g);
+      if (!issue_group(s / kRecGrp + 2)) {
+        bail();
+        return;
       }
-      if (g * kRecGrp < nsteps) g_issued = g + 1;
     }
     PHASE_MARK(6);
     if (s - win0 + 1 == kRing && s + 1 < nsteps) flush(s);
@@ -934,6 +964,34 @@ __global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float
   }
 }
 
+template <int KB>
+__global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float* __restrict__ lp, long long sb,
+                                                         long long stt, int mode, const int* __restrict__ nframes,
+                                                         int chunk_T, int tile_start, int tile_len) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  step_warp_body<KB>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x, nullptr);
+}
+
+// Pre-pass and steps in one cooperative launch: blocks [0, nsb) run the rows'
+// steps, the others rank frames (frame-major) and publish each record with a
+// release flag that the step warps acquire before copying it.  Every block is
+// resident at once (cooperative launch), so the waits always end; each one is
+// bounded all the same.
+template <int KB>
+__global__ void __launch_bounds__(256, 1) k_fused(View st, const float* __restrict__ lp, long long sb, long long stt,
+                                                  int mode, const int* __restrict__ nframes, int chunk_T,
+                                                  int tile_start, int tile_len, int nsb, int rank_warps) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&st.hdr()->fused_launches, 1u);
+  if ((int)blockIdx.x < nsb) {
+    step_warp_body<KB>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x, st.rflag());
+  } else {
+    RecItems items{st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, st.rflag()};
+    rank_tma_body(items, st.lay.V, st.lay.blank, st.lay.L, &st.hdr()->status, smem, (int)blockIdx.x - nsb,
+                  (int)gridDim.x - nsb, rank_warps);
+  }
+}
+
 bool step_warp_fits(const Layout& lay) {
   return lay.beam <= 32 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
 }
@@ -960,6 +1018,45 @@ cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long
   if (st.lay.beam <= 8) return launch_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   if (st.lay.beam <= 16) return launch_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   return launch_kb<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+}
+
+template <int KB>
+static cudaError_t launch_fused_kb(const View& st, const float* lp, long long sb, long long stt, int mode,
+                                  const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  const Layout& Ly = st.lay;
+  int dev = 0, coop = 0, sms = 0, maxsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  int rw = rank_tma_warps(Ly.V);
+  if (rw > 8) rw = 8;
+  const size_t rank_smem = rank_tma_per_warp(Ly.V) * (size_t)rw;
+  const size_t smem = rank_smem > step_warp_smem_bytes() ? rank_smem : step_warp_smem_bytes();
+  if (!coop || rw < 1 || smem > (size_t)maxsm) return cudaErrorNotSupported;
+  static size_t attr_smem = 0;
+  if (attr_smem != smem) {
+    cudaError_t e = cudaFuncSetAttribute(k_fused<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_smem = smem;
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<KB>, 256, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = per_sm * sms;
+  int nsb = (Ly.B + kWPC - 1) / kWPC;
+  if (per_sm < 1 || nsb + 8 > grid) return cudaErrorNotSupported;  // keep at least 8 ranking blocks
+  View stv = st;
+  void* args[] = {&stv, (void*)&lp, &sb, &stt, &mode, (void*)&nframes, &chunk_T, &tile_start, &tile_len, &nsb, &rw};
+  return cudaLaunchCooperativeKernel((const void*)k_fused<KB>, grid, 256, args, smem, s);
+}
+
+cudaError_t launch_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
+                         int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  if (!step_warp_fits(st.lay) || !rank_tma_ok(lp, sb, stt, st.lay.V, st.lay.L)) return cudaErrorNotSupported;
+  if (st.lay.beam <= 8) return launch_fused_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  if (st.lay.beam <= 16) return launch_fused_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return launch_fused_kb<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }
 
 }  // namespace ctcpb

@@ -237,9 +237,9 @@ def read_status(buf: torch.Tensor) -> int:
 
 
 def read_counters(buf: torch.Tensor) -> dict:
-    v = (ctypes.c_uint32 * 5)()
+    v = (ctypes.c_uint32 * 6)()
     _check(lib().ctcpb_read_counters(_ptr(buf), v), "read_counters")
-    return dict(steps=v[0], unproven=v[1], exhaustive=v[2], frame_scans=v[3], hash_merges=v[4])
+    return dict(steps=v[0], unproven=v[1], exhaustive=v[2], frame_scans=v[3], hash_merges=v[4], fused=v[5])
 
 
 def select_frames(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None):

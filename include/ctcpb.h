@@ -92,9 +92,11 @@ typedef struct ctcpb_config {
  * candidate set could not prove the selection, [2] of those, steps that fell
  * back to an exhaustive selection over the frame's list, [3] steps that also
  * scored every unlisted label of the frame, [4] merges proposed by prefix
- * hashes and checked on stored tokens.
+ * hashes and checked on stored tokens, [5] launches that ran the pre-pass and
+ * the steps of a tile as one cooperative kernel (CTCPB_NO_FUSE=1 in the
+ * environment makes every call use two kernels instead).
  */
-int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[5]);
+int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[6]);
 
 /* Human-readable text for a host status code. */
 const char* ctcpb_status_string(int status);
