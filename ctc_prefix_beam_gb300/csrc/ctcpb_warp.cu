@@ -30,9 +30,11 @@
 // other parity = its origin row's prefix + the labels it gained in the window.
 // lp[t][last] for step s+1 is gathered at the top of step s over every label
 // that can be "last" then (the current lasts and step s's list) into
-// shared memory by 4-byte asynchronous copies, so the loads overlap step s; ranked-frame
-// records arrive kRecGrp at a time by bulk copies into two alternating
-// shared-memory groups, one group ahead.
+// shared memory by 4-byte asynchronous copies, so the loads overlap step s.
+// Ranked-frame records are loaded from L2 into registers one step ahead
+// (header broadcast, list position = lane), their frame index two steps
+// ahead for the gather; every register copied at the end of a step was loaded
+// a whole step earlier.
 #include "ctcpb_async.cuh"
 #include "ctcpb_internal.cuh"
 #include "ctcpb_kernels.h"
@@ -59,7 +61,6 @@ namespace {
 #endif
 
 constexpr int kRing = 128;            // steps of history between materialisations
-constexpr int kRecGrp = 4;            // ranked-frame records per bulk copy (two groups in flight)
 constexpr int kWPC = 4;               // rows (warps) per block
 constexpr int kGenCap = 512;          // keys of the exhaustive selection
 constexpr int kGath = 128;            // gathered log-probs per frame (beam + L <= 98)
@@ -70,7 +71,7 @@ constexpr u32 kGold = 0x9e3779b9u;
 struct __align__(16) WarpSmem {
   u64 keys[kGenCap];
   u32 hist[kRing][32];
-  char rec[2][kRecGrp * kMaxRec];  // two groups of records, rec_bytes apart
+  char rec1[kMaxRec];  // the current record, copied for the slow selection
   float A[32], bpb[32], bpnb[32], scb[32], rep[32];
   int last[32], len[32];
   int bw[32];
@@ -80,14 +81,14 @@ struct __align__(16) WarpSmem {
   int4 nst[32][4];  // the new hypothesis of slot r, written by the candidate ranked r
   u32 fk[32];       // fold key of slot j: (i << 20 | last_j) when l_j = l_i + last_j
   u32 hk[32];       // prefix hash keys of the extension winners
-  u64 rbar[2];      // completion of the record groups
   float gath[2][kGath];  // lp[t][slot] of the next step, slot = hypothesis or beam + list position
 };
 
-struct Tables {
+struct __align__(16) Tables {
   unsigned short qmap[33][32];  // nlive -> lane -> (hyp << 8 | list position), 0xffff: none
   unsigned char qcnt[33][32];  // nlive -> hyp -> listed labels of that hyp in the round-1 set
 };
+static_assert(sizeof(Tables) % 16 == 0, "tables copy as 16-byte words");
 
 // 4-byte asynchronous copy global -> shared (completes at cp_wait_all)
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -149,17 +150,16 @@ __device__ __noinline__ void sort_keys(WarpSmem& W, int m, int lane) {
   __syncwarp();
 }
 
-// Staircase tables, one lane per nlive value (lane 0 also does nlive = 32).
-__device__ void build_tables(Tables& tb, int lane) {
-  for (int n = lane; n <= 32; n += 32) {
-    unsigned char q[32];
-    for (int k = 0; k < 32; ++k) {
-      q[k] = 0;
-      tb.qmap[n][k] = 0xffff;
-    }
+// Staircase tables for every nlive (compile-time constant): hypothesis k of n
+// live ones gets q_k list positions, one per hypothesis first (a frame whose
+// best label extends every hypothesis needs each of them in the set), then
+// greedily by the smallest (k+1)(q_k+1).
+constexpr Tables make_tables() {
+  Tables tb{};
+  for (int n = 0; n <= 32; ++n) {
+    unsigned char q[32] = {};
+    for (int k = 0; k < 32; ++k) tb.qmap[n][k] = 0xffff;
     int l = n;
-    // one listed label per hypothesis first: a frame whose best label extends
-    // every hypothesis (a label frame) needs each of them in the set
     for (int k = 0; k < n && l < 32; ++k, ++l) {
       tb.qmap[n][l] = (unsigned short)(k << 8);
       q[k] = 1;
@@ -178,7 +178,9 @@ __device__ void build_tables(Tables& tb, int lane) {
     }
     for (int k = 0; k < 32; ++k) tb.qcnt[n][k] = q[k];
   }
+  return tb;
 }
+__device__ const Tables g_tables = make_tables();
 
 // Append `key` (if nonzero and >= thr) to the candidate buffer W.keys[32 ..];
 // the first 32 entries hold the running best after each compaction.
@@ -579,7 +581,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   const int wid = threadIdx.x >> 5;
   WarpSmem& W = reinterpret_cast<WarpSmem*>(smem + align_up(sizeof(Tables), 16))[wid < kWPC ? wid : 0];
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 32) build_tables(tb, lane);
+  for (int i = threadIdx.x; i < (int)(sizeof(Tables) / 16); i += blockDim.x)
+    reinterpret_cast<int4*>(&tb)[i] = reinterpret_cast<const int4*>(&g_tables)[i];
   __syncthreads();
 
   const Layout& Ly = st.lay;
@@ -635,18 +638,12 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   long long prof_t0 = clock64();
 #endif
   const float* lpb_row = lp + (long long)b * sb;
-  auto row_of = [&](int s, const RecHdr* hd) -> const float* {
-    return lpb_row + (long long)(mode == 0 ? hd->t : tile_start + s) * stt;
-  };
   char* const rec_g = st.rec(b, 0);  // this row's records, rec_bytes apart
   const unsigned rbytes = (unsigned)Ly.rec_bytes;
-  auto rec_of = [&](int s) -> const char* { return W.rec[(s / kRecGrp) & 1] + (s % kRecGrp) * rbytes; };
-  int g_issued = 0, g_waited = 0;
   u32* const rflags = flags ? flags + (size_t)b * Ly.tile : nullptr;
   int s_pub = rflags ? 0 : nsteps;  // records [0, s_pub) are known to be published
-  // all lanes: make sure records [s0, s_end) are published.  Lane j acquires
-  // the flag of record s_pub + j, so one pass covers up to 32 records; the
-  // barrier orders those acquires before lane 0's bulk copies.
+  // all lanes: make sure records [0, s_end) are published.  Lane j acquires
+  // the flag of record s_pub + j, so one pass covers up to 32 records.
   auto await_records = [&](int s_end) -> bool {
     for (long long spin = 0; s_pub < s_end; ++spin) {
       if (spin >= kFlagSpins) return false;
@@ -659,36 +656,30 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     __syncwarp();
     return true;
   };
-  // all lanes: bulk copy of record group g (steps g*kRecGrp ...) into its
-  // half, once its records are published; false if that wait ran out
-  auto issue_group = [&](int g) -> bool {
-    const int s0 = g * kRecGrp;
-    if (s0 >= nsteps) return true;
-    const int nr = nsteps - s0 < kRecGrp ? nsteps - s0 : kRecGrp;
-    const bool fresh = s_pub < s0 + nr;
-    if (fresh && !await_records(s0 + nr)) return false;
-    if (lane == 0) {
-      if (fresh) fence_proxy_async_global();
-      fence_proxy_async();  // this half's earlier reads come before the copy's writes
-      mbar_arrive_tx(&W.rbar[g & 1], (unsigned)nr * rbytes);
-      bulk_g2s(W.rec[g & 1], rec_g + (size_t)s0 * rbytes, (unsigned)nr * rbytes, &W.rbar[g & 1]);
-    }
-    g_issued = g + 1;
-    return true;
+  // record of step s in registers (L2 loads: records may be written by other
+  // SMs during this launch)
+  struct RecR {
+    int cnt, t, id;
+    float lpb, flp, lp;
   };
-  // all lanes: wait for group g (the (g/2)-th use of its barrier), then clear
-  // its records' flags for the next use of the slots
-  auto wait_group = [&](int g) -> bool {
-    const bool ok = mbar_wait(&W.rbar[g & 1], (unsigned)((g >> 1) & 1));
-    g_waited = g + 1;
-    const int s0 = g * kRecGrp;
-    if (ok && rflags && lane < kRecGrp && s0 + lane < nsteps) rflags[s0 + lane] = 0u;
-    return ok;
+  auto rec_t = [&](int s) -> int { return __ldcg(reinterpret_cast<const int*>(rec_g + (size_t)s * rbytes + 16)); };
+  auto load_rec = [&](int s) -> RecR {
+    const char* g = rec_g + (size_t)s * rbytes;
+    const int4 h0 = __ldcg(reinterpret_cast<const int4*>(g));  // cnt, front id, lp[blank], front lp
+    RecR r;
+    r.cnt = h0.x;
+    r.lpb = __int_as_float(h0.z);
+    r.flp = __int_as_float(h0.w);
+    r.t = __ldcg(reinterpret_cast<const int*>(g + 16));
+    // list position `lane` (lanes past the list read position 0; see my_id)
+    const int p = lane < Ly.L ? lane : 0;
+    r.id = __ldcg(reinterpret_cast<const int*>(g + 32) + p);
+    r.lp = __ldcg(reinterpret_cast<const float*>(g + 32 + 4 * Lpad) + p);
+    return r;
   };
-  // a wait ran out: report it, give the copies in flight a last bounded wait
+  // a wait ran out: report it, let this warp's copies in flight land
   auto bail = [&]() {
     if (lane == 0) atomicOr(&st.hdr()->status, CTCPB_DEV_TIMEOUT);
-    for (int g = g_waited; g < g_issued; ++g) mbar_wait(&W.rbar[g & 1], (unsigned)((g >> 1) & 1));
     cp_wait_all();
   };
 
@@ -704,33 +695,32 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     win0 = s_last + 1;
   };
 
-  if (lane == 0) {
-    mbar_init(&W.rbar[0]);
-    mbar_init(&W.rbar[1]);
-    mbar_init_fence();
-  }
-  __syncwarp();
-  if (!issue_group(0) || !issue_group(1) || !wait_group(0)) {
+  if (!await_records(nsteps < 2 ? nsteps : 2)) {
     bail();
     return;
   }
+  RecR cur = load_rec(0);                   // the record of step s
+  int t1 = nsteps > 1 ? rec_t(1) : 0;      // frame index of step s+1
 
   for (int s = 0; s < nsteps; ++s) {
     PHASE_MARK(7);
-    // step s+1 opens the next group: its record is read by this step's gather
-    if ((s + 1) % kRecGrp == 0 && s + 1 < nsteps && !wait_group((s + 1) / kRecGrp)) {
+    // the record of step s+1 and the frame index of step s+2
+    if (s + 2 < nsteps && !await_records(s + 3)) {
       bail();
       return;
     }
+    // unconditional loads (clamped to a published record): a select on the
+    // loaded values would wait for them here
+    const RecR nx = load_rec(s + 1 < nsteps ? s + 1 : s);
+    const int t2 = rec_t(s + 2 < nsteps ? s + 2 : s);
+    if (rflags && lane == 0) rflags[s] = 0u;  // consumed: the slot is free for the next tile
     PHASE_MARK(0);
-    const char* Rc = rec_of(s);
-    const RecHdr* hd = (const RecHdr*)Rc;
-    const int cnt = hd->cnt;
-    const float lpb = hd->lpb;
-    const int my_id = lane < cnt ? ((const int*)(Rc + 32))[lane] : -1;
-    const float my_lp = lane < cnt ? ((const float*)(Rc + 32 + 4 * Lpad))[lane] : NEG;
-    const int t = mode == 0 ? hd->t : tcount + s;
-    const float* row = row_of(s, hd);
+    const int cnt = cur.cnt;
+    const float lpb = cur.lpb;
+    const int my_id = lane < Ly.L ? cur.id : -1;
+    const float my_lp = lane < Ly.L ? cur.lp : NEG;
+    const int t = mode == 0 ? cur.t : tcount + s;
+    const float* row = lpb_row + (long long)(mode == 0 ? cur.t : tile_start + s) * stt;
     const bool gap = t > t_prev + 1;
     const bool live = lane < nlive;
     // lp[t][last] of this lane's hypothesis, gathered by the previous step
@@ -738,16 +728,12 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     __syncwarp();
     const float gcur = gl >= 0 ? W.gath[s & 1][gl] : 0.0f;
     // lp[t_{s+1}][x] for every label x that can be "last" at step s+1: the
-    // current lasts (slots 0..beam-1) and this step's list (beam + position)
+    // current lasts (slot k) and this step's list (slot beam + position)
     if (s + 1 < nsteps) {
-      const float* row1 = row_of(s + 1, (const RecHdr*)rec_of(s + 1));
-      const int* ids = (const int*)(Rc + 32);
+      const float* row1 = lpb_row + (long long)(mode == 0 ? t1 : tile_start + s + 1) * stt;
       float* gdst = W.gath[(s + 1) & 1];
-      for (int x = lane; x < beam + cnt && x < kGath; x += 32) {
-        // x < beam <= 32 means x == lane: this lane's own hypothesis
-        const int lab = x < beam ? ((live && len > 0) ? last : -1) : ids[x - beam];
-        if (lab >= 0) cp_async4(gdst + x, row1 + lab);
-      }
+      if (live && len > 0) cp_async4(gdst + lane, row1 + last);
+      if (lane < cnt && beam + lane < kGath) cp_async4(gdst + beam + lane, row1 + my_id);
       cp_commit();
     }
 
@@ -828,8 +814,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         if (live && len < cap) {
           if (q < cnt)
             bnd = dadd(nxt, A);
-          else if (hd->front_lp > NEG)
-            bnd = dadd(hd->front_lp, A);
+          else if (cur.flp > NEG)
+            bnd = dadd(cur.flp, A);
         }
       }
 
@@ -855,9 +841,12 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
       const bool proven = !__any_sync(WFULL, bnd > NEG && (nw < beam || fkey(bnd) >= sstar));
       PHASE_MARK(3);
       if (!proven) {
-        __syncwarp();  // the optimistic slots are written before they are rewritten
+        // the record, for the slow selection, into shared memory
+        const int4* rg = reinterpret_cast<const int4*>(rec_g + (size_t)s * rbytes);
+        for (int i = lane; i < (int)(rbytes / 16); i += 32) reinterpret_cast<int4*>(W.rec1)[i] = __ldcg(rg + i);
+        __syncwarp();  // (also: the optimistic slots are written before they are rewritten)
         ++c_fb;
-        const int res = slow_select<KB>(W, Rc, row, sstar, nw, A, last, len, live, Rrep, my_id, my_lp, scB, bpb, bpnb,
+        const int res = slow_select<KB>(W, W.rec1, row, sstar, nw, A, last, len, live, Rrep, my_id, my_lp, scB, bpb, bpnb,
                                         mi, anyfold, n, cnt, cap, beam, blank, V, Lpad, gap, s - win0, lane);
         nw = res & 0xff;
         c_gen += (u32)((res >> 8) & 1);
@@ -920,14 +909,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     t_prev = t;
     ++step;
     ++c_steps;
-    // ---- the group of step s is used up: refill its half two groups ahead
-    if (s % kRecGrp == kRecGrp - 1) {
-      __syncwarp();
-      if (!issue_group(s / kRecGrp + 2)) {
-        bail();
-        return;
-      }
-    }
+    cur = nx;
+    t1 = t2;
     PHASE_MARK(6);
     if (s - win0 + 1 == kRing && s + 1 < nsteps) flush(s);
   }
