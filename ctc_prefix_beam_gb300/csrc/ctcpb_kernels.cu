@@ -186,7 +186,9 @@ struct StepSmem {
   int xu_k[NT], xu_c[NT];
   int pi[2 * NT], pj[2 * NT];
   int dfree[NT];
+  u64 top2[2 * NT];  // each hypothesis' best two candidate keys
   int cnt, front_id, nw, npairs, nxu, nkeys, ndfree;
+  int ptop, pnext;  // the row's page pool: LIFO top and bump pointer (paged)
   float lpb, front_lp;
 };
 
@@ -206,20 +208,20 @@ struct TokenStore {
   }
 };
 
-// allocate one page of row b: LIFO pool first, then the bump pointer
-__device__ int page_alloc(const View& st, int b) {
-  int* top = st.ptop() + b;
-  int cur = *((volatile int*)top);
-  if (cur > st.lay.ppr) {
-    set_status(st, CTCPB_DEV_OVERFLOW);
-    return -1;
+// The row's page pool (only the row's block touches it): the LIFO top and the
+// bump pointer live in shared memory during a call, the stack in the state.
+// Allocate one page: LIFO pool first, then the bump pointer.  Allocations and
+// releases never run in the same phase of a step.
+__device__ int page_alloc(const View& st, int b, int* ptop, int* pnext) {
+  const int pos = atomicSub(ptop, 1) - 1;  // may go below zero; the phase end clamps it
+  if (pos >= 0) {
+    if (pos >= st.lay.ppr) {
+      set_status(st, CTCPB_DEV_OVERFLOW);
+      return -1;
+    }
+    return st.pool(b)[pos];
   }
-  while (cur > 0) {
-    int prev = atomicCAS(top, cur, cur - 1);
-    if (prev == cur) return st.pool(b)[cur - 1];
-    cur = prev;
-  }
-  int phys = atomicAdd(st.pnext() + b, 1);
+  const int phys = atomicAdd(pnext, 1);
   if (phys >= st.lay.ppr) {
     set_status(st, CTCPB_DEV_PAGES);
     return -1;
@@ -227,8 +229,8 @@ __device__ int page_alloc(const View& st, int b) {
   return phys;
 }
 
-__device__ __forceinline__ void page_push(const View& st, int b, int phys) {
-  int pos = atomicAdd(st.ptop() + b, 1);
+__device__ __forceinline__ void page_push(const View& st, int b, int phys, int* ptop) {
+  const int pos = atomicAdd(ptop, 1);
   if (pos < st.lay.ppr)
     st.pool(b)[pos] = phys;
   else
@@ -284,6 +286,11 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
   }
   TokenStore tok{st, b};
   const int M = sortcap - NT;  // candidates per selection chunk
+  if (Ly.paged && tid == 0) {
+    S.ptop = st.ptop()[b];
+    S.pnext = st.pnext()[b];
+  }
+  gsync<NT>();
 
   for (int s = 0; s < nsteps; ++s) {
     const int t = mode == 0 ? st.sel()[(size_t)b * Ly.T_sel + s] : tcount + s;
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         for (int k = tid; k < nw; k += NT) {
           int* bt = st.btab(np, b, k);
           if (k < ntok) {
-            int phys = page_alloc(st, b);
+            int phys = page_alloc(st, b, &S.ptop, &S.pnext);
             if (phys >= 0) {
               st.refc(b)[phys] = 1;
               st.page(b, phys)[0] = S.ids[k];
@@ -358,6 +365,8 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
           }
         }
       }
+      gsync<NT>();
+      if (Ly.paged && tid == 0 && S.ptop < 0) S.ptop = 0;
       gsync<NT>();
     } else {
       // ---- section 3.4: collapsed-blank correction, extension and blank slots
@@ -447,10 +456,86 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       gsync<NT>();
 
       // ---- sections 3.4.4-3.4.6: best `beam` candidates over
-      // {blank slot, repeat slot, listed labels} of every live hypothesis
+      // {blank slot, repeat slot, listed labels} of every live hypothesis.
+      // Thread k = hypothesis k (nlive <= beam <= NT).  Its listed candidates
+      // score in list order, so its keys are (blank, repeat, listed ones in
+      // order).  tau = the beam-th largest of every hypothesis' best two keys
+      // is at most the beam-th largest key of the step (those are distinct
+      // candidates), so the winners are among the candidates >= tau.
+      auto blank_key = [&](int k) -> u64 {
+        const float sc = dlse(S.bpb[k], S.bpnb[k]);
+        return sc > NEG ? cand_key(sc, k, blank) : 0ull;
+      };
+      auto rep_key = [&](int k) -> u64 {
+        const int L = S.len[k];
+        return (L > 0 && L < cap && !S.repdead[k] && S.rep[k] > NEG) ? cand_key(S.rep[k], k, S.last[k]) : 0ull;
+      };
+      auto list_key = [&](int k, int p) -> u64 {  // 0: not a candidate
+        const int L = S.len[k];
+        const int c = S.ids[p];
+        if (L < cap && !(L > 0 && c == S.last[k]) && !((S.excl[k][p >> 5] >> (p & 31)) & 1u)) {
+          const float sc = dadd(S.lps[p], S.A[k]);
+          if (sc > NEG) return cand_key(sc, k, c);
+        }
+        return 0ull;
+      };
+      bool selected = false;
+      {
+        u64 kb = 0ull, kr = 0ull, ka = 0ull, kc = 0ull;
+        if (tid < nlive) {
+          kb = blank_key(tid);
+          kr = rep_key(tid);
+          for (int p = 0, got = 0; p < cnt && got < 2; ++p) {
+            const u64 key = list_key(tid, p);
+            if (key) {
+              if (got == 0) ka = key; else kc = key;
+              ++got;
+            }
+          }
+        }
+        // best two of {kb, kr, ka, kc}
+        u64 m1 = kb > kr ? kb : kr, m2 = kb > kr ? kr : kb;
+        if (ka > m1) { m2 = m1; m1 = ka; } else if (ka > m2) { m2 = ka; }
+        if (kc > m1) { m2 = m1; m1 = kc; } else if (kc > m2) { m2 = kc; }
+        S.top2[tid] = m1;
+        S.top2[NT + tid] = m2;
+        if (tid == 0) S.nkeys = 0;
+        gsync<NT>();
+        bitonic_desc<NT>(S.top2, 2 * NT, tid);
+        const u64 tau = S.top2[beam - 1];  // 0 (every live key) when fewer than beam are live
+        // every candidate >= tau (the listed ones stop at the first below tau)
+        const int cap_keys = sortcap;
+        if (tid < nlive) {
+          const u64 c0 = blank_key(tid), c1 = rep_key(tid);
+          if (c0 && c0 >= tau) { const int q = atomicAdd(&S.nkeys, 1); if (q < cap_keys) keys[q] = c0; }
+          if (c1 && c1 >= tau) { const int q = atomicAdd(&S.nkeys, 1); if (q < cap_keys) keys[q] = c1; }
+          for (int p = 0; p < cnt; ++p) {
+            const u64 key = list_key(tid, p);
+            if (!key) continue;
+            // scores fall along the list; equal scores may come in any token order
+            if ((key >> 32) < (tau >> 32)) break;
+            if (key < tau) continue;
+            const int q = atomicAdd(&S.nkeys, 1);
+            if (q < cap_keys) keys[q] = key;
+          }
+        }
+        gsync<NT>();
+        const int nk = S.nkeys;
+        if (nk <= cap_keys) {
+          const int P = pow2_at_least(nk > beam ? nk : beam, 2 * NT);
+          for (int i = nk + tid; i < P; i += NT) keys[i] = 0ull;
+          gsync<NT>();
+          bitonic_desc<NT>(keys, P, tid);
+          selected = true;
+        }
+        gsync<NT>();
+        if (tid == 0) S.nkeys = 0;
+        gsync<NT>();
+      }
       const int stride = cnt + 2;
-      const int NC = nlive * stride;
-      for (int i = tid; i < NT; i += NT) keys[i] = 0ull;
+      const int NC = selected ? 0 : nlive * stride;  // the chunked sort of every candidate (overflow only)
+      if (!selected)
+        for (int i = tid; i < NT; i += NT) keys[i] = 0ull;
       for (int base = 0; base < NC; base += M) {
         const int m = (NC - base) < M ? (NC - base) : M;
         for (int x = tid; x < m; x += NT) {
@@ -584,13 +669,16 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       } else {
         const int ps = Ly.page_size, mlp = Ly.max_lp;
         int* refc = st.refc(b);
-        // fork, pass A: acquire the source pages of every winner
-        for (int w = 0; w < nw; ++w) {
+        // fork, pass A: acquire the source pages of every winner (a thread per winner)
+        for (int w = tid; w < nw; w += NT) {
           const int src = S.nsrc[w];
           const int npg = (S.len[src] + ps - 1) / ps;
           const int* bs = st.btab(par, b, src);
-          for (int x = tid; x < npg; x += NT)
-            if (bs[x] >= 0) atomicAdd(&refc[bs[x]], 1);
+#pragma unroll 4
+          for (int x = 0; x < npg; ++x) {
+            const int phys = bs[x];
+            if (phys >= 0) atomicAdd(&refc[phys], 1);
+          }
         }
         gsync<NT>();
         // fork, pass B: release what each destination slot held, install the
@@ -600,7 +688,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
           for (int x = 0; x < mlp; ++x) {
             const int phys = bd[x];
             if (phys < 0) break;
-            if (atomicSub(&refc[phys], 1) == 1) page_push(st, b, phys);
+            if (atomicSub(&refc[phys], 1) == 1) page_push(st, b, phys, &S.ptop);
             bd[x] = -1;
           }
           if (w < nw) {
@@ -620,7 +708,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
           const int lpi = pos / ps, off = pos - lpi * ps;
           int* bd = st.btab(np, b, w);
           if (off == 0) {
-            const int phys = page_alloc(st, b);
+            const int phys = page_alloc(st, b, &S.ptop, &S.pnext);
             if (phys >= 0) {
               refc[phys] = 1;
               st.page(b, phys)[0] = tk;
@@ -630,7 +718,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
             const int phys = bd[lpi];
             if (phys < 0) continue;
             if (atomicAdd(&refc[phys], 0) > 1) {
-              const int nph = page_alloc(st, b);
+              const int nph = page_alloc(st, b, &S.ptop, &S.pnext);
               if (nph >= 0) {
                 const int* from = st.page(b, phys);
                 int* to = st.page(b, nph);
@@ -649,7 +737,9 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
           }
         }
         gsync<NT>();
-        for (int q = tid; q < S.ndfree; q += NT) page_push(st, b, S.dfree[q]);
+        if (tid == 0 && S.ptop < 0) S.ptop = 0;  // allocations past an empty pool
+        gsync<NT>();
+        for (int q = tid; q < S.ndfree; q += NT) page_push(st, b, S.dfree[q], &S.ptop);
         gsync<NT>();
       }
     }
@@ -682,6 +772,10 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
     st.hp()[rb + k] = S.hp[k];
   }
   if (tid == 0) {
+    if (Ly.paged) {
+      st.ptop()[b] = S.ptop;
+      st.pnext()[b] = S.pnext;
+    }
     rh->step = step;
     rh->tcount = mode == 1 ? tcount + nsteps : rh->tcount;
     rh->t_prev = t_prev;
