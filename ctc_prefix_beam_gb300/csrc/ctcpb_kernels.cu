@@ -187,6 +187,11 @@ struct StepSmem {
   int pi[2 * NT], pj[2 * NT];
   int dfree[NT];
   u64 top2[2 * NT];  // each hypothesis' best two candidate keys
+  // merge sources: slot i with l_k = l_i + last_k (or -1), tracked through the winners' sources
+  int msrc[NT], nmsrc[NT], bw[NT];
+  u64 hkey[2 * NT];   // the extension winners' prefix hashes (open addressing) ...
+  int hval[2 * NT];   // ... and their slots (-1: empty)
+  int npg[2][NT];     // paged: pages held by slot w of each parity's block table
   int cnt, front_id, nw, npairs, nxu, nkeys, ndfree;
   int ptop, pnext;  // the row's page pool: LIFO top and bump pointer (paged)
   float lpb, front_lp;
@@ -283,6 +288,16 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
     S.len[k] = st.len()[rb + k];
     S.h[k] = st.h()[rb + k];
     S.hp[k] = st.hp()[rb + k];
+    S.msrc[k] = st.msrc()[rb + k];
+  }
+  if (Ly.paged) {
+    for (int k = tid; k < 2 * beam; k += NT) {
+      const int pp = k / beam, w = k - pp * beam;
+      const int* bt = st.btab(pp, b, w);
+      int n = 0;
+      while (n < Ly.max_lp && bt[n] >= 0) ++n;
+      S.npg[pp][w] = n;
+    }
   }
   TokenStore tok{st, b};
   const int M = sortcap - NT;  // candidates per selection chunk
@@ -335,6 +350,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
           S.nhp[k] = kH0;
           S.ntok[k] = c;
           S.nsrc[k] = -1;
+          S.nmsrc[k] = empty_live ? ntok : -1;  // l_k = empty prefix + c
         } else if (k == ntok && empty_live) {
           S.npb[k] = S.lpb;
           S.npnb[k] = NEG;
@@ -345,6 +361,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
           S.nhp[k] = 0ull;
           S.ntok[k] = blank;
           S.nsrc[k] = -1;
+          S.nmsrc[k] = -1;
         }
       }
       if (tid == 0) S.nw = ntok + (empty_live ? 1 : 0);
@@ -363,6 +380,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
             }
             bt[0] = phys;
           }
+          S.npg[np][k] = k < ntok ? 1 : 0;
         }
       }
       gsync<NT>();
@@ -395,37 +413,10 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         S.nkeys = 0;
       }
       gsync<NT>();
-      // ---- section 3.4.3: pairs (i shorter, j longer) with l_j = l_i + last_j;
-      // the prefix hash proposes pairs, token comparison decides.
-      for (int j = tid; j < nlive; j += NT) {
-        for (int i = 0; i < nlive; ++i) {
-          if (S.len[j] == S.len[i] + 1 && S.hp[j] == S.h[i]) {
-            if (S.len[i] == 0) {
-              S.into[j] = i;
-            } else {
-              int p = atomicAdd(&S.npairs, 1);
-              if (p < 2 * NT) {
-                S.pi[p] = i;
-                S.pj[p] = j;
-              } else {
-                set_status(st, CTCPB_DEV_OVERFLOW);
-              }
-            }
-          }
-        }
-      }
-      gsync<NT>();
-      {
-        const int npairs = S.npairs < 2 * NT ? S.npairs : 2 * NT;
-        for (int p = 0; p < npairs; ++p) {
-          const int i = S.pi[p], j = S.pj[p];
-          const int Li = S.len[i];
-          bool mism = false;
-          for (int x = tid; x < Li; x += NT) mism |= tok.get(par, i, x) != tok.get(par, j, x);
-          const bool any = g_any<NT>(mism);
-          if (!any && tid == 0) S.into[j] = i;
-        }
-      }
+      // ---- section 3.4.3: pairs (i shorter, j longer) with l_j = l_i + last_j,
+      // known from the merge sources tracked through the previous steps
+      for (int j = tid; j < nlive; j += NT) S.into[j] = S.msrc[j];
+      for (int k = tid; k < NT; k += NT) S.bw[k] = -1;
       gsync<NT>();
       // fold (i, last_j) into j's blank slot; drop the folded candidate
       for (int j = tid; j < nlive; j += NT) {
@@ -653,6 +644,32 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         S.ndfree = 0;
       }
       gsync<NT>();
+      // the new slot of each source's blank winner; then every winner's merge
+      // source: a blank winner keeps its source's relation, an extension of
+      // source s relates to s's blank winner
+      for (int w = tid; w < nw; w += NT)
+        if (S.ntok[w] == blank) S.bw[S.nsrc[w]] = w;
+      for (int i = tid; i < 2 * NT; i += NT) {
+        S.hval[i] = -1;
+        S.hkey[i] = 0ull;
+      }
+      gsync<NT>();
+      for (int w = tid; w < nw; w += NT) {
+        const int src = S.nsrc[w];
+        S.nmsrc[w] = S.ntok[w] == blank ? (S.msrc[src] >= 0 ? S.bw[S.msrc[src]] : -1) : S.bw[src];
+        if (S.ntok[w] != blank) {  // the extension winners by prefix hash, for the check below
+          const u64 key = S.nh[w];
+          for (int q = 0; q < 2 * NT; ++q) {
+            const int slot = (int)((key + (u64)q) & (u64)(2 * NT - 1));
+            if (atomicCAS(&S.hval[slot], -1, w) == -1) {
+              S.hkey[slot] = key;
+              break;
+            }
+          }
+        }
+      }
+      if (tid == 0) S.npairs = 0;
+      gsync<NT>();
 
       // ---- token store
       if (!Ly.paged) {
@@ -669,34 +686,36 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       } else {
         const int ps = Ly.page_size, mlp = Ly.max_lp;
         int* refc = st.refc(b);
-        // fork, pass A: acquire the source pages of every winner (a thread per winner)
+        // fork: slot w of parity np takes winner w's source table (parity par).
+        // Only the pages that differ from what the slot held change reference
+        // counts; every acquire comes before every release.
+        // pass A: acquire (a thread per winner)
         for (int w = tid; w < nw; w += NT) {
           const int src = S.nsrc[w];
-          const int npg = (S.len[src] + ps - 1) / ps;
+          const int nn = (S.len[src] + ps - 1) / ps, no = S.npg[np][w];
           const int* bs = st.btab(par, b, src);
+          const int* bd = st.btab(np, b, w);
 #pragma unroll 4
-          for (int x = 0; x < npg; ++x) {
-            const int phys = bs[x];
-            if (phys >= 0) atomicAdd(&refc[phys], 1);
+          for (int x = 0; x < nn; ++x) {
+            const int nv = bs[x], ov = x < no ? bd[x] : -1;
+            if (nv >= 0 && nv != ov) atomicAdd(&refc[nv], 1);
           }
         }
         gsync<NT>();
-        // fork, pass B: release what each destination slot held, install the
-        // source's pages
+        // pass B: release what changed, install the source's pages
         for (int w = tid; w < beam; w += NT) {
+          const int src = w < nw ? S.nsrc[w] : 0;
+          const int nn = w < nw ? (S.len[src] + ps - 1) / ps : 0, no = S.npg[np][w];
+          const int* bs = st.btab(par, b, src);
           int* bd = st.btab(np, b, w);
-          for (int x = 0; x < mlp; ++x) {
-            const int phys = bd[x];
-            if (phys < 0) break;
-            if (atomicSub(&refc[phys], 1) == 1) page_push(st, b, phys, &S.ptop);
-            bd[x] = -1;
+          const int m = nn > no ? nn : no;
+#pragma unroll 4
+          for (int x = 0; x < m; ++x) {
+            const int nv = x < nn ? bs[x] : -1, ov = x < no ? bd[x] : -1;
+            if (ov >= 0 && ov != nv && atomicSub(&refc[ov], 1) == 1) page_push(st, b, ov, &S.ptop);
+            bd[x] = nv;
           }
-          if (w < nw) {
-            const int src = S.nsrc[w];
-            const int npg = (S.len[src] + ps - 1) / ps;
-            const int* bs = st.btab(par, b, src);
-            for (int x = 0; x < npg; ++x) bd[x] = bs[x];
-          }
+          S.npg[np][w] = nn;
         }
         gsync<NT>();
         // append / copy-on-write; page releases here are deferred past the
@@ -714,6 +733,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
               st.page(b, phys)[0] = tk;
             }
             bd[lpi] = phys;
+            S.npg[np][w] = lpi + 1;
           } else {
             const int phys = bd[lpi];
             if (phys < 0) continue;
@@ -744,6 +764,39 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       }
     }
 
+    // ---- the one merge relation the sources cannot show: a blank winner whose
+    // parent prefix was just rebuilt by an extension winner (prefix hash
+    // proposal, confirmed on the stored tokens)
+    if (step > 0) {
+      const int nw = S.nw;
+      for (int j = tid; j < nw; j += NT) {
+        if (S.ntok[j] != blank || S.nmsrc[j] >= 0 || S.nlen[j] < 1) continue;
+        const u64 key = S.nhp[j];
+        for (int q = 0; q < 2 * NT; ++q) {
+          const int slot = (int)((key + (u64)q) & (u64)(2 * NT - 1));
+          const int i = S.hval[slot];
+          if (i < 0) break;
+          if (S.hkey[slot] == key && S.nlen[i] == S.nlen[j] - 1) {
+            const int pq = atomicAdd(&S.npairs, 1);
+            if (pq < 2 * NT) {
+              S.pi[pq] = i;
+              S.pj[pq] = j;
+            }
+          }
+        }
+      }
+      gsync<NT>();
+      const int npairs = S.npairs < 2 * NT ? S.npairs : 2 * NT;
+      for (int pq = 0; pq < npairs; ++pq) {
+        const int i = S.pi[pq], j = S.pj[pq];
+        const int Li = S.nlen[i];
+        bool mism = false;
+        for (int x = tid; x < Li; x += NT) mism |= tok.get(np, i, x) != tok.get(np, j, x);
+        if (!g_any<NT>(mism) && tid == 0) S.nmsrc[j] = i;
+      }
+      gsync<NT>();
+    }
+
     // ---- commit
     const int nw = S.nw;
     for (int k = tid; k < nw; k += NT) {
@@ -754,6 +807,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       S.len[k] = S.nlen[k];
       S.h[k] = S.nh[k];
       S.hp[k] = S.nhp[k];
+      S.msrc[k] = S.nmsrc[k];
     }
     gsync<NT>();
     nlive = nw;
@@ -770,6 +824,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
     st.len()[rb + k] = S.len[k];
     st.h()[rb + k] = S.h[k];
     st.hp()[rb + k] = S.hp[k];
+    st.msrc()[rb + k] = S.msrc[k];
   }
   if (tid == 0) {
     if (Ly.paged) {
