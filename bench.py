@@ -41,6 +41,14 @@ sys.path.insert(0, ROOT)
 from ctc_prefix_beam_gb300 import synth  # noqa: E402
 
 METRIC = "frames/sec (B·T/s) and achieved HBM GB/s vs roofline, 1×GB300"
+DESCR = {
+    "tiny": "tiny: B=1 T=50 V=32 beam=4 nbest=4 offline, logits N(0,2) +4 on blank",
+    "bpe": "bpe: B=32 T=500 V=5000 beam=10 nbest=10 offline, lengths U[250,500], peaky logits",
+    "char": "char: B=16 T=1000 V=29 beam=128 nbest=128 offline, paged (page 16, max_seq_len 400), "
+            "logits N(0,1.5) +3 on blank, held labels +2",
+    "skip": "skip: B=256 T=2000 V=1024 beam=16 nbest=16 offline, blank threshold 0.999",
+    "stream": "stream (decoded offline): B=128 T=1600 V=5000 beam=10 nbest=10, peaky logits",
+}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -216,6 +224,61 @@ def job_frames(world: int, B: int, T: int) -> int:
     return world * B * T
 
 
+# ------------------------------------------------------------------ streaming (config 3)
+
+def run_stream(a, w, torch, D, dev):
+    """One step = one streaming session: stream_init, then every 16-frame tick of
+    the 128 staggered streams through stream_step_chunk, ticks resident in HBM."""
+    offsets = synth.stream_offsets(w)
+    nt = synth.n_ticks(w, offsets)
+    cache = {}
+    ticks = []
+    for k in range(nt):
+        c, nf = synth.stream_tick(w, k, offsets, cache, threads=os.cpu_count() or 8)
+        ticks.append((torch.from_numpy(c).to(dev), torch.from_numpy(nf).to(dev)))
+    cache.clear()
+    cfg = D.Config(beam=w.beam, nbest=w.nbest, blank_id=w.blank_id, max_seq_len=w.max_seq_len)
+    st = D.StreamState(cfg, w.B, w.V, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def session():
+        st.init()
+        for c, nf in ticks:
+            st.step_chunk(c, nf)
+
+    for _ in range(max(3, a.warmup)):
+        session()
+    torch.cuda.synchronize(dev)
+    fused = D.read_counters(st.buf)["fused"] > 0
+    ts = []
+    with Clocks(0, enabled=not a.no_clocks) as clk:
+        for _ in range(a.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            session()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+    ms = statistics.mean(ts)
+    frames = w.B * w.T
+    tick_bytes = w.B * w.chunk * w.V * 4
+    gbs = nt * tick_bytes / (ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": METRIC, "value": frames / (ms / 1e3), "unit": "frames/s", "n_gpus": 1, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"stream: {w.B} streams x {w.T} frames, V={w.V}, beam={w.beam}, chunks of {w.chunk} "
+                               f"frames over {nt} ticks, offsets U[0,160)",
+                   "l2": "inputs (4.5 GB of ticks) larger than L2"},
+        "ms_per_tick": ms / nt, "fused": fused,
+        "roofline": {"kernel": "k_fused" if fused else "k_step_warp", "bound": "hbm", "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_kind": peak_kind},
+        "gpu_launches": a.steps * (1 + nt),
+        "clocks": clk.summary(),
+    }), flush=True)
+
+
 # ------------------------------------------------------------------ our arm
 
 def main():
@@ -233,6 +296,10 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if w.streaming:
+        B.build()
+        D.lib()
+        return run_stream(a, w, torch, D, dev)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -355,8 +422,7 @@ def main():
         "metric": METRIC, "value": frames / (ms / 1e3), "unit": "frames/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B={Bn} T={T} V={V} beam={w.beam} nbest={w.nbest} offline, "
-                               f"lengths U[250,500], peaky logits",
+        "config": {"workload": DESCR.get(w.name, w.name),
                    "l2": "flushed between steps (2x L2 write)", "parallelism": f"rows x{world}"},
         "valid_frames_per_s": valid / (ms / 1e3),
         "stage_ms": stage_ms,
@@ -384,6 +450,15 @@ def main():
         dt = time.perf_counter() - t0
         res["cpu_baseline"] = {"value": reps * Bn * T / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
                                "sample": f"whole {w.name} batch (B={Bn}) x{reps}, {cores} threads, {dt:.2f} s"}
+        # the same oracle on one thread, on the first rows (about 2 s)
+        nr, t0 = 0, time.perf_counter()
+        while nr < Bn and time.perf_counter() - t0 < 2.0:
+            O.decode(lp_np[nr:nr + 1], lens_np[nr:nr + 1], beam=w.beam, nbest=w.nbest, blank=w.blank_id,
+                     cap=w.max_seq_len if w.max_seq_len > 0 else T, thr=w.blank_threshold, threads=1)
+            nr += 1
+        dt1 = time.perf_counter() - t0
+        res["cpu_baseline_1thread"] = {"value": nr * T / dt1, "unit": "frames/s", "cores": 1, "kind": "oracle",
+                                       "sample": f"first {nr} rows of the {w.name} batch, 1 thread, {dt1:.2f} s"}
     print(json.dumps(res), flush=True)
     if dist is not None:
         dist.destroy_process_group()
