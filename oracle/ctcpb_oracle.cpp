@@ -41,6 +41,8 @@
 //         (i, last_j) is folded into j's blank slot (pnb'_j = lse(pnb'_j, .))
 //         and dropped.
 //   3.4.4/5 score = lse(pb', pnb'); keep the best `beam` live candidates.
+//   8, 14 a speech mask skips the frames it marks 0 exactly like the blank
+//         threshold does (streaming decodes compare against it).
 // Readings where the page is silent or inconsistent:
 //   * ties rank by (score desc, source slot asc, token asc), blank's token is
 //     blank_id; a candidate with score <= NEG is dead and never kept;
@@ -164,6 +166,7 @@ struct Args {
   int32_t* out_lengths;
   float* out_scores;
   int out_len;
+  const uint8_t* mask;  // [B, T] speech mask (0: skip the frame), or null
 };
 
 bool keep_frame(float lpb, float thr, float log_thr) {
@@ -197,10 +200,13 @@ void decode_row(const Args& a, int b) {
   const float log_thr = log_threshold(a.thr);
   int len_b = std::min(std::max(a.lens ? a.lens[b] : a.T, 0), a.T);
 
-  // section 3.5: ordered list of kept frames
+  // section 3.5: ordered list of kept frames.  A speech mask (sections 8, 14
+  // and 15: frames the caller marks as non-speech bypass the decoder, like
+  // frames skipped by the blank threshold) removes frames as well.
   std::vector<int> sel;
   for (int t = 0; t < len_b; ++t)
-    if (keep_frame(rd(row(t) + a.blank), a.thr, log_thr)) sel.push_back(t);
+    if (keep_frame(rd(row(t) + a.blank), a.thr, log_thr) && (!a.mask || a.mask[(int64_t)b * a.T + t] != 0))
+      sel.push_back(t);
 
   std::vector<Hyp> beams;
   if (sel.empty()) {
@@ -408,15 +414,17 @@ int ctcpb_oracle_frame_lists(const float* lp, int64_t st, int R, int V, int blan
   return 0;
 }
 
-// Offline decode of B rows.  cap >= 1 is the per-hypothesis token cap.
+// Offline decode of B rows.  cap >= 1 is the per-hypothesis token cap; mask
+// ([B, T] uint8, may be null) skips every frame marked 0.
 // Outputs: tokens [B, nbest, out_len], lengths [B, nbest], scores [B, nbest].
 int ctcpb_oracle_decode(const float* lp, int64_t sb, int64_t st, const int32_t* lens, int B, int T, int V,
                         int beam, int nbest, int blank, int cap, float thr, int threads, int32_t* out_tokens,
-                        int32_t* out_lengths, float* out_scores, int out_len) {
+                        int32_t* out_lengths, float* out_scores, int out_len, const uint8_t* mask) {
   if (B < 0 || T < 0 || V < 2 || beam < 1 || nbest < 1 || nbest > beam || blank < 0 || blank >= V || cap < 1 ||
       out_len < 0)
     return -1;
-  Args a{lp, sb, st, lens, B, T, V, beam, nbest, blank, cap, thr, out_tokens, out_lengths, out_scores, out_len};
+  Args a{lp, sb, st, lens, B, T, V, beam, nbest, blank, cap, thr, out_tokens, out_lengths, out_scores, out_len,
+         mask};
   for_rows(B, threads, [&](int b) { decode_row(a, b); });
   return 0;
 }

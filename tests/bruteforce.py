@@ -49,12 +49,15 @@ def virtual_blank(V, blank):
     return f
 
 
-def skip_augmented(frames, blank, thr):
+def skip_augmented(frames, blank, thr, kept=None):
     """Kept frames of section 3.5 with a certain-blank frame before and after each
-    kept frame that follows skipped ones (the collapsed-blank correction)."""
+    kept frame that follows skipped ones (the collapsed-blank correction).
+    ``kept`` (frame indices in order) overrides the threshold selection."""
     frames = np.asarray(frames, dtype=np.float32)
     T, V = frames.shape
-    if thr >= 1.0:
+    if kept is not None:
+        kept = list(kept)
+    elif thr >= 1.0:
         kept = list(range(T))
     elif thr <= 0.0:
         kept = []

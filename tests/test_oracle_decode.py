@@ -268,3 +268,55 @@ def test_frame_lists_match_lexsort(oracle):
             assert out["front_id"][r] == order[C] and out["front_lp"][r] == v[order[C]]
         else:
             assert out["front_id"][r] == -1 and out["front_lp"][r] == NEG
+
+
+# ---- speech mask ("GPU CTC Prefix Beam Search Decoder", sections 8, 14, 15:
+# frames the caller marks as non-speech bypass the decoder like skipped frames)
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mask_equals_virtual_blank_brute_force(oracle, seed):
+    rng = np.random.default_rng(90 + seed)
+    V, T = 3, 9
+    lp = random_frames(rng, T, V, 1.2, 0, 0.5)
+    mask = (rng.random(T) < 0.6).astype(np.uint8)
+    mask[rng.integers(0, T)] = 1
+    kept = [t for t in range(T) if mask[t]]
+    aug, _ = skip_augmented(lp, 0, 1.0, kept=kept)
+    exact = posteriors(aug, 0)
+    beam = max(V, n_prefixes(V, len(kept)))
+    got, *_ = decoded(oracle, lp, beam=beam, mask=mask[None])
+    assert set(got) == set(exact)
+    for pre, s in got.items():
+        assert abs(s - exact[pre]) <= 2e-5 * max(1.0, abs(exact[pre]))
+
+
+def test_mask_of_ones_is_no_mask_and_zeros_decode_nothing(oracle):
+    rng = np.random.default_rng(7)
+    B, T, V = 3, 40, 12
+    lp = np.stack([random_frames(rng, T, V, 2.0, 0, 1.5) for _ in range(B)])
+    lens = np.array([40, 17, 1], np.int32)
+    ref = oracle.decode(lp, lens, beam=5)
+    ones = oracle.decode(lp, lens, beam=5, mask=np.ones((B, T), np.uint8))
+    for a, b in zip(ref, ones):
+        assert np.array_equal(a, b)
+    tok, ln, sc = oracle.decode(lp, lens, beam=5, mask=np.zeros((B, T), np.uint8))
+    assert (ln[:, 0] == 0).all() and (sc[:, 0] == 0.0).all()
+
+
+def test_mask_and_threshold_select_their_intersection(oracle):
+    rng = np.random.default_rng(11)
+    B, T, V = 4, 60, 10
+    x = rng.normal(0.0, 1.0, size=(B, T, V))
+    x[:, :, 0] += np.where(rng.random((B, T)) < 0.5, 9.0, 0.0)
+    lp = log_softmax(x)
+    thr = 0.99
+    mask = (rng.random((B, T)) < 0.7).astype(np.uint8)
+    sel, nsel = oracle.select_frames(lp, np.full(B, T, np.int32), 0, thr)
+    both = np.zeros((B, T), np.uint8)
+    for b in range(B):
+        for t in sel[b, :nsel[b]]:
+            both[b, t] = mask[b, t]
+    a = oracle.decode(lp, None, beam=6, thr=thr, mask=mask)
+    c = oracle.decode(lp, None, beam=6, mask=both)
+    for u, v in zip(a, c):
+        assert np.array_equal(u, v)
