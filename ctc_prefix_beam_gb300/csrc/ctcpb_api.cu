@@ -42,8 +42,9 @@ Layout offline_layout(const ctcpb_config* c, int B, int T, int V) {
 }
 
 Layout stream_layout(const ctcpb_config* c, int B, int V) {
+  // T_sel = kStreamTile: the selection holds one tile's chunk rows (speech-masked streaming)
   return make_layout(B, V, c->beam, stream_cap(c), c->paged, c->paged ? c->page_size : 16, c->blank_id,
-                     default_list_len(c->beam, V, c->list_len), kStreamTile, 0);
+                     default_list_len(c->beam, V, c->list_len), kStreamTile, kStreamTile);
 }
 
 int check_buf(const void* p, size_t have, size_t need) {
@@ -185,6 +186,30 @@ int ctcpb_stream_step_chunk(const ctcpb_config* cfg, void* state, size_t state_b
     if (try_fused(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s)) continue;
     TRY(launch_prepass(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s));
     TRY(launch_step(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s));
+  }
+  return CTCPB_OK;
+}
+
+int ctcpb_stream_step_chunk_masked(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                                   const float* lp_chunk, int64_t stride_b, int64_t stride_t,
+                                   const int32_t* n_frames, const uint8_t* is_speech, int64_t mask_stride,
+                                   int chunk_T, ctcpb_stream_t stream) {
+  int rc = check_cfg(cfg, V);
+  if (rc) return rc;
+  if (B < 0 || chunk_T < 0) return CTCPB_EINVAL;
+  if (B == 0 || chunk_T == 0) return CTCPB_OK;
+  if (stride_t < V || stride_b < V || mask_stride < chunk_T) return CTCPB_EINVAL;
+  if (!lp_chunk || !is_speech) return CTCPB_ENULL;
+  const Layout lay = stream_layout(cfg, B, V);
+  if ((rc = check_buf(state, state_bytes, lay.total))) return rc;
+  View st{(char*)state, lay};
+  cudaStream_t s = (cudaStream_t)stream;
+  for (int t0 = 0; t0 < chunk_T; t0 += kStreamTile) {
+    const int tl = chunk_T - t0 < kStreamTile ? chunk_T - t0 : kStreamTile;
+    TRY(launch_select_tile(st, is_speech, mask_stride, n_frames, chunk_T, t0, tl, s));
+    if (try_fused(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s)) continue;
+    TRY(launch_prepass(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s));
+    TRY(launch_step(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s));
   }
   return CTCPB_OK;
 }

@@ -55,7 +55,7 @@ struct Layout {
   int ldseq;   // flat: labels per hypothesis row
   int max_lp;  // paged: logical pages per hypothesis
   int ppr;     // paged: physical pages per row
-  int T_sel;   // offline: frames per row of the selection list (0 when streaming)
+  int T_sel;   // selection entries per row: offline T (frames); streaming kStreamTile (one tile's chunk rows)
   size_t rec_bytes;
   size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp, o_msrc;
   size_t o_clist, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;

@@ -161,6 +161,28 @@ __global__ void __launch_bounds__(256) k_select(View st, const float* __restrict
   if (tid == 0) nsel[b] = n;
 }
 
+// Speech-masked streaming: the chunk rows of tile [tile_start, tile_start +
+// tile_len) that stream b decodes (mask != 0), in order, into sel/nsel.  One
+// warp per stream.
+__global__ void __launch_bounds__(32) k_select_tile(View st, const uint8_t* __restrict__ mask, long long mstride,
+                                                    const int* __restrict__ nframes, int chunk_T, int tile_start,
+                                                    int tile_len) {
+  const int b = blockIdx.x, lane = threadIdx.x;
+  int nf = nframes ? nframes[b] : chunk_T;
+  nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
+  const int end = tile_start + tile_len < nf ? tile_start + tile_len : nf;
+  int* sel = st.sel() + (size_t)b * st.lay.T_sel;
+  int n = 0;
+  for (int j0 = tile_start; j0 < end; j0 += 32) {
+    const int j = j0 + lane;
+    const bool keep = j < end && mask[(long long)b * mstride + j] != 0;
+    const unsigned m = __ballot_sync(FULL, keep);
+    if (keep) sel[n + __popc(m & ((1u << lane) - 1u))] = j;
+    n += __popc(m);
+  }
+  if (lane == 0) st.nsel()[b] = n;
+}
+
 // ------------------------------------------------------------------ step
 //
 // One block of NT threads owns one row for the whole call.  The beam state of
@@ -254,7 +276,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V;
   const float NEG = CTCPB_NEG;
 
-  if (mode == 1) {
+  if (mode != 0) {
     const Header* hd = st.hdr();
     bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
               hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
@@ -267,16 +289,20 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
   }
 
   RowHdr* rh = st.rows() + b;
-  int nsteps;
-  if (mode == 0) {
-    nsteps = st.nsel()[b];
-  } else {
+  // mode 0: offline (frame list); 1: streaming, every frame of the tile;
+  // 2: streaming with a speech mask (the tile's selected chunk rows)
+  int nsteps, nft = 0;  // nft: the tile's frames of this stream, skipped ones included
+  if (mode != 0) {
     int nf = nframes ? nframes[b] : chunk_T;
     nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
-    nsteps = nf - tile_start;
-    nsteps = nsteps < 0 ? 0 : (nsteps > tile_len ? tile_len : nsteps);
+    nft = nf - tile_start;
+    nft = nft < 0 ? 0 : (nft > tile_len ? tile_len : nft);
   }
-  if (nsteps == 0) return;
+  nsteps = mode == 1 ? nft : st.nsel()[b];
+  if (nsteps == 0) {
+    if (mode == 2 && tid == 0) rh->tcount += nft;  // every frame of the tile was skipped
+    return;
+  }
 
   int step = rh->step, tcount = rh->tcount, t_prev = rh->t_prev, nlive = rh->nlive, par = rh->parity;
   const size_t rb = (size_t)b * beam;
@@ -308,8 +334,9 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
   gsync<NT>();
 
   for (int s = 0; s < nsteps; ++s) {
-    const int t = mode == 0 ? st.sel()[(size_t)b * Ly.T_sel + s] : tcount + s;
-    const float* row = lp + (long long)b * sb + (long long)(mode == 0 ? t : tile_start + s) * stt;
+    const int srow = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;  // batch or chunk row
+    const int t = mode == 0 ? srow : (mode == 1 ? tcount + s : tcount + srow - tile_start);
+    const float* row = lp + (long long)b * sb + (long long)srow * stt;
     char* rec = st.rec(b, s);
     {
       const RecHdr* rhd = (const RecHdr*)rec;
@@ -832,7 +859,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       st.pnext()[b] = S.pnext;
     }
     rh->step = step;
-    rh->tcount = mode == 1 ? tcount + nsteps : rh->tcount;
+    rh->tcount = mode == 0 ? rh->tcount : tcount + nft;
     rh->t_prev = t_prev;
     rh->nlive = nlive;
     rh->parity = par;
@@ -931,6 +958,13 @@ cudaError_t launch_step(const View& st, const float* lp, long long sb, long long
     return launch_step_warp(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   if (st.lay.beam <= 32) return launch_step_t<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   return launch_step_t<128>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+}
+
+cudaError_t launch_select_tile(const View& st, const uint8_t* mask, long long mstride, const int* nframes,
+                               int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  if (st.lay.B == 0) return cudaSuccess;
+  k_select_tile<<<st.lay.B, 32, 0, s>>>(st, mask, mstride, nframes, chunk_T, tile_start, tile_len);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_output(const View& st, int nbest, int* out_tokens, int* out_lengths, float* out_scores,

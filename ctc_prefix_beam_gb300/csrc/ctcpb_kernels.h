@@ -6,6 +6,9 @@
 namespace ctcpb {
 
 cudaError_t launch_init(const View& st, cudaStream_t s);
+// Speech-masked streaming: the tile's selected chunk rows per stream.
+cudaError_t launch_select_tile(const View& st, const uint8_t* mask, long long mstride, const int* nframes,
+                               int chunk_T, int tile_start, int tile_len, cudaStream_t s);
 cudaError_t launch_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
                           int mode, float log_thr, int* sel, int* nsel, cudaStream_t s);
 cudaError_t launch_prepass(const View& st, const float* lp, long long sb, long long stt, int mode,

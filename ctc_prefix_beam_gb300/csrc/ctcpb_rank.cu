@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) k_prepass(View st, const float* __restric
     const int b = (int)(it % Ly.B);
     const int s = (int)(it / Ly.B);
     const float* row;
-    if (mode == 0) {
+    if (mode != 1) {
       if (s >= st.nsel()[b]) continue;
       const int t = st.sel()[(size_t)b * Ly.T_sel + s];
       row = lp + (long long)b * sb + (long long)t * stt;
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(256) k_prepass(View st, const float* __restric
     }
     char* r = st.rec(b, s);
     RecHdr* h = (RecHdr*)r;
-    if (lane == 0) h->t = mode == 0 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
+    if (lane == 0) h->t = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
     rank_row(row, Ly.V, Ly.blank, Ly.L, bufs[wid], lane, rec_ids(r), rec_lps(r, Ly.Lpad), &h->cnt, &h->lpb,
              &h->front_lp, &h->front_id);
   }

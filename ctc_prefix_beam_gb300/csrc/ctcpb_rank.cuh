@@ -186,7 +186,7 @@ struct RecItems {
   __device__ bool probe(long long it, const float** row, int* t) const {
     const int B = st.lay.B;
     const int b = (int)(it % B), s = (int)(it / B);
-    if (mode == 0) {
+    if (mode != 1) {  // offline (frame index) or masked streaming (chunk row), from the selection
       if (s >= st.nsel()[b]) return false;
       *t = st.sel()[(size_t)b * st.lay.T_sel + s];
     } else {

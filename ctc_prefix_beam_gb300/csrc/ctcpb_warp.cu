@@ -591,7 +591,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V, Lpad = Ly.Lpad;
   const float NEG = CTCPB_NEG;
 
-  if (mode == 1) {
+  if (mode != 0) {
     const Header* hd = st.hdr();
     bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
               hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
@@ -602,16 +602,20 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
       return;
     }
   }
-  int nsteps;
-  if (mode == 0) {
-    nsteps = st.nsel()[b];
-  } else {
+  // mode 0: offline (frame list); 1: streaming, every frame of the tile;
+  // 2: streaming with a speech mask (the tile's selected chunk rows)
+  int nsteps, nft = 0;  // nft: the tile's frames of this stream, skipped ones included
+  if (mode != 0) {
     int nf = nframes ? nframes[b] : chunk_T;
     nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
-    nsteps = nf - tile_start;
-    nsteps = nsteps < 0 ? 0 : (nsteps > tile_len ? tile_len : nsteps);
+    nft = nf - tile_start;
+    nft = nft < 0 ? 0 : (nft > tile_len ? tile_len : nft);
   }
-  if (nsteps == 0) return;
+  nsteps = mode == 1 ? nft : st.nsel()[b];
+  if (nsteps == 0) {
+    if (mode == 2 && lane == 0) st.rows()[b].tcount += nft;  // every frame of the tile was skipped
+    return;
+  }
 
   const RowHdr rh0 = st.rows()[b];
   int step = rh0.step, t_prev = rh0.t_prev, nlive = rh0.nlive, par = rh0.parity;
@@ -719,8 +723,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     const float lpb = cur.lpb;
     const int my_id = lane < Ly.L ? cur.id : -1;
     const float my_lp = lane < Ly.L ? cur.lp : NEG;
-    const int t = mode == 0 ? cur.t : tcount + s;
-    const float* row = lpb_row + (long long)(mode == 0 ? cur.t : tile_start + s) * stt;
+    const int t = mode == 0 ? cur.t : (mode == 1 ? tcount + s : tcount + cur.t - tile_start);
+    const float* row = lpb_row + (long long)(mode != 1 ? cur.t : tile_start + s) * stt;
     const bool gap = t > t_prev + 1;
     const bool live = lane < nlive;
     // lp[t][last] of this lane's hypothesis, gathered by the previous step
@@ -730,7 +734,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     // lp[t_{s+1}][x] for every label x that can be "last" at step s+1: the
     // current lasts (slot k) and this step's list (slot beam + position)
     if (s + 1 < nsteps) {
-      const float* row1 = lpb_row + (long long)(mode == 0 ? t1 : tile_start + s + 1) * stt;
+      const float* row1 = lpb_row + (long long)(mode != 1 ? t1 : tile_start + s + 1) * stt;
       float* gdst = W.gath[(s + 1) & 1];
       if (live && len > 0) cp_async4(gdst + lane, row1 + last);
       if (lane < cnt && beam + lane < kGath) cp_async4(gdst + beam + lane, row1 + my_id);
@@ -939,7 +943,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
 #endif
     RowHdr rr = rh0;
     rr.step = step;
-    rr.tcount = mode == 1 ? tcount + nsteps : rh0.tcount;
+    rr.tcount = mode == 0 ? rh0.tcount : tcount + nft;
     rr.t_prev = t_prev;
     rr.nlive = nlive;
     rr.parity = par;

@@ -81,6 +81,7 @@ def lib():
                 "ctcpb_state_size": (I, [cfgp, I, I, ctypes.POINTER(SZ)]),
                 "ctcpb_stream_init": (I, [cfgp, P, SZ, I, I, P]),
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
+                "ctcpb_stream_step_chunk_masked": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, P, I64, I, P]),
                 "ctcpb_read_state": (I, [cfgp, P, SZ, I, I, P, P, P, I, P]),
                 "ctcpb_read_status": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
                 "ctcpb_read_counters": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -204,7 +205,10 @@ class StreamState:
         _check(lib().ctcpb_stream_init(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
                                        self.V, _stream(self.buf.device)), "stream_init")
 
-    def step_chunk(self, lp_chunk: torch.Tensor, n_frames: Optional[torch.Tensor] = None):
+    def step_chunk(self, lp_chunk: torch.Tensor, n_frames: Optional[torch.Tensor] = None,
+                   is_speech: Optional[torch.Tensor] = None):
+        """Decode one chunk [B, chunk_T, V] for every stream.  ``is_speech``
+        (CUDA uint8 [B, chunk_T]) skips the frames it marks 0."""
         lp = _f32_3d(lp_chunk)
         if lp.shape[0] != self.B or lp.shape[2] != self.V:
             raise ValueError("chunk must be [B, chunk_T, V] for this state")
@@ -212,6 +216,15 @@ class StreamState:
             if n_frames.dtype != torch.int32 or not n_frames.is_cuda:
                 raise ValueError("n_frames must be a CUDA int32 tensor [B]")
             n_frames = n_frames.contiguous()
+        if is_speech is not None:
+            if is_speech.dtype != torch.uint8 or not is_speech.is_cuda or is_speech.dim() != 2 \
+                    or is_speech.shape[0] != self.B or is_speech.shape[1] < lp.shape[1] or is_speech.stride(1) != 1:
+                raise ValueError("is_speech must be a CUDA uint8 tensor [B, >= chunk_T] with unit column stride")
+            _check(lib().ctcpb_stream_step_chunk_masked(
+                ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B, self.V, _ptr(lp), lp.stride(0),
+                lp.stride(1), _ptr(n_frames), _ptr(is_speech), is_speech.stride(0), lp.shape[1],
+                _stream(lp.device)), "stream_step_chunk_masked")
+            return
         _check(lib().ctcpb_stream_step_chunk(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
                                              self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames),
                                              lp.shape[1], _stream(lp.device)), "stream_step_chunk")

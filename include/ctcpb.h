@@ -181,6 +181,25 @@ int ctcpb_stream_step_chunk(const ctcpb_config* cfg, void* state, size_t state_b
                             int chunk_T, ctcpb_stream_t stream);
 
 /*
+ * ctcpb_stream_step_chunk with a speech mask (section 8's is_speech_mask of
+ * ctc_beam_search_chunk; sections 14 and 15: frames marked as non-speech
+ * bypass the decoder).
+ *   is_speech    [B, chunk_T] uint8 device array, row stride mask_stride
+ *                (>= chunk_T): frame j of stream b is decoded iff
+ *                is_speech[b * mask_stride + j] != 0.
+ * A masked frame still advances the stream's frame counter; the decoder
+ * treats it like a frame skipped by the blank threshold (section 3.5): the
+ * next decoded frame collapses the beam's blank-ending residue (section 3.4).
+ * Decoding a stream in any chunking gives the same result as decoding its
+ * frames offline with the same mask.  Errors: CTCPB_ENULL for a null mask,
+ * CTCPB_EINVAL for mask_stride < chunk_T, otherwise as ctcpb_stream_step_chunk.
+ */
+int ctcpb_stream_step_chunk_masked(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                                   const float* lp_chunk, int64_t stride_b, int64_t stride_t,
+                                   const int32_t* n_frames, const uint8_t* is_speech, int64_t mask_stride,
+                                   int chunk_T, ctcpb_stream_t stream);
+
+/*
  * Write the current N best of every stream (section 8, read_streaming_results)
  * in the output layout of ctcpb_decode_offline.  Does not modify the state.
  */

@@ -94,6 +94,12 @@ def test_host_validation_before_any_launch(lib):
     assert lib.ctcpb_stream_init(ctypes.byref(c), ctypes.c_void_p(512), 16, 4, 5000, NULL) == D.ESIZE
     assert lib.ctcpb_stream_step_chunk(ctypes.byref(c), ctypes.c_void_p(512), 16, 4, 5000, NULL, 5000, 5000,
                                        NULL, 16, NULL) == D.ENULL
+    # speech-masked streaming: a null mask, a mask row shorter than the chunk
+    big = ctypes.c_void_p(1 << 20)
+    assert lib.ctcpb_stream_step_chunk_masked(ctypes.byref(c), big, 1 << 40, 4, 5000, big, 5000, 5000, NULL, NULL,
+                                              16, 16, NULL) == D.ENULL
+    assert lib.ctcpb_stream_step_chunk_masked(ctypes.byref(c), big, 1 << 40, 4, 5000, big, 5000, 5000, NULL, big,
+                                              8, 16, NULL) == D.EINVAL
     assert lib.ctcpb_read_status(NULL, NULL) == D.ENULL
     assert lib.ctcpb_topk_prepass(ctypes.byref(c), NULL, 10, 5, 5000, NULL, NULL, NULL, NULL, NULL, NULL,
                                   NULL) == D.EINVAL
