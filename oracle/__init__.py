@@ -70,7 +70,7 @@ def lib():
             L.ctcpb_oracle_decode.argtypes = [
                 f32p, ctypes.c_int64, ctypes.c_int64, i32p, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_float, ctypes.c_int, i32p, i32p, f32p, ctypes.c_int, ctypes.c_void_p]
+                ctypes.c_float, ctypes.c_int, i32p, i32p, f32p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
             _lib = L
     return _lib
 
@@ -148,12 +148,12 @@ def frame_lists(rows: np.ndarray, blank: int, C: int):
 
 def decode(lp: np.ndarray, lens=None, *, beam: int, nbest: int | None = None, blank: int = 0,
            cap: int | None = None, thr: float = 1.0, threads: int = 0, out_len: int | None = None,
-           mask: np.ndarray | None = None):
+           mask: np.ndarray | None = None, space: int = -1):
     """Offline CTC prefix beam search of a [B, T, V] float32 batch.
 
     ``cap`` is max_seq_len (default T), ``thr`` the blank-skip threshold
     (>= 1 keeps all frames), ``mask`` an optional [B, T] speech mask (frames
-    marked 0 are skipped too).  Returns (tokens [B, nbest, out_len] int32
+    marked 0 are skipped too), ``space`` the word-boundary label (-1: none).  Returns (tokens [B, nbest, out_len] int32
     padded with -1, lengths [B, nbest] int32, scores [B, nbest] float32).
     """
     lp = _f32(lp)
@@ -172,7 +172,7 @@ def decode(lp: np.ndarray, lens=None, *, beam: int, nbest: int | None = None, bl
             raise ValueError("mask must be [B, T]")
     rc = lib().ctcpb_oracle_decode(lp.ravel(), T * V, V, lens, B, T, V, beam, nbest, blank, cap,
                                    float(thr), threads, tok.ravel(), ln.ravel(), sc.ravel(),
-                                   out_len, None if mk is None else mk.ctypes.data)
+                                   out_len, None if mk is None else mk.ctypes.data, int(space))
     if rc != 0:
         raise ValueError(f"oracle decode rejected its arguments (rc={rc})")
     return tok, ln, sc

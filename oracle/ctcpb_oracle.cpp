@@ -43,6 +43,9 @@
 //   3.4.4/5 score = lse(pb', pnb'); keep the best `beam` live candidates.
 //   8, 14 a speech mask skips the frames it marks 0 exactly like the blank
 //         threshold does (streaming decodes compare against it).
+//   3.4.1/3.4.2 with a word-boundary label (space_id): its extension always
+//         uses lse(pb, pnb) -- every space frame is a token of its own -- and a
+//         space-ending beam gets no stay contribution.
 // Readings where the page is silent or inconsistent:
 //   * ties rank by (score desc, source slot asc, token asc), blank's token is
 //     blank_id; a candidate with score <= NEG is dead and never kept;
@@ -167,6 +170,7 @@ struct Args {
   float* out_scores;
   int out_len;
   const uint8_t* mask;  // [B, T] speech mask (0: skip the frame), or null
+  int space;            // word-boundary label, or -1
 };
 
 bool keep_frame(float lpb, float thr, float log_thr) {
@@ -262,6 +266,10 @@ void decode_row(const Args& a, int b) {
         if (into[j] >= 0) folded[into[j]].push_back(beams[j].last(a.blank));
 
       const float lpb = rd(lpt + a.blank);
+      // sections 3.4.1/3.4.2 with a word-boundary label: the space extension
+      // always takes lp[space] + lse(pb, pnb) (it never repeats into the
+      // previous space), so a space-ending beam has no stay contribution
+      const int space = (a.space >= 0 && a.space != a.blank) ? a.space : -1;
       cands.clear();
       for (int k = 0; k < K; ++k) {
         const Hyp& h = beams[k];
@@ -269,13 +277,13 @@ void decode_row(const Args& a, int b) {
         const bool empty = h.pre.empty();
         // section 3.4.2 blank slot, with section 3.4.1's stay contribution
         float bpb = add(lpb, A[k]);
-        float bpnb = (!empty && !gap) ? add(rd(lpt + last), pnb[k]) : NEG;
+        float bpnb = (!empty && !gap && last != space) ? add(rd(lpt + last), pnb[k]) : NEG;
         if (into[k] >= 0) {
           // section 3.4.3: fold candidate (i, last_k) into this blank slot; its
           // value is the section 3.4.1 table entry, which takes the repeat
           // path (pb only) when last_k is also the last label of l_i
           int i = into[k];
-          const bool rep = !beams[i].pre.empty() && beams[i].pre.back() == last;
+          const bool rep = !beams[i].pre.empty() && beams[i].pre.back() == last && last != space;
           float ext = rep ? add(rd(lpt + last), pb[i]) : add(rd(lpt + last), A[i]);
           bpnb = lse(bpnb, ext);
         }
@@ -287,7 +295,7 @@ void decode_row(const Args& a, int b) {
           if (c == a.blank) continue;
           if (std::find(folded[k].begin(), folded[k].end(), c) != folded[k].end()) continue;
           float v = rd(lpt + c);
-          float ext = (!empty && c == last) ? add(v, pb[k]) : add(v, A[k]);
+          float ext = (!empty && c == last && c != space) ? add(v, pb[k]) : add(v, A[k]);
           if (ext > NEG) cands.push_back(Cand{ext, k, c, NEG, ext});
         }
       }
@@ -415,16 +423,18 @@ int ctcpb_oracle_frame_lists(const float* lp, int64_t st, int R, int V, int blan
 }
 
 // Offline decode of B rows.  cap >= 1 is the per-hypothesis token cap; mask
-// ([B, T] uint8, may be null) skips every frame marked 0.
+// ([B, T] uint8, may be null) skips every frame marked 0; space_id (-1: none)
+// is the word-boundary label.
 // Outputs: tokens [B, nbest, out_len], lengths [B, nbest], scores [B, nbest].
 int ctcpb_oracle_decode(const float* lp, int64_t sb, int64_t st, const int32_t* lens, int B, int T, int V,
                         int beam, int nbest, int blank, int cap, float thr, int threads, int32_t* out_tokens,
-                        int32_t* out_lengths, float* out_scores, int out_len, const uint8_t* mask) {
+                        int32_t* out_lengths, float* out_scores, int out_len, const uint8_t* mask,
+                        int space_id) {
   if (B < 0 || T < 0 || V < 2 || beam < 1 || nbest < 1 || nbest > beam || blank < 0 || blank >= V || cap < 1 ||
       out_len < 0)
     return -1;
   Args a{lp, sb, st, lens, B, T, V, beam, nbest, blank, cap, thr, out_tokens, out_lengths, out_scores, out_len,
-         mask};
+         mask, space_id};
   for_rows(B, threads, [&](int b) { decode_row(a, b); });
   return 0;
 }

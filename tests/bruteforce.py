@@ -14,28 +14,31 @@ import numpy as np
 NEG32 = float(np.finfo(np.float32).min)
 
 
-def collapse(path, blank):
+def collapse(path, blank, space=None):
+    """Merge repeats, drop blanks.  A word-boundary label ``space`` is never
+    merged with itself: every frame of it is a token of its own."""
     out = []
     prev = None
     for a in path:
-        if a != prev and a != blank:
+        if a != blank and (a != prev or a == space):
             out.append(a)
         prev = a
     return tuple(out)
 
 
-def posteriors(frames, blank, cap=None):
+def posteriors(frames, blank, cap=None, space=None):
     """{prefix: log P(prefix)} over all alignments of ``frames`` ([T, V], log-probs).
 
     Labels whose log-prob is <= -FLT_MAX are impossible and not enumerated.
     With ``cap``, alignments collapsing to more than ``cap`` labels are dropped.
+    ``space``: the word-boundary label of ``collapse``.
     """
     frames = np.asarray(frames, dtype=np.float64)
     T, V = frames.shape
     allowed = [[c for c in range(V) if frames[t, c] > NEG32] for t in range(T)]
     acc = {}
     for path in itertools.product(*allowed):
-        lab = collapse(path, blank)
+        lab = collapse(path, blank, space)
         if cap is not None and len(lab) > cap:
             continue
         lp = sum(frames[t, a] for t, a in enumerate(path))

@@ -320,3 +320,48 @@ def test_mask_and_threshold_select_their_intersection(oracle):
     c = oracle.decode(lp, None, beam=6, mask=both)
     for u, v in zip(a, c):
         assert np.array_equal(u, v)
+
+
+# ---- word-boundary label ("GPU CTC Prefix Beam Search Decoder", sections
+# 3.4.1/3.4.2: the space extension always takes lp[space] + lse(pb, pnb), and
+# a space-ending beam has no stay path): every space frame is its own token
+
+@pytest.mark.parametrize("seed", range(5))
+def test_space_unpruned_equals_brute_force(oracle, seed):
+    rng = np.random.default_rng(120 + seed)
+    V, T, space = 3, 8, 2
+    lp = random_frames(rng, T, V, 1.0, 0, 0.3)
+    exact = posteriors(lp, 0, space=space)
+    beam = n_prefixes(V, T)
+    got, *_ = decoded(oracle, lp, beam=beam, space=space)
+    assert set(got) == set(exact)
+    for pre, s in got.items():
+        assert abs(s - exact[pre]) <= 2e-5 * max(1.0, abs(exact[pre]))
+    # the collapse really differs from the plain one on these frames
+    assert set(exact) != set(posteriors(lp, 0))
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_space_with_skipping_equals_brute_force(oracle, seed):
+    rng = np.random.default_rng(140 + seed)
+    V, T, space = 3, 9, 1
+    x = rng.normal(0.0, 1.0, size=(T, V))
+    x[rng.random(T) < 0.4, 0] += 9.0
+    lp = log_softmax(x)
+    thr = 0.99
+    aug, kept = skip_augmented(lp, 0, thr)
+    exact = posteriors(aug, 0, space=space)
+    beam = max(V, n_prefixes(V, len(kept)))
+    got, *_ = decoded(oracle, lp, beam=beam, thr=thr, space=space)
+    assert set(got) == set(exact)
+    for pre, s in got.items():
+        assert abs(s - exact[pre]) <= 2e-5 * max(1.0, abs(exact[pre]))
+
+
+def test_space_equal_to_blank_has_no_effect(oracle):
+    rng = np.random.default_rng(5)
+    lp = np.stack([random_frames(rng, 30, 8, 2.0, 0, 1.0) for _ in range(3)])
+    a = oracle.decode(lp, None, beam=6)
+    b = oracle.decode(lp, None, beam=6, space=0)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
