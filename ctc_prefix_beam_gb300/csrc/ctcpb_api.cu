@@ -25,6 +25,8 @@ int check_cfg(const ctcpb_config* c, int V) {
   if (c->paged && (c->page_size < 1 || c->page_size > 1024)) return CTCPB_EINVAL;
   if (c->list_len < 0) return CTCPB_EINVAL;
   if (!finite_or_inf(c->blank_threshold)) return CTCPB_EINVAL;
+  if (c->word_boundary != 0 && c->word_boundary != 1) return CTCPB_EINVAL;
+  if (c->word_boundary && (c->space_id < 0 || c->space_id >= V)) return CTCPB_EINVAL;
   return CTCPB_OK;
 }
 
@@ -34,17 +36,19 @@ int offline_cap(const ctcpb_config* c, int T) {
   return (c->max_seq_len > 0 && c->max_seq_len < t) ? c->max_seq_len : t;
 }
 
+int space_of(const ctcpb_config* c) { return c->word_boundary ? c->space_id : -1; }
+
 int stream_cap(const ctcpb_config* c) { return c->max_seq_len > 0 ? c->max_seq_len : kStreamDefaultCap; }
 
 Layout offline_layout(const ctcpb_config* c, int B, int T, int V) {
   return make_layout(B, V, c->beam, offline_cap(c, T), c->paged, c->paged ? c->page_size : 16, c->blank_id,
-                     default_list_len(c->beam, V, c->list_len), T > 0 ? T : 1, T > 0 ? T : 1);
+                     default_list_len(c->beam, V, c->list_len), T > 0 ? T : 1, T > 0 ? T : 1, space_of(c));
 }
 
 Layout stream_layout(const ctcpb_config* c, int B, int V) {
   // T_sel = kStreamTile: the selection holds one tile's chunk rows (speech-masked streaming)
   return make_layout(B, V, c->beam, stream_cap(c), c->paged, c->paged ? c->page_size : 16, c->blank_id,
-                     default_list_len(c->beam, V, c->list_len), kStreamTile, kStreamTile);
+                     default_list_len(c->beam, V, c->list_len), kStreamTile, kStreamTile, space_of(c));
 }
 
 int check_buf(const void* p, size_t have, size_t need) {

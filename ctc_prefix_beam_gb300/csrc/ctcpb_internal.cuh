@@ -31,7 +31,7 @@ constexpr u32 kVersion = 1u;
 // per chunk tile).  Every slab is 256-byte aligned; offsets are from the base.
 struct Header {
   u32 magic, version;
-  int32_t B, V, beam, cap, paged, page_size, blank, list_len, tile, pad0;
+  int32_t B, V, beam, cap, paged, page_size, blank, list_len, tile, space;
   u32 status;  // CTCPB_DEV_* bits
   u32 counters[5];  // decode steps, unproven first sets, exhaustive selections, full-frame scans,
                     // hash-proposed merges
@@ -52,6 +52,7 @@ struct RowHdr {
 
 struct Layout {
   int B, V, beam, cap, paged, page_size, blank, L, Lpad, tile;
+  int space;   // word-boundary label (sections 3.4.1/3.4.2), -1: none
   int ldseq;   // flat: labels per hypothesis row
   int max_lp;  // paged: logical pages per hypothesis
   int ppr;     // paged: physical pages per row
@@ -78,8 +79,9 @@ inline int default_list_len(int beam, int V, int list_len) {
 // Build the layout.  tile = records per row; T_sel = selection list length
 // (offline T, 0 when streaming).
 inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_size, int blank, int L,
-                          int tile, int T_sel) {
+                          int tile, int T_sel, int space = -1) {
   Layout o{};
+  o.space = (space >= 0 && space != blank) ? space : -1;
   o.B = B; o.V = V; o.beam = beam; o.cap = cap; o.paged = paged; o.page_size = page_size;
   o.blank = blank; o.L = L; o.Lpad = (int)align_up((size_t)L, 4); o.tile = tile; o.T_sel = T_sel;
   o.ldseq = (int)align_up((size_t)cap, 16);

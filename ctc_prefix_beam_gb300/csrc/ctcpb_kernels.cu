@@ -88,7 +88,7 @@ __global__ void k_init(View st) {
     h->magic = kMagic;
     h->version = kVersion;
     h->B = L.B; h->V = L.V; h->beam = L.beam; h->cap = L.cap; h->paged = L.paged;
-    h->page_size = L.page_size; h->blank = L.blank; h->list_len = L.L; h->tile = L.tile;
+    h->page_size = L.page_size; h->blank = L.blank; h->list_len = L.L; h->tile = L.tile; h->space = L.space;
     h->status = 0u;
     for (int i = 0; i < 5; ++i) h->counters[i] = 0u;
     for (int i = 0; i < 8; ++i) h->phase_cycles[i] = 0ull;
@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
   const Layout& Ly = st.lay;
   const int b = blockIdx.x, tid = threadIdx.x;
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V;
+  const int space = Ly.space;  // word-boundary label, -1: none
   const float NEG = CTCPB_NEG;
 
   if (mode != 0) {
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
     bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
               hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
               hd->page_size == Ly.page_size && hd->blank == Ly.blank && hd->list_len == Ly.L &&
-              hd->tile == Ly.tile;
+              hd->tile == Ly.tile && hd->space == Ly.space;
     if (!ok) {
       if (tid == 0) set_status(st, CTCPB_DEV_HEADER);
       return;
@@ -428,8 +429,11 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         S.pbg[k] = pb;
         S.lpl[k] = lpl;
         S.bpb[k] = dadd(S.lpb, A);
-        S.bpnb[k] = (L > 0 && !gap) ? dadd(lpl, pnb) : NEG;
-        S.rep[k] = (L > 0 && L < cap) ? dadd(lpl, pb) : NEG;
+        // a space-ending beam has no stay path, and its candidate (k, last)
+        // extends from both paths (every space frame is a token)
+        const bool spc = S.last[k] == space;
+        S.bpnb[k] = (L > 0 && !gap && !spc) ? dadd(lpl, pnb) : NEG;
+        S.rep[k] = (L > 0 && L < cap) ? dadd(lpl, spc ? A : pb) : NEG;
         S.repdead[k] = 0;
         S.into[k] = -1;
         for (int w = 0; w < (kMaxList + 31) / 32; ++w) S.excl[k][w] = 0u;
@@ -450,10 +454,11 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         const int i = S.into[j];
         if (i < 0) continue;
         const int c = S.last[j];
-        const bool rep_i = S.len[i] > 0 && S.last[i] == c;
+        const bool same = S.len[i] > 0 && S.last[i] == c;  // the folded candidate is i's (i, last) entry
+        const bool rep_i = same && c != space;
         const float ext = rep_i ? dadd(S.lpl[j], S.pbg[i]) : dadd(S.lpl[j], S.A[i]);
         S.bpnb[j] = dlse(S.bpnb[j], ext);
-        if (rep_i) {
+        if (same) {
           S.repdead[i] = 1;
         } else {
           int p = -1;

@@ -589,6 +589,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   const int b = row_block * kWPC + wid;
   if (wid >= kWPC || b >= Ly.B) return;
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V, Lpad = Ly.Lpad;
+  const int space = Ly.space;  // word-boundary label, -1: none
   const float NEG = CTCPB_NEG;
 
   if (mode != 0) {
@@ -596,7 +597,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
               hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
               hd->page_size == Ly.page_size && hd->blank == Ly.blank && hd->list_len == Ly.L &&
-              hd->tile == Ly.tile;
+              hd->tile == Ly.tile && hd->space == Ly.space;
     if (!ok) {
       if (lane == 0) atomicOr(&st.hdr()->status, CTCPB_DEV_HEADER);
       return;
@@ -795,16 +796,19 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         if (live && len > 0) lpl = gathered ? rdlp(gcur) : rdlp(__ldg(row + last));
       }
       const float bpb = dadd(lpb, A);
-      const float stay = (live && len > 0 && !gap) ? dadd(lpl, pnbx) : NEG;
+      // (a space-ending beam has no stay path: every space frame is a token)
+      const float stay = (live && len > 0 && !gap && last != space) ? dadd(lpl, pnbx) : NEG;
       const int mil = mi < 0 ? 0 : mi;
       const float A_i = __shfl_sync(WFULL, A, mil);
       const float pb_i = __shfl_sync(WFULL, pbx, mil);
       const int last_i = __shfl_sync(WFULL, last, mil);
       const int len_i = __shfl_sync(WFULL, len, mil);
-      const bool rep_i = mi >= 0 && len_i > 0 && last_i == last;
+      const bool rep_i = mi >= 0 && len_i > 0 && last_i == last && last != space;
       // the extension of l_i folded into this blank slot (NEG when there is none)
       const float mterm = mi >= 0 ? dadd(lpl, rep_i ? pb_i : A_i) : NEG;
-      const float Rrep = (live && len > 0 && len < cap) ? dadd(lpl, pbx) : NEG;
+      // candidate (k, last): the repeat path (pb only); the word-boundary label
+      // extends from both paths
+      const float Rrep = (live && len > 0 && len < cap) ? dadd(lpl, last == space ? A : pbx) : NEG;
       const int n = nlive;
       // blank slot (3.4.1-3.4.3), branch-free so it overlaps the candidates below
       const bool anyfold = __any_sync(WFULL, mi >= 0);

@@ -34,7 +34,8 @@ class CtcpbError(RuntimeError):
 class _Cfg(ctypes.Structure):
     _fields_ = [("beam", ctypes.c_int32), ("nbest", ctypes.c_int32), ("blank_id", ctypes.c_int32),
                 ("max_seq_len", ctypes.c_int32), ("blank_threshold", ctypes.c_float),
-                ("paged", ctypes.c_int32), ("page_size", ctypes.c_int32), ("list_len", ctypes.c_int32)]
+                ("paged", ctypes.c_int32), ("page_size", ctypes.c_int32), ("list_len", ctypes.c_int32),
+                ("word_boundary", ctypes.c_int32), ("space_id", ctypes.c_int32)]
 
 
 @dataclasses.dataclass
@@ -48,11 +49,12 @@ class Config:
     paged: bool = False
     page_size: int = 16
     list_len: int = 0
+    space_id: int = -1  # word-boundary label (sections 3.4.1/3.4.2), -1: none
 
     def c(self) -> _Cfg:
         return _Cfg(self.beam, self.beam if self.nbest is None else self.nbest, self.blank_id,
                     self.max_seq_len, self.blank_threshold, int(bool(self.paged)), self.page_size,
-                    self.list_len)
+                    self.list_len, 1 if self.space_id >= 0 else 0, max(self.space_id, 0))
 
 
 def lib_path() -> str:

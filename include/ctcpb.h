@@ -74,6 +74,13 @@ typedef struct CUstream_st* ctcpb_stream_t;
  *                    selects min(2*beam+2, V-1) (section 3.4.7).  Any value in
  *                    1..V-1 gives the same decode: when a frame's list cannot
  *                    prove the selection, that step re-ranks the whole frame.
+ *   word_boundary    0: no word-boundary label (a zero-initialised config);
+ *                    1: space_id is the model's word-boundary ("space") label
+ *                    (sections 3.4.1/3.4.2): its extension always takes
+ *                    lp[space] + lse(pb, pnb), so every space frame is a token
+ *                    of its own, and a space-ending beam has no stay path.
+ *   space_id         the word-boundary label, 0..V-1 (no effect when it equals
+ *                    blank_id); ignored when word_boundary is 0.
  */
 typedef struct ctcpb_config {
   int32_t beam;
@@ -84,6 +91,8 @@ typedef struct ctcpb_config {
   int32_t paged;
   int32_t page_size;
   int32_t list_len;
+  int32_t word_boundary;
+  int32_t space_id;
 } ctcpb_config;
 
 /*

@@ -38,7 +38,7 @@ def oracle_offline(cfg, lp, lens, out_len=None, rows=None):
         lp = lp[rows]
         lens = None if lens is None else lens[rows]
     return O.decode(lp, lens, beam=cfg.beam, nbest=nb, blank=cfg.blank_id, cap=cap,
-                    thr=cfg.blank_threshold, out_len=out_len)
+                    thr=cfg.blank_threshold, out_len=out_len, space=cfg.space_id)
 
 
 def assert_same(g, o, what="", exact_scores=True):

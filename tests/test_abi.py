@@ -46,11 +46,26 @@ def cfg(**kw):
 
 @pytest.mark.parametrize("bad", [dict(beam=0), dict(beam=129), dict(nbest=11), dict(nbest=0),
                                  dict(blank_id=-1), dict(blank_id=5000), dict(paged=True, page_size=0),
-                                 dict(list_len=-1), dict(blank_threshold=float("nan"))])
+                                 dict(list_len=-1), dict(blank_threshold=float("nan")),
+                                 dict(space_id=5000)])
 def test_size_query_rejects_bad_config(lib, bad):
     with pytest.raises(D.CtcpbError) as e:
         D.workspace_size(cfg(**bad), 4, 10, 5000)
     assert e.value.code == D.EINVAL
+
+
+def test_word_boundary_fields(lib):
+    # a zero-initialised config has no word-boundary label; word_boundary must be 0 or 1
+    c = cfg().c()
+    c.word_boundary, c.space_id = 0, 9999  # ignored while word_boundary is 0
+    n = ctypes.c_size_t()
+    assert lib.ctcpb_workspace_size(ctypes.byref(c), 2, 10, 50, ctypes.byref(n)) == D.OK
+    c.word_boundary = 2
+    assert lib.ctcpb_workspace_size(ctypes.byref(c), 2, 10, 50, ctypes.byref(n)) == D.EINVAL
+    c.word_boundary, c.space_id = 1, -1
+    assert lib.ctcpb_workspace_size(ctypes.byref(c), 2, 10, 50, ctypes.byref(n)) == D.EINVAL
+    c.space_id = 7
+    assert lib.ctcpb_workspace_size(ctypes.byref(c), 2, 10, 50, ctypes.byref(n)) == D.OK
 
 
 def test_size_queries(lib):
