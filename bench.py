@@ -343,7 +343,7 @@ def main():
     core = [("rank+steps", D.STAGE_RANK | D.STAGE_STEPS)] if fused else [("rank", D.STAGE_RANK),
                                                                           ("steps", D.STAGE_STEPS)]
     stages = [("init", D.STAGE_INIT), ("select", D.STAGE_SELECT)] + core + [("output", D.STAGE_OUTPUT)]
-    warp_path = w.beam <= 32 and not w.paged and 32 + 8 * ((L + 3) // 4 * 4) <= 576
+    warp_path = w.beam <= 16 and not w.paged and 32 + 8 * ((L + 3) // 4 * 4) <= 576
     kernel_of = {"init": "k_init", "select": "k_select", "rank": "k_rank_tma" if V % 4 == 0 and L + 1 <= 64 else "k_prepass",
                  "steps": "k_step_warp" if warp_path else "k_step", "rank+steps": "k_fused", "output": "k_output"}
     per_stage = {n: [] for n, _ in stages}

@@ -20,6 +20,7 @@ constexpr int kMaxBeam = 128;                 // section 11: beam 1..128
 constexpr int kMaxList = 2 * kMaxBeam + 2;    // section 3.4.6: K_all <= 2*beam+2
 constexpr int kMaxV = 1 << 20;                // labels fit the 20-bit token field of a rank key
 constexpr int kStreamTile = 64;               // frames ranked per pre-pass tile when streaming
+constexpr int kBlockRing = 64;                // block step kernel: steps between token-store writes
 constexpr int kStreamDefaultCap = 4096;       // section 11: STREAMING_MAX_SEQ_LEN
 constexpr u32 kMagic = 0x42504354u;           // "TCPB"
 constexpr u32 kVersion = 1u;
@@ -86,7 +87,11 @@ inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_s
   o.blank = blank; o.L = L; o.Lpad = (int)align_up((size_t)L, 4); o.tile = tile; o.T_sel = T_sel;
   o.ldseq = (int)align_up((size_t)cap, 16);
   o.max_lp = paged ? (cap + page_size - 1) / page_size : 0;
-  o.ppr = paged ? beam * (o.max_lp + 1) : 0;
+  // a row's pages at a token-store write: the tables written at the previous
+  // write (<= max_lp pages a slot) and each slot's pages for the labels it
+  // gained since, at most kBlockRing of them (one partial page copied)
+  const int gain_pages = (kBlockRing + page_size - 1) / page_size + 1;
+  o.ppr = paged ? beam * (o.max_lp + (gain_pages < o.max_lp ? gain_pages : o.max_lp)) : 0;
   o.rec_bytes = align_up(32 + 8 * (size_t)o.Lpad, 32);
   const size_t A = 256;
   size_t off = sizeof(Header);

@@ -20,6 +20,21 @@ namespace ctcpb {
 
 #define FULL 0xffffffffu
 
+// Optional per-phase cycle accounting of the block step kernel (build with
+// -DCTCPB_PHASE_PROF): thread 0's clock between marks, summed over rows.
+#ifdef CTCPB_PHASE_PROF
+#define BPHASE(i)                     \
+  do {                                \
+    const long long now_ = clock64(); \
+    prof[i] += (u64)(now_ - prof_t0); \
+    prof_t0 = now_;                   \
+  } while (0)
+#else
+#define BPHASE(i) \
+  do {            \
+  } while (0)
+#endif
+
 // ------------------------------------------------------------------ helpers
 
 template <int NT>
@@ -214,7 +229,17 @@ struct StepSmem {
   u64 hkey[2 * NT];   // the extension winners' prefix hashes (open addressing) ...
   int hval[2 * NT];   // ... and their slots (-1: empty)
   int npg[2][NT];     // paged: pages held by slot w of each parity's block table
-  int cnt, front_id, nw, npairs, nxu, nkeys, ndfree;
+  // the step history since the token store was last written (ring row r =
+  // step win0 + r, entry w = source slot << 24 | token of winner w), and per
+  // slot the stored slot it descends from and how many of its labels that
+  // slot holds
+  static constexpr int R = kBlockRing;
+  u32 hist[R][NT];
+  int org[NT], lo[NT], norg[NT], nlo[NT];
+  int uc[8 * NT];      // frame scan: unlisted labels that can reach the threshold ...
+  float uv[8 * NT];    // ... and their log-probs
+  u64 tau;  // the step's selection threshold
+  int cnt, front_id, nw, npairs, nxu, nkeys, ndfree, nuc;
   int ptop, pnext;  // the row's page pool: LIFO top and bump pointer (paged)
   float lpb, front_lp;
 };
@@ -264,8 +289,156 @@ __device__ __forceinline__ void page_push(const View& st, int b, int phys, int* 
     set_status(st, CTCPB_DEV_OVERFLOW);
 }
 
+// Flat rows: write every next slot w < nw into the rows of parity par ^ 1 --
+// its origin row's first nlo[w] labels (parity par) followed by the labels it
+// gained in ring rows 0..nrows-1, found by walking its sources backwards --
+// then make each slot its own origin.  Ends with a group barrier.
 template <int NT>
-__global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ lp, long long sb, long long stt,
+__device__ void flush_flat(StepSmem<NT>& S, const View& st, int b, int par, int nrows, int nw, int blank, int tid) {
+  const int to = par ^ 1;
+  const int lw = st.lay.ldseq >> 2;  // 16-byte words per row
+  // whole words of the origin prefixes, four independent copies in flight
+  for (int i0 = 0; i0 < nw * lw; i0 += 4 * NT) {
+    int4 v[4];
+    int dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * NT + tid;
+      dst[u] = -1;
+      if (i < nw * lw) {
+        const int w = i / lw, x = i - w * lw;
+        const int o = S.norg[w];
+        if (o >= 0 && 4 * x + 4 <= S.nlo[w]) {
+          v[u] = reinterpret_cast<const int4*>(st.clist(par, b, o))[x];
+          dst[u] = i;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (dst[u] >= 0) {
+        const int w = dst[u] / lw, x = dst[u] - w * lw;
+        reinterpret_cast<int4*>(st.clist(to, b, w))[x] = v[u];
+      }
+  }
+  // the prefix tail after the last whole word, then the gained labels
+  for (int w = tid; w < nw; w += NT) {
+    const int o = S.norg[w], l0 = S.nlo[w];
+    int* row = st.clist(to, b, w);
+    if (o >= 0) {
+      const int* from = st.clist(par, b, o);
+      for (int x = l0 & ~3; x < l0; ++x) row[x] = from[x];
+    }
+    int slot = w, rem = S.nlen[w] - l0;
+    for (int r = nrows - 1; r >= 0 && rem > 0; --r) {
+      const u32 e = S.hist[r][slot];
+      const int tk = (int)(e & 0xffffffu);
+      if (tk != blank) row[l0 + --rem] = tk;
+      slot = (int)(e >> 24);
+    }
+    S.norg[w] = w;
+    S.nlo[w] = S.nlen[w];
+  }
+  gsync<NT>();
+}
+
+// Paged storage: the same write into the block tables of parity par ^ 1.
+// Slot w's table takes its origin's pages (parity par; reference counts change
+// only for entries that differ from what the slot held), then the labels it
+// gained go to a copy of the origin's partial last page (the origin's table
+// still holds the original) and to new pages.  Ends with a group barrier.
+template <int NT>
+__device__ void flush_paged(StepSmem<NT>& S, const View& st, int b, int par, int nrows, int nw, int blank, int tid) {
+  const int to = par ^ 1, ps = st.lay.page_size, beam = st.lay.beam;
+  int* refc = st.refc(b);
+  // pass A: acquire (a thread per slot)
+  for (int w = tid; w < nw; w += NT) {
+    const int o = S.norg[w];
+    const int nn = o >= 0 ? (S.nlo[w] + ps - 1) / ps : 0, no = S.npg[to][w];
+    const int* bs = st.btab(par, b, o >= 0 ? o : 0);
+    const int* bd = st.btab(to, b, w);
+#pragma unroll 4
+    for (int x = 0; x < nn; ++x) {
+      const int nv = bs[x], ov = x < no ? bd[x] : -1;
+      if (nv >= 0 && nv != ov) atomicAdd(&refc[nv], 1);
+    }
+  }
+  if (tid == 0) S.ndfree = 0;
+  gsync<NT>();
+  // pass B: release what changed, install the origin's pages
+  for (int w = tid; w < beam; w += NT) {
+    const int o = w < nw ? S.norg[w] : -1;
+    const int nn = o >= 0 ? (S.nlo[w] + ps - 1) / ps : 0, no = S.npg[to][w];
+    const int* bs = st.btab(par, b, o >= 0 ? o : 0);
+    int* bd = st.btab(to, b, w);
+    const int m = nn > no ? nn : no;
+#pragma unroll 4
+    for (int x = 0; x < m; ++x) {
+      const int nv = x < nn ? bs[x] : -1, ov = x < no ? bd[x] : -1;
+      if (ov >= 0 && ov != nv && atomicSub(&refc[ov], 1) == 1) page_push(st, b, ov, &S.ptop);
+      bd[x] = nv;
+    }
+    S.npg[to][w] = nn;
+  }
+  gsync<NT>();
+  // pass C: pages for the gained labels, then the labels (ring walk)
+  for (int w = tid; w < nw; w += NT) {
+    const int l0 = S.nlo[w], l1 = S.nlen[w];
+    if (l1 > l0) {
+      int* bd = st.btab(to, b, w);
+      const int x0 = l0 / ps, off = l0 - x0 * ps;
+      bool ok = true;  // false: a shared page could not be copied; nothing is written into it
+      if (off != 0) {
+        const int phys = bd[x0];
+        if (phys >= 0) {
+          const int nph = page_alloc(st, b, &S.ptop, &S.pnext);
+          if (nph >= 0) {
+            const int* from = st.page(b, phys);
+            int* top = st.page(b, nph);
+            for (int y = 0; y < off; ++y) top[y] = from[y];
+            refc[nph] = 1;
+            bd[x0] = nph;
+            if (atomicSub(&refc[phys], 1) == 1) S.dfree[atomicAdd(&S.ndfree, 1)] = phys;
+          } else {
+            ok = false;
+          }
+        }
+      }
+      int xe = (l1 - 1) / ps;  // the table ends at the first page that could not be had
+      for (int y = off != 0 ? x0 + 1 : x0; y <= xe; ++y) {
+        const int phys = page_alloc(st, b, &S.ptop, &S.pnext);
+        if (phys < 0) {
+          xe = y - 1;
+          break;
+        }
+        refc[phys] = 1;
+        bd[y] = phys;
+      }
+      S.npg[to][w] = xe + 1;
+      int slot = w, rem = l1 - l0;
+      for (int r = nrows - 1; r >= 0 && rem > 0; --r) {
+        const u32 e = S.hist[r][slot];
+        const int tk = (int)(e & 0xffffffu);
+        if (tk != blank) {
+          const int pos = l0 + --rem, y = pos / ps;
+          const int phys = bd[y];
+          if (phys >= 0 && (ok || y != x0)) st.page(b, phys)[pos - y * ps] = tk;
+        }
+        slot = (int)(e >> 24);
+      }
+    }
+    S.norg[w] = w;
+    S.nlo[w] = l1;
+  }
+  gsync<NT>();
+  if (tid == 0 && S.ptop < 0) S.ptop = 0;  // allocations past an empty pool
+  gsync<NT>();
+  for (int q = tid; q < S.ndfree; q += NT) page_push(st, b, S.dfree[q], &S.ptop);
+  gsync<NT>();
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict__ lp, long long sb, long long stt,
                                              int mode, const int* __restrict__ nframes, int chunk_T,
                                              int tile_start, int tile_len, int sortcap) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -316,7 +489,10 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
     S.h[k] = st.h()[rb + k];
     S.hp[k] = st.hp()[rb + k];
     S.msrc[k] = st.msrc()[rb + k];
+    S.org[k] = k;
+    S.lo[k] = S.len[k];
   }
+  int win0 = 0;  // flat rows: the call step of ring row 0
   if (Ly.paged) {
     for (int k = tid; k < 2 * beam; k += NT) {
       const int pp = k / beam, w = k - pp * beam;
@@ -328,6 +504,13 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
   }
   TokenStore tok{st, b};
   const int M = sortcap - NT;  // candidates per selection chunk
+  // decode steps, unlisted-label scans, overflow (chunked) selections,
+  // hash-proposed merges confirmed
+  u32 c_steps = 0, c_scan = 0, c_exh = 0, c_hash = 0;
+#ifdef CTCPB_PHASE_PROF
+  u64 prof[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  long long prof_t0 = clock64();
+#endif
   if (Ly.paged && tid == 0) {
     S.ptop = st.ptop()[b];
     S.pnext = st.pnext()[b];
@@ -356,9 +539,9 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       }
     }
     gsync<NT>();
+    BPHASE(0);
     const bool gap = t > t_prev + 1;
     const int cnt = S.cnt;
-    const int np = par ^ 1;
 
     if (step == 0) {
       // ---- section 3.3: seed the top (beam-1) labels, then the empty prefix
@@ -395,24 +578,11 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       if (tid == 0) S.nw = ntok + (empty_live ? 1 : 0);
       gsync<NT>();
       const int nw = S.nw;
-      if (!Ly.paged) {
-        for (int k = tid; k < ntok; k += NT) st.clist(np, b, k)[0] = S.ids[k];
-      } else {
-        for (int k = tid; k < nw; k += NT) {
-          int* bt = st.btab(np, b, k);
-          if (k < ntok) {
-            int phys = page_alloc(st, b, &S.ptop, &S.pnext);
-            if (phys >= 0) {
-              st.refc(b)[phys] = 1;
-              st.page(b, phys)[0] = S.ids[k];
-            }
-            bt[0] = phys;
-          }
-          S.npg[np][k] = k < ntok ? 1 : 0;
-        }
+      for (int k = tid; k < nw; k += NT) {
+        S.hist[s - win0][k] = (u32)S.ntok[k] & 0xffffffu;
+        S.norg[k] = -1;
+        S.nlo[k] = 0;
       }
-      gsync<NT>();
-      if (Ly.paged && tid == 0 && S.ptop < 0) S.ptop = 0;
       gsync<NT>();
     } else {
       // ---- section 3.4: collapsed-blank correction, extension and blank slots
@@ -477,6 +647,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         }
       }
       gsync<NT>();
+      BPHASE(1);
 
       // ---- sections 3.4.4-3.4.6: best `beam` candidates over
       // {blank slot, repeat slot, listed labels} of every live hypothesis.
@@ -520,12 +691,27 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         u64 m1 = kb > kr ? kb : kr, m2 = kb > kr ? kr : kb;
         if (ka > m1) { m2 = m1; m1 = ka; } else if (ka > m2) { m2 = ka; }
         if (kc > m1) { m2 = m1; m1 = kc; } else if (kc > m2) { m2 = kc; }
-        S.top2[tid] = m1;
-        S.top2[NT + tid] = m2;
-        if (tid == 0) S.nkeys = 0;
+        S.top2[2 * tid] = m1;
+        S.top2[2 * tid + 1] = m2;
+        if (tid == 0) {
+          S.nkeys = 0;
+          S.tau = 0ull;  // every live key when fewer than beam are live
+        }
         gsync<NT>();
-        bitonic_desc<NT>(S.top2, 2 * NT, tid);
-        const u64 tau = S.top2[beam - 1];  // 0 (every live key) when fewer than beam are live
+        // tau: the key that exactly beam-1 of the 2 nlive keys exceed (live
+        // keys are distinct: score, source, token)
+        if (tid < nlive) {
+          int r1 = 0, r2 = 0;
+          for (int j = 0; j < 2 * nlive; ++j) {
+            const u64 y = S.top2[j];
+            r1 += y > m1 ? 1 : 0;
+            r2 += y > m2 ? 1 : 0;
+          }
+          if (m1 != 0ull && r1 == beam - 1) S.tau = m1;
+          if (m2 != 0ull && r2 == beam - 1) S.tau = m2;
+        }
+        gsync<NT>();
+        const u64 tau = S.tau;
         // every candidate >= tau (the listed ones stop at the first below tau)
         const int cap_keys = sortcap;
         if (tid < nlive) {
@@ -544,7 +730,29 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         }
         gsync<NT>();
         const int nk = S.nkeys;
-        if (nk <= cap_keys) {
+        if (nk <= 4 * NT) {
+          // the best beam in order by rank: each key counts the keys above it
+          u64 mk[4];
+          int mr[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = tid + u * NT;
+            mk[u] = i < nk ? keys[i] : 0ull;
+            mr[u] = 0;
+          }
+          for (int j = 0; j < nk; ++j) {
+            const u64 y = keys[j];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mr[u] += y > mk[u] ? 1 : 0;
+          }
+          gsync<NT>();
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (mk[u] != 0ull && mr[u] < beam) keys[mr[u]] = mk[u];
+          // the rest of the first NT slots holds no key (a frame scan sorts them)
+          for (int i = (nk < beam ? nk : beam) + tid; i < NT; i += NT) keys[i] = 0ull;
+          selected = true;
+        } else if (nk <= cap_keys) {
           const int P = pow2_at_least(nk > beam ? nk : beam, 2 * NT);
           for (int i = nk + tid; i < P; i += NT) keys[i] = 0ull;
           gsync<NT>();
@@ -555,6 +763,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         if (tid == 0) S.nkeys = 0;
         gsync<NT>();
       }
+      c_exh += selected ? 0u : 1u;
       const int stride = cnt + 2;
       const int NC = selected ? 0 : nlive * stride;  // the chunked sort of every candidate (overflow only)
       if (!selected)
@@ -588,6 +797,7 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       }
       int nw = 0;
       for (int w = 0; w < beam; ++w) nw += keys[w] != 0ull;
+      BPHASE(2);
 
       // ---- the list proves the selection unless an unlisted label could
       // reach the beam: then rank every unlisted label of this frame
@@ -602,47 +812,92 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         }
         const bool need = g_any<NT>(bad);
         if (need) {
-          const u64 thr = nw == beam ? (keys[beam - 1] & 0xffffffff00000000ull) : 0ull;
+          ++c_scan;
+          // One pass over the frame: an unlisted label is worth scoring only
+          // if it reaches the threshold with the largest A of a hypothesis
+          // that can grow (adding is monotone), so only those labels are
+          // kept and then paired with every hypothesis.
+          u64 thr = nw == beam ? (keys[beam - 1] & 0xffffffff00000000ull) : 0ull;
           const u64 kfront = lab_key(S.front_lp, S.front_id);
-          const long long items = (long long)nlive * V;
-          for (long long base = 0; base < items; base += NT) {
-            const long long x = base + tid;
-            if (x < items) {
-              const int k = (int)(x / V), c = (int)(x - (long long)k * V);
-              const int L = S.len[k];
-              if (c != blank && L < cap && !(L > 0 && c == S.last[k])) {
-                const float v = rdlp(row[c]);
-                if (v > NEG && lab_key(v, c) <= kfront) {
-                  bool ex = false;
-                  for (int u = 0; u < S.nxu; ++u) ex |= (S.xu_k[u] == k && S.xu_c[u] == c);
-                  const float sc = dadd(v, S.A[k]);
-                  if (!ex && sc > NEG) {
-                    const u64 key = cand_key(sc, k, c);
-                    if (key >= thr) {
-                      int pos = atomicAdd(&S.nkeys, 1);
-                      keys[NT + pos] = key;
-                    }
-                  }
-                }
+          float amax = NEG;
+          for (int k = 0; k < nlive; ++k)
+            if (S.len[k] < cap) amax = fmaxf(amax, S.A[k]);
+          if (tid == 0) S.nuc = 0;
+          gsync<NT>();
+          for (int c0 = 0; c0 < V; c0 += 4 * NT) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = c0 + u * NT + tid;
+              v[u] = c < V ? rdlp(row[c]) : NEG;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = c0 + u * NT + tid;
+              if (c < V && c != blank && v[u] > NEG && lab_key(v[u], c) <= kfront &&
+                  ((u64)fkey(dadd(v[u], amax)) << 32) >= thr) {
+                const int q = atomicAdd(&S.nuc, 1);  // < 8 NT: flushed above 4 NT
+                S.uc[q] = c;
+                S.uv[q] = v[u];
               }
             }
             gsync<NT>();
-            const int nk = S.nkeys;
-            gsync<NT>();  // every thread has read nk before the next round adds to it
-            if (nk > M - NT || base + NT >= items) {
-              const int P = pow2_at_least(NT + nk, 2 * NT);
-              for (int i = NT + nk + tid; i < P; i += NT) keys[i] = 0ull;
-              gsync<NT>();
-              if (nk > 0) bitonic_desc<NT>(keys, P, tid);
-              if (tid == 0) S.nkeys = 0;
+            const int nl = S.nuc;
+            const bool last_round = c0 + 4 * NT >= V;
+            if (nl > 4 * NT || (last_round && nl > 0)) {
+              // pair the kept labels with every hypothesis, NT pairs a round
+              const int items = nlive * nl;
+              for (int base = 0; base < items; base += NT) {
+                const int x = base + tid;
+                if (x < items) {
+                  const int k = x / nl, j = x - k * nl;
+                  const int c = S.uc[j], L = S.len[k];
+                  if (L < cap && !(L > 0 && c == S.last[k])) {
+                    bool ex = false;
+                    for (int u = 0; u < S.nxu; ++u) ex |= (S.xu_k[u] == k && S.xu_c[u] == c);
+                    const float sc = dadd(S.uv[j], S.A[k]);
+                    if (!ex && sc > NEG) {
+                      const u64 key = cand_key(sc, k, c);
+                      if (key >= thr) keys[NT + atomicAdd(&S.nkeys, 1)] = key;
+                    }
+                  }
+                }
+                gsync<NT>();
+                const int nk = S.nkeys;
+                gsync<NT>();  // every thread has read nk before the next round adds to it
+                if (nk > M - NT) {
+                  const int P = pow2_at_least(NT + nk, 2 * NT);
+                  for (int i = NT + nk + tid; i < P; i += NT) keys[i] = 0ull;
+                  gsync<NT>();
+                  bitonic_desc<NT>(keys, P, tid);
+                  if (tid == 0) S.nkeys = 0;
+                  gsync<NT>();
+                  if (keys[beam - 1] != 0ull) {
+                    const u64 kb = keys[beam - 1] & 0xffffffff00000000ull;
+                    thr = kb > thr ? kb : thr;
+                  }
+                }
+              }
+              if (tid == 0) S.nuc = 0;
               gsync<NT>();
             }
           }
+          const int nk = S.nkeys;
+          if (nk > 0) {
+            const int P = pow2_at_least(NT + nk, 2 * NT);
+            for (int i = NT + nk + tid; i < P; i += NT) keys[i] = 0ull;
+            gsync<NT>();
+            bitonic_desc<NT>(keys, P, tid);
+          }
+          gsync<NT>();
+          if (tid == 0) S.nkeys = 0;
+          gsync<NT>();
           nw = 0;
           for (int w = 0; w < beam; ++w) nw += keys[w] != 0ull;
         }
       }
 
+      BPHASE(3);
       // ---- section 3.4.5: the winners become the next hypotheses
       for (int w = tid; w < nw; w += NT) {
         const u64 key = keys[w];
@@ -702,103 +957,24 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       }
       if (tid == 0) S.npairs = 0;
       gsync<NT>();
+      BPHASE(4);
 
-      // ---- token store
-      if (!Ly.paged) {
-        for (int w = 0; w < nw; ++w) {
-          const int src = S.nsrc[w];
-          const int Ls = S.len[src];
-          const int* from = st.clist(par, b, src);
-          int* to = st.clist(np, b, w);
-          for (int x = tid; x < Ls; x += NT) to[x] = from[x];
-        }
-        for (int w = tid; w < nw; w += NT)
-          if (S.ntok[w] != blank) st.clist(np, b, w)[S.len[S.nsrc[w]]] = S.ntok[w];
-        gsync<NT>();
-      } else {
-        const int ps = Ly.page_size, mlp = Ly.max_lp;
-        int* refc = st.refc(b);
-        // fork: slot w of parity np takes winner w's source table (parity par).
-        // Only the pages that differ from what the slot held change reference
-        // counts; every acquire comes before every release.
-        // pass A: acquire (a thread per winner)
-        for (int w = tid; w < nw; w += NT) {
-          const int src = S.nsrc[w];
-          const int nn = (S.len[src] + ps - 1) / ps, no = S.npg[np][w];
-          const int* bs = st.btab(par, b, src);
-          const int* bd = st.btab(np, b, w);
-#pragma unroll 4
-          for (int x = 0; x < nn; ++x) {
-            const int nv = bs[x], ov = x < no ? bd[x] : -1;
-            if (nv >= 0 && nv != ov) atomicAdd(&refc[nv], 1);
-          }
-        }
-        gsync<NT>();
-        // pass B: release what changed, install the source's pages
-        for (int w = tid; w < beam; w += NT) {
-          const int src = w < nw ? S.nsrc[w] : 0;
-          const int nn = w < nw ? (S.len[src] + ps - 1) / ps : 0, no = S.npg[np][w];
-          const int* bs = st.btab(par, b, src);
-          int* bd = st.btab(np, b, w);
-          const int m = nn > no ? nn : no;
-#pragma unroll 4
-          for (int x = 0; x < m; ++x) {
-            const int nv = x < nn ? bs[x] : -1, ov = x < no ? bd[x] : -1;
-            if (ov >= 0 && ov != nv && atomicSub(&refc[ov], 1) == 1) page_push(st, b, ov, &S.ptop);
-            bd[x] = nv;
-          }
-          S.npg[np][w] = nn;
-        }
-        gsync<NT>();
-        // append / copy-on-write; page releases here are deferred past the
-        // last allocation of the step
-        for (int w = tid; w < nw; w += NT) {
-          const int tk = S.ntok[w];
-          if (tk == blank) continue;
-          const int pos = S.len[S.nsrc[w]];
-          const int lpi = pos / ps, off = pos - lpi * ps;
-          int* bd = st.btab(np, b, w);
-          if (off == 0) {
-            const int phys = page_alloc(st, b, &S.ptop, &S.pnext);
-            if (phys >= 0) {
-              refc[phys] = 1;
-              st.page(b, phys)[0] = tk;
-            }
-            bd[lpi] = phys;
-            S.npg[np][w] = lpi + 1;
-          } else {
-            const int phys = bd[lpi];
-            if (phys < 0) continue;
-            if (atomicAdd(&refc[phys], 0) > 1) {
-              const int nph = page_alloc(st, b, &S.ptop, &S.pnext);
-              if (nph >= 0) {
-                const int* from = st.page(b, phys);
-                int* to = st.page(b, nph);
-                for (int x = 0; x < off; ++x) to[x] = from[x];
-                to[off] = tk;
-                refc[nph] = 1;
-                bd[lpi] = nph;
-                if (atomicSub(&refc[phys], 1) == 1) {
-                  int q = atomicAdd(&S.ndfree, 1);
-                  S.dfree[q] = phys;
-                }
-              }
-            } else {
-              st.page(b, phys)[off] = tk;
-            }
-          }
-        }
-        gsync<NT>();
-        if (tid == 0 && S.ptop < 0) S.ptop = 0;  // allocations past an empty pool
-        gsync<NT>();
-        for (int q = tid; q < S.ndfree; q += NT) page_push(st, b, S.dfree[q], &S.ptop);
-        gsync<NT>();
+      // ---- token store: the winners' (source, token) into the ring; the
+      // rows or pages are written at a flush
+      for (int w = tid; w < nw; w += NT) {
+        const int src = S.nsrc[w];
+        S.hist[s - win0][w] = ((u32)src << 24) | ((u32)S.ntok[w] & 0xffffffu);
+        S.norg[w] = S.org[src];
+        S.nlo[w] = S.lo[src];
       }
+      gsync<NT>();
     }
 
+    BPHASE(5);
     // ---- the one merge relation the sources cannot show: a blank winner whose
     // parent prefix was just rebuilt by an extension winner (prefix hash
     // proposal, confirmed on the stored tokens)
+    int npairs = 0;
     if (step > 0) {
       const int nw = S.nw;
       for (int j = tid; j < nw; j += NT) {
@@ -818,17 +994,33 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
         }
       }
       gsync<NT>();
-      const int npairs = S.npairs < 2 * NT ? S.npairs : 2 * NT;
+      npairs = S.npairs < 2 * NT ? S.npairs : 2 * NT;
+    }
+    // the token store is written when the ring is full, at the call's last
+    // step, and before tokens are compared
+    if (s - win0 + 1 == S.R || s + 1 == nsteps || npairs > 0) {
+      if (Ly.paged)
+        flush_paged<NT>(S, st, b, par, s - win0 + 1, S.nw, blank, tid);
+      else
+        flush_flat<NT>(S, st, b, par, s - win0 + 1, S.nw, blank, tid);
+      par ^= 1;
+      win0 = s + 1;
+    }
+    if (npairs > 0) {
+      const int tp = par;  // the parity holding the next slots' tokens
       for (int pq = 0; pq < npairs; ++pq) {
         const int i = S.pi[pq], j = S.pj[pq];
         const int Li = S.nlen[i];
         bool mism = false;
-        for (int x = tid; x < Li; x += NT) mism |= tok.get(np, i, x) != tok.get(np, j, x);
-        if (!g_any<NT>(mism) && tid == 0) S.nmsrc[j] = i;
+        for (int x = tid; x < Li; x += NT) mism |= tok.get(tp, i, x) != tok.get(tp, j, x);
+        const bool same = !g_any<NT>(mism);
+        c_hash += same ? 1u : 0u;
+        if (same && tid == 0) S.nmsrc[j] = i;
       }
       gsync<NT>();
     }
 
+    BPHASE(6);
     // ---- commit
     const int nw = S.nw;
     for (int k = tid; k < nw; k += NT) {
@@ -840,12 +1032,15 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
       S.h[k] = S.nh[k];
       S.hp[k] = S.nhp[k];
       S.msrc[k] = S.nmsrc[k];
+      S.org[k] = S.norg[k];
+      S.lo[k] = S.nlo[k];
     }
     gsync<NT>();
     nlive = nw;
-    par = np;
     t_prev = t;
     ++step;
+    ++c_steps;
+    BPHASE(7);
   }
 
   for (int k = tid; k < beam; k += NT) {
@@ -859,6 +1054,17 @@ __global__ void __launch_bounds__(NT) k_step(View st, const float* __restrict__ 
     st.msrc()[rb + k] = S.msrc[k];
   }
   if (tid == 0) {
+    Header* hd = st.hdr();
+    atomicAdd(&hd->counters[0], c_steps);
+    if (c_scan) {
+      atomicAdd(&hd->counters[1], c_scan);  // the list could not bound the unlisted labels
+      atomicAdd(&hd->counters[3], c_scan);
+    }
+    if (c_exh) atomicAdd(&hd->counters[2], c_exh);
+    if (c_hash) atomicAdd(&hd->counters[4], c_hash);
+#ifdef CTCPB_PHASE_PROF
+    for (int i = 0; i < 8; ++i) atomicAdd(&hd->phase_cycles[i], prof[i]);
+#endif
     if (Ly.paged) {
       st.ptop()[b] = S.ptop;
       st.pnext()[b] = S.pnext;
@@ -940,6 +1146,9 @@ cudaError_t launch_select(const View& st, const float* lp, long long sb, long lo
   k_select<<<st.lay.B, 256, 0, s>>>(st, lp, sb, stt, lens, T, mode, log_thr, sel, nsel);
   return cudaGetLastError();
 }
+
+static_assert(sizeof(StepSmem<128>) + 4096 * sizeof(u64) <= 227 * 1024, "block step kernel shared memory");
+static_assert(sizeof(StepSmem<32>) + 1024 * sizeof(u64) <= 227 * 1024, "block step kernel shared memory");
 
 template <int NT>
 static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, long long stt, int mode,

@@ -13,7 +13,7 @@
 //   3. every label >= tau is compacted (warp ballots) into shared memory;
 //   4. each compacted label's rank = how many compacted keys beat it; the
 //      first L go to the list, rank L is the front.
-// Rows that are not 16-byte aligned, lists longer than 63 labels, and
+// Rows that are not 16-byte aligned, lists longer than 511 labels, and
 // compactions past the buffer use the plain per-warp ranking (rank_row).
 #include "ctcpb_rank.cuh"
 #include "ctcpb_kernels.h"
@@ -93,16 +93,30 @@ namespace {
 template <class Items>
 __global__ void __launch_bounds__(512, 1) k_rank_tma(Items items, int V, int blank, int L, u32* status) {
   extern __shared__ __align__(128) unsigned char smem[];
-  rank_tma_body(items, V, blank, L, status, smem, blockIdx.x, gridDim.x, blockDim.x >> 5);
+  rank_tma_body_e<Items, 2>(items, V, blank, L, status, smem, blockIdx.x, gridDim.x, blockDim.x >> 5);
+}
+
+// Lists of 64..255 labels: a larger threshold pool (E maxima per lane) and up
+// to 8 warps a block, so the registers are not capped at 128.
+template <class Items, int E>
+__global__ void __launch_bounds__(256, 1) k_rank_tma_big(Items items, int V, int blank, int L, u32* status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  rank_tma_body_e<Items, E>(items, V, blank, L, status, smem, blockIdx.x, gridDim.x, blockDim.x >> 5);
 }
 
 
 template <class Items>
 cudaError_t launch_rank_tma(const Items& items, long long nitems, int V, int blank, int L, u32* status,
                             cudaStream_t s) {
-  const int wpb = rank_tma_warps(V);
+  const int E = L + 1 <= 64 ? 2 : (L + 1 <= 128 ? 4 : (L + 1 <= 256 ? 8 : 16));
+  int wpb = rank_tma_warps(V);
+  if (E > 2 && wpb > 8) wpb = 8;
   const size_t smem = rank_tma_per_warp(V) * wpb;
-  cudaError_t e = cudaFuncSetAttribute(k_rank_tma<Items>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const void* fn = E == 2    ? (const void*)k_rank_tma<Items>
+                  : E == 4  ? (const void*)k_rank_tma_big<Items, 4>
+                  : E == 8  ? (const void*)k_rank_tma_big<Items, 8>
+                            : (const void*)k_rank_tma_big<Items, 16>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -110,17 +124,24 @@ cudaError_t launch_rank_tma(const Items& items, long long nitems, int V, int bla
   long long blocks = (nitems + wpb - 1) / wpb;
   if (blocks > sms) blocks = sms;
   if (blocks < 1) blocks = 1;
-  k_rank_tma<Items><<<(int)blocks, 32 * wpb, smem, s>>>(items, V, blank, L, status);
+  if (E == 2)
+    k_rank_tma<Items><<<(int)blocks, 32 * wpb, smem, s>>>(items, V, blank, L, status);
+  else if (E == 4)
+    k_rank_tma_big<Items, 4><<<(int)blocks, 32 * wpb, smem, s>>>(items, V, blank, L, status);
+  else if (E == 8)
+    k_rank_tma_big<Items, 8><<<(int)blocks, 32 * wpb, smem, s>>>(items, V, blank, L, status);
+  else
+    k_rank_tma_big<Items, 16><<<(int)blocks, 32 * wpb, smem, s>>>(items, V, blank, L, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // The staged path needs 16-byte aligned rows of a multiple of 4 labels, one of
-// which fits a warp's share of shared memory, and lists of at most 63 labels.
+// which fits a warp's share of shared memory, and lists of at most 511 labels.
 bool rank_tma_ok(const float* lp, long long s1, long long s2, int V, int L) {
   return ((uintptr_t)lp & 15u) == 0 && (s1 & 3) == 0 && (s2 & 3) == 0 && (V & 3) == 0 && V >= 4 &&
-         L + 1 <= 64 && rank_tma_warps(V) >= 1;
+         L + 1 <= 512 && rank_tma_warps(V) >= 1;
 }
 
 cudaError_t launch_prepass_tma(const View& st, const float* lp, long long sb, long long stt, int mode,

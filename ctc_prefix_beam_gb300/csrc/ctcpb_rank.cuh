@@ -230,26 +230,68 @@ struct RowItems {
 // be in the top L+1 into `cand`; returns their count, or -1 when they
 // overflow the buffer.  `row`: 16-byte aligned shared memory, V % 4 == 0, the
 // blank already replaced by -inf.
+// Passes 1-2: tau = the K-th largest of a pool of 32*E label maxima, one per
+// disjoint label subset (E = 2: the x,y and z,w halves of each lane's float4
+// slices; 4: each component; 8: each component of the even and of the odd
+// rounds; 16: each component of rounds 0, 1, 2, 3 mod 4), so at least K
+// labels score >= tau and the top K all do.  K <= 32*E.
+template <int E>
+__device__ __forceinline__ float pool_tau(const float4* __restrict__ r4, int V4, int K, int lane) {
+  float m[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) m[e] = -INFINITY;
+  if (E == 16) {
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int q = lane; q < V4; q += 128) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 x = q + 32 * u < V4 ? r4[q + 32 * u] : ninf;
+        m[4 * u] = fmaxf(m[4 * u], x.x);
+        m[4 * u + 1] = fmaxf(m[4 * u + 1], x.y);
+        m[4 * u + 2] = fmaxf(m[4 * u + 2], x.z);
+        m[4 * u + 3] = fmaxf(m[4 * u + 3], x.w);
+      }
+    }
+  } else if (E == 8) {
+#pragma unroll 2
+    for (int q = lane; q < V4; q += 64) {
+      const float4 x = r4[q];
+      const float4 y = q + 32 < V4 ? r4[q + 32] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      m[0] = fmaxf(m[0], x.x); m[1] = fmaxf(m[1], x.y); m[2] = fmaxf(m[2], x.z); m[3] = fmaxf(m[3], x.w);
+      m[4] = fmaxf(m[4], y.x); m[5] = fmaxf(m[5], y.y); m[6] = fmaxf(m[6], y.z); m[7] = fmaxf(m[7], y.w);
+    }
+  } else {
+#pragma unroll 4
+    for (int q = lane; q < V4; q += 32) {
+      const float4 x = r4[q];
+      m[0] = fmaxf(m[0], x.x); m[1] = fmaxf(m[1], x.y); m[2] = fmaxf(m[2], x.z); m[3] = fmaxf(m[3], x.w);
+    }
+    if (E == 2) {
+      m[0] = fmaxf(m[0], m[1]);
+      m[1] = fmaxf(m[2], m[3]);
+    }
+  }
+  u32 pool[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const float v = m[e] + 0.0f;
+    pool[e] = v > CTCPB_NEG ? fkey(v) : 0u;
+  }
+  warp_sort_desc<E>(pool, lane);
+  u32 pk = pool[0];
+#pragma unroll
+  for (int e = 1; e < E; ++e)
+    if (((K - 1) >> 5) == e) pk = pool[e];
+  const u32 kth = __shfl_sync(RFULL, pk, (K - 1) & 31);
+  return kth != 0u ? fkey_inv(kth) : -FLT_MAX;
+}
+
+template <int E>
 __device__ int rank_gather(const float* __restrict__ row, int V, int L, u64* cand, int lane) {
   const int K = L + 1;
   const float4* r4 = reinterpret_cast<const float4*>(row);
   const int V4 = V >> 2;
-  // 1. maxima of the x,y and z,w halves of this lane's labels (four chains)
-  float mx = -INFINITY, my = -INFINITY, mz = -INFINITY, mw = -INFINITY;
-#pragma unroll 4
-  for (int q = lane; q < V4; q += 32) {
-    const float4 x = r4[q];
-    mx = fmaxf(mx, x.x);
-    my = fmaxf(my, x.y);
-    mz = fmaxf(mz, x.z);
-    mw = fmaxf(mw, x.w);
-  }
-  const float hA = fmaxf(mx, my) + 0.0f, hB = fmaxf(mz, mw) + 0.0f;
-  // 2. tau: the K-th largest of these 64 values
-  u32 pool[2] = {hA > CTCPB_NEG ? fkey(hA) : 0u, hB > CTCPB_NEG ? fkey(hB) : 0u};
-  warp_sort_desc<2>(pool, lane);
-  const u32 kth = __shfl_sync(RFULL, K > 32 ? pool[1] : pool[0], (K - 1) & 31);
-  const float tauf = kth != 0u ? fkey_inv(kth) : -FLT_MAX;
+  const float tauf = pool_tau<E>(r4, V4, K, lane);
   // 3. every live label >= tau, four float4 per lane per round, compacted by
   // an exclusive scan of the lanes' hit counts
   int n = 0;
@@ -308,6 +350,7 @@ __device__ __forceinline__ void put_ranked(u64 key, int r, int L, const RankDst&
 }
 
 // Pass 4 (all lanes): rank the n compacted labels and write the row's list.
+template <int E>
 __device__ void rank_finish(const u64* cand, int n, int L, float lpb, int lane, const RankDst& d) {
   const int cnt = n < L ? n : L;
   if (n <= 64) {
@@ -322,6 +365,20 @@ __device__ void rank_finish(const u64* cand, int n, int L, float lpb, int lane, 
     warp_sort_desc<4>(v, lane);
 #pragma unroll
     for (int e = 0; e < 4; ++e) put_ranked(v[e], lane + 32 * e, L, d);
+  } else if (E >= 8 && n <= 256) {
+    u64 v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = lane + 32 * e < n ? cand[lane + 32 * e] : 0ull;
+    warp_sort_desc<8>(v, lane);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) put_ranked(v[e], lane + 32 * e, L, d);
+  } else if (E >= 16 && n <= 512) {
+    u64 v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = lane + 32 * e < n ? cand[lane + 32 * e] : 0ull;
+    warp_sort_desc<16>(v, lane);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) put_ranked(v[e], lane + 32 * e, L, d);
   } else {
     for (int e = lane; e < n; e += 32) {
       const u64 me = cand[e];
@@ -359,9 +416,9 @@ __host__ __device__ inline size_t rank_tma_per_warp(int V) {
 // (vblock, nvblocks) is this block's place among the blocks that rank.  The
 // next row's bulk copy is issued as soon as the current row's passes have read
 // the buffer, so it overlaps pass 4.
-template <class Items>
-__device__ __forceinline__ void rank_tma_body(const Items& items, int V, int blank, int L, u32* status,
-                                              unsigned char* smem, int vblock, int nvblocks, int nwb) {
+template <class Items, int E>
+__device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int blank, int L, u32* status,
+                                                unsigned char* smem, int vblock, int nvblocks, int nwb) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (wid >= nwb) return;
   const size_t per_warp = align_up((size_t)V * 4, 128) + (size_t)kCandCap * 8 + 16;
@@ -425,7 +482,7 @@ __device__ __forceinline__ void rank_tma_body(const Items& items, int V, int bla
     __syncwarp();
     if (lane == 0) buf[blank] = -INFINITY;  // the blank is not a label of the list
     __syncwarp();
-    const int n = rank_gather(buf, V, L, cand, lane);
+    const int n = rank_gather<E>(buf, V, L, cand, lane);
     if (n < 0) {  // constant or near-constant row: plain ranking of the staged row
       if (lane == 0) buf[blank] = rawb;
       __syncwarp();
@@ -439,7 +496,7 @@ __device__ __forceinline__ void rank_tma_body(const Items& items, int V, int bla
       mbar_arrive_tx(bar, bytes);
       bulk_g2s(buf, row, bytes, bar);
     }
-    if (n >= 0) rank_finish(cand, n, L, lpb, lane, dc);
+    if (n >= 0) rank_finish<E>(cand, n, L, lpb, lane, dc);
     if (dc.flag) {  // publish the record: every lane's stores, then the flag
       __threadfence();
       __syncwarp();
@@ -449,6 +506,30 @@ __device__ __forceinline__ void rank_tma_body(const Items& items, int V, int bla
   }
 }
 
+
+// The staged ranking with the threshold pool sized for K = L + 1 <= 512.
+template <class Items>
+__device__ __forceinline__ void rank_tma_body(const Items& items, int V, int blank, int L, u32* status,
+                                              unsigned char* smem, int vblock, int nvblocks, int nwb) {
+  if (L + 1 <= 64)
+    rank_tma_body_e<Items, 2>(items, V, blank, L, status, smem, vblock, nvblocks, nwb);
+  else if (L + 1 <= 128)
+    rank_tma_body_e<Items, 4>(items, V, blank, L, status, smem, vblock, nvblocks, nwb);
+  else if (L + 1 <= 256)
+    rank_tma_body_e<Items, 8>(items, V, blank, L, status, smem, vblock, nvblocks, nwb);
+  else
+    rank_tma_body_e<Items, 16>(items, V, blank, L, status, smem, vblock, nvblocks, nwb);
+}
+
+// The same for lists of at most 127 labels (the fused pre-pass + steps launch).
+template <class Items>
+__device__ __forceinline__ void rank_tma_body_small(const Items& items, int V, int blank, int L, u32* status,
+                                                    unsigned char* smem, int vblock, int nvblocks, int nwb) {
+  if (L + 1 <= 64)
+    rank_tma_body_e<Items, 2>(items, V, blank, L, status, smem, vblock, nvblocks, nwb);
+  else
+    rank_tma_body_e<Items, 4>(items, V, blank, L, status, smem, vblock, nvblocks, nwb);
+}
 
 }  // namespace
 }  // namespace ctcpb

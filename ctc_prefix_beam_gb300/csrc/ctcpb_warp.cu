@@ -1,4 +1,4 @@
-// Warp-per-row decode steps for beam <= 32 (flat token storage).
+// Warp-per-row decode steps for beam <= 16 (flat token storage).
 //
 // One warp owns one row for the whole call and keeps the beam in registers:
 // lane k holds hypothesis k.  Per step ("GPU CTC Prefix Beam Search Decoder",
@@ -64,7 +64,7 @@ constexpr int kRing = 128;            // steps of history between materialisatio
 constexpr int kWPC = 4;               // rows (warps) per block
 constexpr int kGenCap = 512;          // keys of the exhaustive selection
 constexpr int kGath = 128;            // gathered log-probs per frame (beam + L <= 98)
-constexpr int kMaxRec = 32 + 8 * 68;  // record bytes for beam <= 32 (L <= 66)
+constexpr int kMaxRec = 32 + 8 * 68;  // record bytes for lists of L <= 66 labels
 constexpr u32 kH32 = 2166136261u;     // prefix hash of the empty prefix
 constexpr u32 kGold = 0x9e3779b9u;
 
@@ -978,13 +978,16 @@ __global__ void __launch_bounds__(256, 1) k_fused(View st, const float* __restri
     step_warp_body<KB>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x, st.rflag());
   } else {
     RecItems items{st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, st.rflag()};
-    rank_tma_body(items, st.lay.V, st.lay.blank, st.lay.L, &st.hdr()->status, smem, (int)blockIdx.x - nsb,
+    rank_tma_body_small(items, st.lay.V, st.lay.blank, st.lay.L, &st.hdr()->status, smem, (int)blockIdx.x - nsb,
                   (int)gridDim.x - nsb, rank_warps);
   }
 }
 
+// beam <= 16: with more live hypotheses the 32-lane candidate set leaves too
+// few lanes for extensions to prove a selection (the block kernel is faster
+// from beam 17 on: 9.2 vs 17.4 ms at beam 20 on the bpe workload).
 bool step_warp_fits(const Layout& lay) {
-  return lay.beam <= 32 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
+  return lay.beam <= 16 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
 }
 
 size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem); }
@@ -1007,8 +1010,7 @@ static cudaError_t launch_kb(const View& st, const float* lp, long long sb, long
 cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (st.lay.beam <= 8) return launch_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
-  if (st.lay.beam <= 16) return launch_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
-  return launch_kb<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return launch_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }
 
 template <int KB>
@@ -1046,8 +1048,7 @@ cudaError_t launch_fused(const View& st, const float* lp, long long sb, long lon
                          int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (!step_warp_fits(st.lay) || !rank_tma_ok(lp, sb, stt, st.lay.V, st.lay.L)) return cudaErrorNotSupported;
   if (st.lay.beam <= 8) return launch_fused_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
-  if (st.lay.beam <= 16) return launch_fused_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
-  return launch_fused_kb<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return launch_fused_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }
 
 }  // namespace ctcpb

@@ -48,6 +48,7 @@ def adversarial_rows(rng, R, V):
 
 
 @pytest.mark.parametrize("V,beam,list_len", [(5000, 10, 0), (1024, 16, 0), (29, 128, 0), (32, 4, 0),
+                                              (5000, 32, 0), (5000, 64, 0), (1024, 100, 0),
                                              (7, 4, 0), (5000, 2, 3), (5000, 1, 1), (300, 31, 0),
                                              (5000, 40, 0), (2, 1, 0), (3000, 128, 0)])
 def test_prepass_lists_match_oracle(V, beam, list_len):
@@ -135,6 +136,33 @@ def test_edge_cases_match_oracle(case):
     lens = np.array([60, 0, 1, 37, 59], np.int32)
     cfg = D.Config(**case)
     assert_same(gpu_offline(cfg, lp, lens, out_len), oracle_offline(cfg, lp, lens, out_len), str(case))
+
+
+@pytest.mark.parametrize("beam,V,paged,cap", [(32, 3000, False, 0), (64, 2000, False, 0), (40, 700, True, 0),
+                                               (128, 1500, False, 0), (48, 1000, True, 5)])
+def test_block_kernel_frame_scans_match_oracle(beam, V, paged, cap):
+    """Every other frame gives all non-blank labels one log-prob, so the
+    first unlisted label ties with the listed ones and with the beam-th
+    candidate: the list cannot bound the unlisted labels and the step scans
+    the frame, where every unlisted label passes the filter (the kept-label
+    list flushes several times a frame)."""
+    rng = np.random.default_rng(beam * V)
+    B, T = 3, 30
+    x = rng.normal(0.0, 1.0, size=(B, T, V))
+    x[:, :, 0] += 1.0
+    lp = log_softmax(x)
+    lp[:, 1::2, 1:] = lp[:, 1::2, 1:].mean(-1, keepdims=True)
+    lens = np.array([30, 17, 1], np.int32)
+    cfg = D.Config(beam=beam, nbest=beam, max_seq_len=cap, paged=paged, page_size=4)
+    dev = torch.device("cuda")
+    ws = torch.empty(D.workspace_size(cfg, B, T, V), dtype=torch.uint8, device=dev)
+    tok, ln, sc = D.decode_offline(cfg, torch.from_numpy(lp).to(dev), torch.from_numpy(lens).to(dev), workspace=ws)
+    torch.cuda.synchronize()
+    g = (tok.cpu().numpy(), ln.cpu().numpy(), sc.cpu().numpy())
+    assert_same(g, oracle_offline(cfg, lp, lens), f"beam {beam} V {V} paged {paged} cap {cap}")
+    cnt = D.read_counters(ws)
+    assert cnt["steps"] == int(lens.sum())
+    assert cnt["frame_scans"] > 0, cnt
 
 
 def test_ties_and_dead_labels_match_oracle():
