@@ -70,7 +70,8 @@ def lib():
             L.ctcpb_oracle_decode.argtypes = [
                 f32p, ctypes.c_int64, ctypes.c_int64, i32p, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_float, ctypes.c_int, i32p, i32p, f32p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+                ctypes.c_float, ctypes.c_int, i32p, i32p, f32p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -148,12 +149,14 @@ def frame_lists(rows: np.ndarray, blank: int, C: int):
 
 def decode(lp: np.ndarray, lens=None, *, beam: int, nbest: int | None = None, blank: int = 0,
            cap: int | None = None, thr: float = 1.0, threads: int = 0, out_len: int | None = None,
-           mask: np.ndarray | None = None, space: int = -1):
+           mask: np.ndarray | None = None, space: int = -1, boost=None):
     """Offline CTC prefix beam search of a [B, T, V] float32 batch.
 
     ``cap`` is max_seq_len (default T), ``thr`` the blank-skip threshold
     (>= 1 keeps all frames), ``mask`` an optional [B, T] speech mask (frames
-    marked 0 are skipped too), ``space`` the word-boundary label (-1: none).  Returns (tokens [B, nbest, out_len] int32
+    marked 0 are skipped too), ``space`` the word-boundary label (-1: none),
+    ``boost`` the label bonuses: a [B, V] array (0: not boosted) or one
+    {label: bonus} dict per row.  Returns (tokens [B, nbest, out_len] int32
     padded with -1, lengths [B, nbest] int32, scores [B, nbest] float32).
     """
     lp = _f32(lp)
@@ -170,9 +173,21 @@ def decode(lp: np.ndarray, lens=None, *, beam: int, nbest: int | None = None, bl
         mk = np.ascontiguousarray(mask, np.uint8)
         if mk.shape != (B, T):
             raise ValueError("mask must be [B, T]")
+    bon = None
+    if boost is not None:
+        if isinstance(boost, np.ndarray):
+            bon = np.ascontiguousarray(boost, np.float32)
+        else:
+            bon = np.zeros((B, V), np.float32)
+            for b, row in enumerate(boost):
+                for c, v in (row or {}).items():
+                    bon[b, int(c)] = np.float32(v)
+        if bon.shape != (B, V):
+            raise ValueError("boost must be [B, V]")
     rc = lib().ctcpb_oracle_decode(lp.ravel(), T * V, V, lens, B, T, V, beam, nbest, blank, cap,
                                    float(thr), threads, tok.ravel(), ln.ravel(), sc.ravel(),
-                                   out_len, None if mk is None else mk.ctypes.data, int(space))
+                                   out_len, None if mk is None else mk.ctypes.data, int(space),
+                                   None if bon is None else bon.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle decode rejected its arguments (rc={rc})")
     return tok, ln, sc

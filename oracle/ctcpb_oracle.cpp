@@ -46,6 +46,16 @@
 //   3.4.1/3.4.2 with a word-boundary label (space_id): its extension always
 //         uses lse(pb, pnb) -- every space frame is a token of its own -- and a
 //         space-ending beam gets no stay contribution.
+//   Token boosting (the per-utterance word-boosting table of "GPU-Accelerated
+//         WFST Beam Search Decoder for CTC-based Speech Recognition", applied
+//         to CTC labels at the first page's section 15 extension point, where
+//         scores are added before the top-K): each row gives every label a
+//         bonus (0 when it is not boosted).  A label an extension emits scores
+//         lp'[c] = add(lp[c], bonus[c]) in place of lp[c] -- in the step-0
+//         ranking, the 3.4.1 extensions (repeat path included) and the 3.4.3
+//         folds -- while the blank and the stay path, which emit no label,
+//         keep lp.  Without pruning a prefix then scores log P(l) plus the sum
+//         of its labels' bonuses.
 // Readings where the page is silent or inconsistent:
 //   * ties rank by (score desc, source slot asc, token asc), blank's token is
 //     blank_id; a candidate with score <= NEG is dead and never kept;
@@ -171,6 +181,7 @@ struct Args {
   int out_len;
   const uint8_t* mask;  // [B, T] speech mask (0: skip the frame), or null
   int space;            // word-boundary label, or -1
+  const float* boost;   // [B, V] label bonuses (0: not boosted), or null
 };
 
 bool keep_frame(float lpb, float thr, float log_thr) {
@@ -184,12 +195,19 @@ float log_threshold(float thr) {
   return (float)std::log((double)thr);
 }
 
-// Non-blank live labels of one frame in (lp desc, id asc) order.
-void ranked_labels(const float* row, int V, int blank, std::vector<std::pair<float, int32_t>>& out) {
+// A label's log-prob as an emitted label: add(lp, bonus) when the row boosts
+// labels (bonus 0 leaves lp unchanged: lp is never -0).
+float emitted(const float* row, int c, const float* bonus) {
+  return bonus ? add(rd(row + c), bonus[c]) : rd(row + c);
+}
+
+// Non-blank live labels of one frame in (lp desc, id asc) order, lp as emitted.
+void ranked_labels(const float* row, int V, int blank, const float* bonus,
+                   std::vector<std::pair<float, int32_t>>& out) {
   out.clear();
   for (int c = 0; c < V; ++c) {
     if (c == blank) continue;
-    float v = rd(row + c);
+    float v = emitted(row, c, bonus);
     if (v > NEG) out.push_back({v, c});
   }
   std::sort(out.begin(), out.end(), [](const std::pair<float, int32_t>& a, const std::pair<float, int32_t>& b) {
@@ -203,6 +221,7 @@ void decode_row(const Args& a, int b) {
   auto row = [&](int t) { return base + (int64_t)t * a.st; };
   const float log_thr = log_threshold(a.thr);
   int len_b = std::min(std::max(a.lens ? a.lens[b] : a.T, 0), a.T);
+  const float* bonus = a.boost ? a.boost + (int64_t)b * a.V : nullptr;
 
   // section 3.5: ordered list of kept frames.  A speech mask (sections 8, 14
   // and 15: frames the caller marks as non-speech bypass the decoder, like
@@ -221,7 +240,7 @@ void decode_row(const Args& a, int b) {
     const bool gap0 = t0 > 0;
     const int nb = a.beam > 1 ? a.beam - 1 : 1;
     std::vector<std::pair<float, int32_t>> ranked;
-    ranked_labels(row(t0), a.V, a.blank, ranked);
+    ranked_labels(row(t0), a.V, a.blank, bonus, ranked);
     if (a.cap >= 1) {
       for (int k = 0; k < nb && k < (int)ranked.size(); ++k) {
         float v = ranked[k].first;
@@ -284,7 +303,8 @@ void decode_row(const Args& a, int b) {
           // path (pb only) when last_k is also the last label of l_i
           int i = into[k];
           const bool rep = !beams[i].pre.empty() && beams[i].pre.back() == last && last != space;
-          float ext = rep ? add(rd(lpt + last), pb[i]) : add(rd(lpt + last), A[i]);
+          const float v = emitted(lpt, last, bonus);
+          float ext = rep ? add(v, pb[i]) : add(v, A[i]);
           bpnb = lse(bpnb, ext);
         }
         float sc = lse(bpb, bpnb);
@@ -294,7 +314,7 @@ void decode_row(const Args& a, int b) {
         for (int c = 0; c < a.V; ++c) {
           if (c == a.blank) continue;
           if (std::find(folded[k].begin(), folded[k].end(), c) != folded[k].end()) continue;
-          float v = rd(lpt + c);
+          float v = emitted(lpt, c, bonus);
           float ext = (!empty && c == last && c != space) ? add(v, pb[k]) : add(v, A[k]);
           if (ext > NEG) cands.push_back(Cand{ext, k, c, NEG, ext});
         }
@@ -403,7 +423,7 @@ int ctcpb_oracle_frame_lists(const float* lp, int64_t st, int R, int V, int blan
   std::vector<std::pair<float, int32_t>> ranked;
   for (int r = 0; r < R; ++r) {
     const float* row = lp + (int64_t)r * st;
-    ranked_labels(row, V, blank, ranked);
+    ranked_labels(row, V, blank, nullptr, ranked);
     int n = std::min((int)ranked.size(), C);
     for (int i = 0; i < C; ++i) {
       ids[(int64_t)r * C + i] = i < n ? ranked[i].second : -1;
@@ -424,17 +444,18 @@ int ctcpb_oracle_frame_lists(const float* lp, int64_t st, int R, int V, int blan
 
 // Offline decode of B rows.  cap >= 1 is the per-hypothesis token cap; mask
 // ([B, T] uint8, may be null) skips every frame marked 0; space_id (-1: none)
-// is the word-boundary label.
+// is the word-boundary label; boost ([B, V] float, may be null) holds each
+// row's label bonuses.
 // Outputs: tokens [B, nbest, out_len], lengths [B, nbest], scores [B, nbest].
 int ctcpb_oracle_decode(const float* lp, int64_t sb, int64_t st, const int32_t* lens, int B, int T, int V,
                         int beam, int nbest, int blank, int cap, float thr, int threads, int32_t* out_tokens,
                         int32_t* out_lengths, float* out_scores, int out_len, const uint8_t* mask,
-                        int space_id) {
+                        int space_id, const float* boost) {
   if (B < 0 || T < 0 || V < 2 || beam < 1 || nbest < 1 || nbest > beam || blank < 0 || blank >= V || cap < 1 ||
       out_len < 0)
     return -1;
   Args a{lp, sb, st, lens, B, T, V, beam, nbest, blank, cap, thr, out_tokens, out_lengths, out_scores, out_len,
-         mask, space_id};
+         mask, space_id, boost};
   for_rows(B, threads, [&](int b) { decode_row(a, b); });
   return 0;
 }

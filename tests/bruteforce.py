@@ -26,12 +26,13 @@ def collapse(path, blank, space=None):
     return tuple(out)
 
 
-def posteriors(frames, blank, cap=None, space=None):
+def posteriors(frames, blank, cap=None, space=None, bonus=None):
     """{prefix: log P(prefix)} over all alignments of ``frames`` ([T, V], log-probs).
 
     Labels whose log-prob is <= -FLT_MAX are impossible and not enumerated.
     With ``cap``, alignments collapsing to more than ``cap`` labels are dropped.
-    ``space``: the word-boundary label of ``collapse``.
+    ``space``: the word-boundary label of ``collapse``.  ``bonus`` ({label:
+    value}): each label of a prefix adds its bonus to the prefix's log score.
     """
     frames = np.asarray(frames, dtype=np.float64)
     T, V = frames.shape
@@ -43,7 +44,8 @@ def posteriors(frames, blank, cap=None, space=None):
             continue
         lp = sum(frames[t, a] for t, a in enumerate(path))
         acc[lab] = acc.get(lab, 0.0) + math.exp(lp)
-    return {k: math.log(v) for k, v in acc.items() if v > 0.0}
+    bon = bonus or {}
+    return {k: math.log(v) + sum(float(bon.get(c, 0.0)) for c in k) for k, v in acc.items() if v > 0.0}
 
 
 def virtual_blank(V, blank):

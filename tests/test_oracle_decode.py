@@ -365,3 +365,87 @@ def test_space_equal_to_blank_has_no_effect(oracle):
     b = oracle.decode(lp, None, beam=6, space=0)
     for u, v in zip(a, b):
         assert np.array_equal(u, v)
+
+
+# ---- token boosting (the per-utterance word-boosting table of "GPU-Accelerated
+# WFST Beam Search Decoder for CTC-based Speech Recognition", applied to CTC
+# labels): a label emitted by an extension adds its bonus, so without pruning
+# a prefix scores log P(l) + the sum of its labels' bonuses
+
+def random_bonus(rng, V, blank, n):
+    labels = [c for c in range(V) if c != blank]
+    pick = rng.choice(labels, size=min(n, len(labels)), replace=False)
+    return {int(c): float(np.float32(rng.normal(0.0, 2.0))) for c in pick}
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_boost_unpruned_equals_brute_force(oracle, seed):
+    rng = np.random.default_rng(300 + seed)
+    V, T, blank = (3, 6, 0) if seed % 2 == 0 else (4, 4, 2)
+    lp = random_frames(rng, T, V, 1.5, blank, 0.5)
+    bonus = random_bonus(rng, V, blank, 2)
+    exact = posteriors(lp, blank, bonus=bonus)
+    beam = max(V, n_prefixes(V, T))
+    got, *_ = decoded(oracle, lp, beam=beam, blank=blank, boost=[bonus])
+    assert set(got) == set(exact)
+    for pre, s in got.items():
+        assert abs(s - exact[pre]) <= 2e-5 * max(1.0, abs(exact[pre])), (pre, s, exact[pre])
+    # the bonuses really move the scores
+    plain = posteriors(lp, blank)
+    assert any(abs(exact[p] - plain[p]) > 1e-3 for p in exact)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_boost_with_cap_space_and_skipping_equals_brute_force(oracle, seed):
+    rng = np.random.default_rng(330 + seed)
+    V, T, space, cap = 3, 9, 2, 3
+    x = rng.normal(0.0, 1.0, size=(T, V))
+    x[rng.random(T) < 0.4, 0] += 9.0
+    lp = log_softmax(x)
+    thr = 0.99
+    bonus = {1: 1.25, 2: -0.75}
+    aug, kept = skip_augmented(lp, 0, thr)
+    exact = posteriors(aug, 0, cap=cap, space=space, bonus=bonus)
+    beam = max(V, n_prefixes(V, len(kept), cap))
+    got, *_ = decoded(oracle, lp, beam=beam, thr=thr, space=space, cap=cap, boost=[bonus])
+    assert set(got) == set(exact)
+    for pre, s in got.items():
+        assert abs(s - exact[pre]) <= 2e-5 * max(1.0, abs(exact[pre])), (pre, s, exact[pre])
+
+
+def test_zero_bonus_is_bit_identical(oracle):
+    rng = np.random.default_rng(9)
+    lp = np.stack([random_frames(rng, 40, 12, 2.0, 0, 1.0) for _ in range(3)])
+    a = oracle.decode(lp, None, beam=5)
+    b = oracle.decode(lp, None, beam=5, boost=[{c: 0.0 for c in range(1, 12)}] * 3)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_boost_pruned_scores_at_most_exact(oracle, seed):
+    """A pruned beam keeps a subset of each prefix's alignments, each carrying
+    that prefix's bonuses, so its score is at most the exact boosted one."""
+    rng = np.random.default_rng(360 + seed)
+    V, T = 4, 7
+    lp = random_frames(rng, T, V, 1.5, 0, 0.5)
+    bonus = random_bonus(rng, V, 0, 3)
+    exact = posteriors(lp, 0, bonus=bonus)
+    got, *_ = decoded(oracle, lp, beam=3, boost=[bonus])
+    for pre, s in got.items():
+        assert s <= exact[pre] + 2e-5 * max(1.0, abs(exact[pre]))
+
+
+def test_large_bonus_wins_the_beam(oracle):
+    """A label the acoustics rank second on every frame becomes the 1-best's
+    only label once its bonus outweighs the gap."""
+    T, V = 6, 5
+    x = np.full((T, V), -4.0)
+    x[:, 0] = 0.0
+    x[2, 1] = 2.0
+    x[2, 3] = 1.0
+    lp = log_softmax(x)
+    tok, ln, _ = oracle.decode(lp[None], None, beam=4)
+    assert tok[0, 0, :ln[0, 0]].tolist() == [1]
+    tok, ln, _ = oracle.decode(lp[None], None, beam=4, boost=[{3: 2.0}])
+    assert tok[0, 0, :ln[0, 0]].tolist() == [3]
