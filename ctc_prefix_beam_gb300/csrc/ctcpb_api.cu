@@ -27,6 +27,7 @@ int check_cfg(const ctcpb_config* c, int V) {
   if (!finite_or_inf(c->blank_threshold)) return CTCPB_EINVAL;
   if (c->word_boundary != 0 && c->word_boundary != 1) return CTCPB_EINVAL;
   if (c->word_boundary && (c->space_id < 0 || c->space_id >= V)) return CTCPB_EINVAL;
+  if (c->max_boost < 0 || c->max_boost > kMaxBoost) return CTCPB_EINVAL;
   return CTCPB_OK;
 }
 
@@ -42,13 +43,15 @@ int stream_cap(const ctcpb_config* c) { return c->max_seq_len > 0 ? c->max_seq_l
 
 Layout offline_layout(const ctcpb_config* c, int B, int T, int V) {
   return make_layout(B, V, c->beam, offline_cap(c, T), c->paged, c->paged ? c->page_size : 16, c->blank_id,
-                     default_list_len(c->beam, V, c->list_len), T > 0 ? T : 1, T > 0 ? T : 1, space_of(c));
+                     default_list_len(c->beam, V, c->list_len), T > 0 ? T : 1, T > 0 ? T : 1, space_of(c),
+                     c->max_boost);
 }
 
 Layout stream_layout(const ctcpb_config* c, int B, int V) {
   // T_sel = kStreamTile: the selection holds one tile's chunk rows (speech-masked streaming)
   return make_layout(B, V, c->beam, stream_cap(c), c->paged, c->paged ? c->page_size : 16, c->blank_id,
-                     default_list_len(c->beam, V, c->list_len), kStreamTile, kStreamTile, space_of(c));
+                     default_list_len(c->beam, V, c->list_len), kStreamTile, kStreamTile, space_of(c),
+                     c->max_boost);
 }
 
 int check_buf(const void* p, size_t have, size_t need) {
@@ -59,6 +62,13 @@ int check_buf(const void* p, size_t have, size_t need) {
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? CTCPB_OK : CTCPB_ECUDA; }
+
+// A label-boost argument: boosting configured, every array given.
+int check_boost(const ctcpb_config* c, const ctcpb_boost* bo) {
+  if (c->max_boost < 1) return CTCPB_EINVAL;
+  if (!bo || !bo->row_ptr || !bo->tokens || !bo->bonus) return CTCPB_ENULL;
+  return CTCPB_OK;
+}
 
 #define TRY(x)                      \
   do {                              \
@@ -111,12 +121,18 @@ int ctcpb_workspace_size(const ctcpb_config* cfg, int B, int T, int V, size_t* b
   return CTCPB_OK;
 }
 
-int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
-                                const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
-                                int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
-                                uint32_t stage_mask, ctcpb_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The offline decode stages; boost (may be null) is built right after the init.
+int decode_offline_impl(const ctcpb_config* cfg, const ctcpb_boost* boost, const float* log_prob, int64_t stride_b,
+                        int64_t stride_t, const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                        int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                        uint32_t stage_mask, ctcpb_stream_t stream) {
   int rc = check_cfg(cfg, V);
   if (rc) return rc;
+  if (boost && (rc = check_boost(cfg, boost))) return rc;
   if (B < 0 || T < 0 || out_len < 0) return CTCPB_EINVAL;
   if (stage_mask & ~CTCPB_STAGE_ALL) return CTCPB_EINVAL;
   if (B == 0) return CTCPB_OK;
@@ -126,7 +142,10 @@ int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, 
   if ((rc = check_buf(ws, ws_bytes, lay.total))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   View st{(char*)ws, lay};
-  if (stage_mask & CTCPB_STAGE_INIT) TRY(launch_init(st, s));
+  if (stage_mask & CTCPB_STAGE_INIT) {
+    TRY(launch_init(st, s));
+    if (boost) TRY(launch_boost_build(st, boost->row_ptr, boost->tokens, boost->bonus, s));
+  }
   if (T > 0) {
     const float thr = cfg->blank_threshold;
     const int mode = thr >= 1.0f ? 0 : (thr > 0.0f ? 1 : 2);
@@ -142,6 +161,26 @@ int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, 
   if (stage_mask & CTCPB_STAGE_OUTPUT)
     TRY(launch_output(st, cfg->nbest, out_tokens, out_lengths, out_scores, out_len, s));
   return CTCPB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                                const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                                int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                                uint32_t stage_mask, ctcpb_stream_t stream) {
+  return decode_offline_impl(cfg, nullptr, log_prob, stride_b, stride_t, seq_lengths, B, T, V, ws, ws_bytes,
+                             out_tokens, out_lengths, out_scores, out_len, stage_mask, stream);
+}
+
+int ctcpb_decode_offline_boosted(const ctcpb_config* cfg, const ctcpb_boost* boost, const float* log_prob,
+                                 int64_t stride_b, int64_t stride_t, const int32_t* seq_lengths, int B, int T,
+                                 int V, void* ws, size_t ws_bytes, int32_t* out_tokens, int32_t* out_lengths,
+                                 float* out_scores, int out_len, ctcpb_stream_t stream) {
+  return decode_offline_impl(cfg, boost, log_prob, stride_b, stride_t, seq_lengths, B, T, V, ws, ws_bytes,
+                             out_tokens, out_lengths, out_scores, out_len, CTCPB_STAGE_ALL, stream);
 }
 
 int ctcpb_decode_offline(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
@@ -170,6 +209,18 @@ int ctcpb_stream_init(const ctcpb_config* cfg, void* state, size_t state_bytes, 
   if ((rc = check_buf(state, state_bytes, lay.total))) return rc;
   View st{(char*)state, lay};
   return cuda_rc(launch_init(st, (cudaStream_t)stream));
+}
+
+int ctcpb_stream_set_boost(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                           const ctcpb_boost* boost, ctcpb_stream_t stream) {
+  int rc = check_cfg(cfg, V);
+  if (rc) return rc;
+  if ((rc = check_boost(cfg, boost))) return rc;
+  if (B < 0) return CTCPB_EINVAL;
+  const Layout lay = stream_layout(cfg, B, V);
+  if ((rc = check_buf(state, state_bytes, lay.total))) return rc;
+  View st{(char*)state, lay};
+  return cuda_rc(launch_boost_build(st, boost->row_ptr, boost->tokens, boost->bonus, (cudaStream_t)stream));
 }
 
 int ctcpb_stream_step_chunk(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,

@@ -21,9 +21,11 @@ constexpr int kMaxList = 2 * kMaxBeam + 2;    // section 3.4.6: K_all <= 2*beam+
 constexpr int kMaxV = 1 << 20;                // labels fit the 20-bit token field of a rank key
 constexpr int kStreamTile = 64;               // frames ranked per pre-pass tile when streaming
 constexpr int kBlockRing = 64;                // block step kernel: steps between token-store writes
+constexpr int kMaxBoost = 4096;               // boosted labels per row
+constexpr float kMaxBonus = 1e6f;             // largest bonus magnitude
 constexpr int kStreamDefaultCap = 4096;       // section 11: STREAMING_MAX_SEQ_LEN
 constexpr u32 kMagic = 0x42504354u;           // "TCPB"
-constexpr u32 kVersion = 1u;
+constexpr u32 kVersion = 2u;
 
 // ---------------------------------------------------------------- layout
 //
@@ -38,7 +40,8 @@ struct Header {
                     // hash-proposed merges
   u64 phase_cycles[8];  // CTCPB_PHASE_PROF builds: clock64 cycles per step phase, summed over rows
   u32 fused_launches;   // pre-pass + steps launches made as one cooperative kernel
-  u32 pad1[29];
+  int32_t hcap;         // label-boost hash slots per row (0: no boosting)
+  u32 pad1[28];
 };
 static_assert(sizeof(Header) == 256, "header is 256 bytes");
 
@@ -58,10 +61,11 @@ struct Layout {
   int max_lp;  // paged: logical pages per hypothesis
   int ppr;     // paged: physical pages per row
   int T_sel;   // selection entries per row: offline T (frames); streaming kStreamTile (one tile's chunk rows)
+  int max_boost, hcap;  // boosted labels per row and hash slots per row (a power of two, 0: no boosting)
   size_t rec_bytes;
   size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp, o_msrc;
   size_t o_clist, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;
-  size_t o_recs, o_rflag, o_sel, o_nsel, total;
+  size_t o_recs, o_rflag, o_sel, o_nsel, o_bkey, o_bval, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -80,7 +84,7 @@ inline int default_list_len(int beam, int V, int list_len) {
 // Build the layout.  tile = records per row; T_sel = selection list length
 // (offline T, 0 when streaming).
 inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_size, int blank, int L,
-                          int tile, int T_sel, int space = -1) {
+                          int tile, int T_sel, int space = -1, int max_boost = 0) {
   Layout o{};
   o.space = (space >= 0 && space != blank) ? space : -1;
   o.B = B; o.V = V; o.beam = beam; o.cap = cap; o.paged = paged; o.page_size = page_size;
@@ -93,6 +97,12 @@ inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_s
   const int gain_pages = (kBlockRing + page_size - 1) / page_size + 1;
   o.ppr = paged ? beam * (o.max_lp + (gain_pages < o.max_lp ? gain_pages : o.max_lp)) : 0;
   o.rec_bytes = align_up(32 + 8 * (size_t)o.Lpad, 32);
+  o.max_boost = max_boost > 0 ? max_boost : 0;
+  o.hcap = 0;
+  if (o.max_boost > 0) {  // open addressing at load <= 1/2
+    o.hcap = 2;
+    while (o.hcap < 2 * o.max_boost) o.hcap <<= 1;
+  }
   const size_t A = 256;
   size_t off = sizeof(Header);
   auto take = [&](size_t bytes) { size_t at = align_up(off, A); off = at + bytes; return at; };
@@ -121,6 +131,10 @@ inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_s
   if (T_sel > 0) {
     o.o_sel = take(4 * (size_t)B * T_sel);
     o.o_nsel = take(4 * (size_t)B);
+  }
+  if (o.hcap > 0) {
+    o.o_bkey = take(4 * (size_t)B * o.hcap);
+    o.o_bval = take(4 * (size_t)B * o.hcap);
   }
   o.total = align_up(off, A);
   return o;
@@ -162,6 +176,9 @@ struct View {
   }
   // record ready flags [B][tile]: set by the pre-pass, cleared by the step
   // kernel once it has copied the record (only when the two run concurrently)
+  // label-boost hash table of row b: hcap (label, bonus) slots, label -1 empty
+  __host__ __device__ int* bkey(int b) const { return (int*)(base + lay.o_bkey) + (size_t)b * lay.hcap; }
+  __host__ __device__ float* bval(int b) const { return (float*)(base + lay.o_bval) + (size_t)b * lay.hcap; }
   __host__ __device__ u32* rflag() const { return (u32*)(base + lay.o_rflag); }
   __host__ __device__ int* sel() const { return (int*)(base + lay.o_sel); }
   __host__ __device__ int* nsel() const { return (int*)(base + lay.o_nsel); }
@@ -249,6 +266,32 @@ __device__ __forceinline__ float dadd(float a, float b) { return fmaxf(__fadd_rn
 
 // Read a log-prob: NaN and -inf become NEG, -0 becomes +0.
 __device__ __forceinline__ float rdlp(float raw) { return __fadd_rn(fmaxf(raw, CTCPB_NEG), 0.0f); }
+
+// Does the state's header describe this layout?  (A state initialised with
+// another configuration or size must not be written through this one.)
+__device__ __forceinline__ bool header_matches(const View& st) {
+  const Header* hd = st.hdr();
+  const Layout& Ly = st.lay;
+  return hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V && hd->beam == Ly.beam &&
+         hd->cap == Ly.cap && hd->paged == Ly.paged && hd->page_size == Ly.page_size && hd->blank == Ly.blank &&
+         hd->list_len == Ly.L && hd->tile == Ly.tile && hd->space == Ly.space && hd->hcap == Ly.hcap;
+}
+
+// Home slot of label c in a label-boost table of hmask + 1 slots.
+__host__ __device__ __forceinline__ int boost_slot(int c, int hmask) { return (int)(((u32)c * 0x9E3779B1u) & (u32)hmask); }
+
+// The bonus of label c in a row's label-boost table (0 when c is not boosted):
+// linear probing from its home slot to the label or an empty slot (the table
+// is at most half full, so one exists).
+__device__ __forceinline__ float boost_of(const int* __restrict__ keys, const float* __restrict__ vals, int hmask,
+                                          int c) {
+  for (int i = boost_slot(c, hmask), n = 0; n <= hmask; i = (i + 1) & hmask, ++n) {
+    const int k = keys[i];
+    if (k == c) return vals[i];
+    if (k < 0) break;
+  }
+  return 0.0f;
+}
 
 // Order-preserving unsigned image of a float (larger float -> larger key).
 __host__ __device__ __forceinline__ u32 fkey(float f) {

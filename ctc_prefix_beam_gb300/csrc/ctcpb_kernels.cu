@@ -108,6 +108,7 @@ __global__ void k_init(View st) {
     for (int i = 0; i < 5; ++i) h->counters[i] = 0u;
     for (int i = 0; i < 8; ++i) h->phase_cycles[i] = 0ull;
     h->fused_launches = 0u;
+    h->hcap = L.hcap;
   }
   for (size_t b = tid; b < (size_t)L.B; b += nthr) {
     RowHdr r;
@@ -124,6 +125,11 @@ __global__ void k_init(View st) {
     u32* rf = st.rflag();
     for (size_t i = tid; i < nf; i += nthr) rf[i] = 0u;
   }
+  if (L.hcap > 0) {  // no label is boosted until a table is set
+    const size_t nk = (size_t)L.B * L.hcap;
+    int* bk = (int*)(st.base + L.o_bkey);
+    for (size_t i = tid; i < nk; i += nthr) bk[i] = -1;
+  }
   if (L.paged) {
     const size_t nt = 2 * (size_t)L.B * L.beam * L.max_lp;
     int* bt = (int*)(st.base + L.o_btab);
@@ -132,6 +138,49 @@ __global__ void k_init(View st) {
     int* rc = (int*)(st.base + L.o_refc);
     for (size_t i = tid; i < np; i += nthr) rc[i] = 0;
   }
+}
+
+// ------------------------------------------------------------------ label boosts
+// Row b's label-boost hash table from entries [row_ptr[b], row_ptr[b+1]) of
+// (tokens, bonus), taken in order by one thread (so a repeated label keeps its
+// first bonus whatever the launch).  Rejected entries set CTCPB_DEV_BOOST.
+__global__ void __launch_bounds__(64) k_boost_build(View st, const int* __restrict__ row_ptr,
+                                                    const int* __restrict__ tokens, const float* __restrict__ bonus) {
+  const Layout& L = st.lay;
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= L.B) return;
+  if (!header_matches(st)) {
+    set_status(st, CTCPB_DEV_HEADER);
+    return;
+  }
+  const int hm = L.hcap - 1;
+  int* keys = st.bkey(b);
+  float* vals = st.bval(b);
+  for (int i = 0; i <= hm; ++i) {
+    keys[i] = -1;
+    vals[i] = 0.0f;
+  }
+  const int lo = row_ptr[b], hi = row_ptr[b + 1];
+  bool bad = lo < 0 || hi < lo;
+  int n = 0;
+  for (int e = bad ? hi : lo; e < hi; ++e) {
+    const int c = tokens[e];
+    const float v = bonus[e];
+    if (n >= L.max_boost || c < 0 || c >= L.V || c == L.blank || !(fabsf(v) <= kMaxBonus)) {
+      bad = true;
+      continue;
+    }
+    int i = boost_slot(c, hm);
+    while (keys[i] >= 0 && keys[i] != c) i = (i + 1) & hm;  // n < hcap / 2: an empty slot exists
+    if (keys[i] == c) {
+      bad = true;
+      continue;
+    }
+    keys[i] = c;
+    vals[i] = v;
+    ++n;
+  }
+  if (bad) set_status(st, CTCPB_DEV_BOOST);
 }
 
 // ------------------------------------------------------------------ select
@@ -210,7 +259,7 @@ struct StepSmem {
   int last[NT], len[NT];
   u64 h[NT], hp[NT];
   // per step
-  float A[NT], pbg[NT], lpl[NT], bpb[NT], bpnb[NT], rep[NT];
+  float A[NT], pbg[NT], lpl[NT], lple[NT], bpb[NT], bpnb[NT], rep[NT];  // lple: lp[last] as emitted (boosted)
   int into[NT], repdead[NT];
   // next hypotheses
   float npb[NT], npnb[NT], nsc[NT];
@@ -449,13 +498,17 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V;
   const int space = Ly.space;  // word-boundary label, -1: none
   const float NEG = CTCPB_NEG;
+  // the row's label-boost table (null: no boosting)
+  const int* bkeys = Ly.hcap > 0 ? st.bkey(b) : nullptr;
+  const float* bvals = Ly.hcap > 0 ? st.bval(b) : nullptr;
+  const int hmask = Ly.hcap - 1;
 
   if (mode != 0) {
     const Header* hd = st.hdr();
     bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
               hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
               hd->page_size == Ly.page_size && hd->blank == Ly.blank && hd->list_len == Ly.L &&
-              hd->tile == Ly.tile && hd->space == Ly.space;
+              hd->tile == Ly.tile && hd->space == Ly.space && hd->hcap == Ly.hcap;
     if (!ok) {
       if (tid == 0) set_status(st, CTCPB_DEV_HEADER);
       return;
@@ -595,15 +648,18 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         const float A = dlse(pb, pnb);
         const int L = S.len[k];
         const float lpl = L > 0 ? rdlp(row[S.last[k]]) : NEG;
+        // the last label emitted again (the repeat path, a merge fold) carries its bonus
+        const float lple = (L > 0 && bkeys) ? dadd(lpl, boost_of(bkeys, bvals, hmask, S.last[k])) : lpl;
         S.A[k] = A;
         S.pbg[k] = pb;
         S.lpl[k] = lpl;
+        S.lple[k] = lple;
         S.bpb[k] = dadd(S.lpb, A);
         // a space-ending beam has no stay path, and its candidate (k, last)
         // extends from both paths (every space frame is a token)
         const bool spc = S.last[k] == space;
         S.bpnb[k] = (L > 0 && !gap && !spc) ? dadd(lpl, pnb) : NEG;
-        S.rep[k] = (L > 0 && L < cap) ? dadd(lpl, spc ? A : pb) : NEG;
+        S.rep[k] = (L > 0 && L < cap) ? dadd(lple, spc ? A : pb) : NEG;
         S.repdead[k] = 0;
         S.into[k] = -1;
         for (int w = 0; w < (kMaxList + 31) / 32; ++w) S.excl[k][w] = 0u;
@@ -626,7 +682,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         const int c = S.last[j];
         const bool same = S.len[i] > 0 && S.last[i] == c;  // the folded candidate is i's (i, last) entry
         const bool rep_i = same && c != space;
-        const float ext = rep_i ? dadd(S.lpl[j], S.pbg[i]) : dadd(S.lpl[j], S.A[i]);
+        const float ext = rep_i ? dadd(S.lple[j], S.pbg[i]) : dadd(S.lple[j], S.A[i]);
         S.bpnb[j] = dlse(S.bpnb[j], ext);
         if (same) {
           S.repdead[i] = 1;
@@ -830,6 +886,13 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
             for (int u = 0; u < 4; ++u) {
               const int c = c0 + u * NT + tid;
               v[u] = c < V ? rdlp(row[c]) : NEG;
+            }
+            if (bkeys) {  // labels as emitted: the list ranks them by the boosted log-prob
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * NT + tid;
+                if (c < V) v[u] = dadd(v[u], boost_of(bkeys, bvals, hmask, c));
+              }
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -1137,6 +1200,13 @@ static int grid_for(long long items_per_warp_units, int warps_per_block) {
 
 cudaError_t launch_init(const View& st, cudaStream_t s) {
   k_init<<<grid_for((long long)st.lay.B * st.lay.beam * 2 + 1, 8), 256, 0, s>>>(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_boost_build(const View& st, const int* row_ptr, const int* tokens, const float* bonus,
+                               cudaStream_t s) {
+  if (st.lay.B == 0 || st.lay.hcap == 0) return cudaSuccess;
+  k_boost_build<<<(st.lay.B + 63) / 64, 64, 0, s>>>(st, row_ptr, tokens, bonus);
   return cudaGetLastError();
 }
 

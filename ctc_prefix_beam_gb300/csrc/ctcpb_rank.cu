@@ -69,8 +69,9 @@ __global__ void __launch_bounds__(256) k_prepass(View st, const float* __restric
     char* r = st.rec(b, s);
     RecHdr* h = (RecHdr*)r;
     if (lane == 0) h->t = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
+    const BoostTab bt{Ly.hcap > 0 ? st.bkey(b) : nullptr, Ly.hcap > 0 ? st.bval(b) : nullptr, Ly.hcap - 1};
     rank_row(row, Ly.V, Ly.blank, Ly.L, bufs[wid], lane, rec_ids(r), rec_lps(r, Ly.Lpad), &h->cnt, &h->lpb,
-             &h->front_lp, &h->front_id);
+             &h->front_lp, &h->front_id, bt);
   }
 }
 

@@ -64,20 +64,31 @@ __device__ __forceinline__ int pow2_at_least(int n, int lo) {
 //      L+1 rounds of "largest key below the previous one".
 constexpr int kRankCap = 512;  // shared keys per ranking warp
 
-__device__ __forceinline__ u64 label_key_at(const float* __restrict__ row, int c, int V, int blank) {
+// A row's label-boost table (keys null: no boosting).
+struct BoostTab {
+  const int* keys;
+  const float* vals;
+  int hmask;
+};
+
+// Label c's ranking key, by its log-prob as emitted (boosted when bt.keys).
+__device__ __forceinline__ u64 label_key_at(const float* __restrict__ row, int c, int V, int blank,
+                                            const BoostTab& bt) {
   if (c >= V || c == blank) return 0ull;
   float v = rdlp(row[c]);
+  if (bt.keys) v = dadd(v, boost_of(bt.keys, bt.vals, bt.hmask, c));
   return v > CTCPB_NEG ? lab_key(v, c) : 0ull;
 }
 
 __device__ void rank_row(const float* __restrict__ row, int V, int blank, int L, u64* buf, int lane,
-                         int* o_ids, float* o_lps, int* o_cnt, float* o_lpb, float* o_flp, int* o_fid) {
+                         int* o_ids, float* o_lps, int* o_cnt, float* o_lpb, float* o_flp, int* o_fid,
+                         const BoostTab& bt = BoostTab{nullptr, nullptr, 0}) {
   const int K = L + 1;
   u64 tau = 0ull;
   if (K <= 64) {
     u64 k1 = 0ull, k2 = 0ull;
     for (int c = lane; c < V; c += 32) {
-      u64 key = label_key_at(row, c, V, blank);
+      u64 key = label_key_at(row, c, V, blank, bt);
       if (key > k2) {
         if (key > k1) {
           k2 = k1;
@@ -98,7 +109,7 @@ __device__ void rank_row(const float* __restrict__ row, int V, int blank, int L,
   bool ovf = false;
   for (int c0 = 0; c0 < V; c0 += 32) {
     const int c = c0 + lane;
-    u64 key = label_key_at(row, c, V, blank);
+    u64 key = label_key_at(row, c, V, blank, bt);
     bool take = key != 0ull && key >= tau;
     unsigned m = __ballot_sync(FULL, take);
     int tot = __popc(m);
@@ -121,7 +132,7 @@ __device__ void rank_row(const float* __restrict__ row, int V, int blank, int L,
     for (int r = 0; r < K; ++r) {
       u64 best = 0ull;
       for (int c = lane; c < V; c += 32) {
-        u64 key = label_key_at(row, c, V, blank);
+        u64 key = label_key_at(row, c, V, blank, bt);
         if (key < prev && key > best) best = key;
       }
       best = warp_max_u64(best);
@@ -170,6 +181,7 @@ struct RankDst {
   int* tout;
   int t;
   u32* flag;  // set (release) once the record is complete; null: none
+  BoostTab boost;  // the frame's row's label boosts (keys null: none)
 };
 
 // Items of the decode: (row b, step s), frame-major, records in the state.
@@ -203,8 +215,10 @@ struct RecItems {
     const int b = (int)(it % B), s = (int)(it / B);
     char* r = st.rec(b, s);
     RecHdr* h = (RecHdr*)r;
+    const bool bo = st.lay.hcap > 0;
     return RankDst{rec_ids(r),  rec_lps(r, st.lay.Lpad), &h->cnt, &h->lpb, &h->front_lp, &h->front_id, &h->t, t,
-                   flags ? flags + (size_t)b * st.lay.tile + s : nullptr};
+                   flags ? flags + (size_t)b * st.lay.tile + s : nullptr,
+                   BoostTab{bo ? st.bkey(b) : nullptr, bo ? st.bval(b) : nullptr, st.lay.hcap - 1}};
   }
 };
 
@@ -222,7 +236,8 @@ struct RowItems {
     return true;
   }
   __device__ RankDst dst(long long r, int t) const {
-    return RankDst{ids + r * L, lps + r * L, cnt + r, lpb + r, flp + r, fid + r, nullptr, t, nullptr};
+    return RankDst{ids + r * L, lps + r * L, cnt + r, lpb + r, flp + r, fid + r, nullptr, t, nullptr,
+                   BoostTab{nullptr, nullptr, 0}};
   }
 };
 
@@ -481,6 +496,12 @@ __device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int b
     const float lpb = rdlp(rawb);
     __syncwarp();
     if (lane == 0) buf[blank] = -INFINITY;  // the blank is not a label of the list
+    if (dc.boost.keys) {  // rank the labels as emitted: add the row's bonuses (never the blank's)
+      for (int i = lane; i <= dc.boost.hmask; i += 32) {
+        const int c = dc.boost.keys[i];
+        if (c >= 0) buf[c] = dadd(rdlp(buf[c]), dc.boost.vals[i]);
+      }
+    }
     __syncwarp();
     const int n = rank_gather<E>(buf, V, L, cand, lane);
     if (n < 0) {  // constant or near-constant row: plain ranking of the staged row

@@ -597,7 +597,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     bool ok = hd->magic == kMagic && hd->version == kVersion && hd->B == Ly.B && hd->V == Ly.V &&
               hd->beam == Ly.beam && hd->cap == Ly.cap && hd->paged == Ly.paged &&
               hd->page_size == Ly.page_size && hd->blank == Ly.blank && hd->list_len == Ly.L &&
-              hd->tile == Ly.tile && hd->space == Ly.space;
+              hd->tile == Ly.tile && hd->space == Ly.space && hd->hcap == Ly.hcap;
     if (!ok) {
       if (lane == 0) atomicOr(&st.hdr()->status, CTCPB_DEV_HEADER);
       return;
@@ -987,7 +987,7 @@ __global__ void __launch_bounds__(256, 1) k_fused(View st, const float* __restri
 // few lanes for extensions to prove a selection (the block kernel is faster
 // from beam 17 on: 9.2 vs 17.4 ms at beam 20 on the bpe workload).
 bool step_warp_fits(const Layout& lay) {
-  return lay.beam <= 16 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
+  return lay.beam <= 16 && !lay.paged && lay.hcap == 0 && lay.rec_bytes <= (size_t)kMaxRec;
 }
 
 size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem); }

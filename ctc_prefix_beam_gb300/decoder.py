@@ -35,7 +35,11 @@ class _Cfg(ctypes.Structure):
     _fields_ = [("beam", ctypes.c_int32), ("nbest", ctypes.c_int32), ("blank_id", ctypes.c_int32),
                 ("max_seq_len", ctypes.c_int32), ("blank_threshold", ctypes.c_float),
                 ("paged", ctypes.c_int32), ("page_size", ctypes.c_int32), ("list_len", ctypes.c_int32),
-                ("word_boundary", ctypes.c_int32), ("space_id", ctypes.c_int32)]
+                ("word_boundary", ctypes.c_int32), ("space_id", ctypes.c_int32), ("max_boost", ctypes.c_int32)]
+
+
+class _Boost(ctypes.Structure):
+    _fields_ = [("row_ptr", ctypes.c_void_p), ("tokens", ctypes.c_void_p), ("bonus", ctypes.c_void_p)]
 
 
 @dataclasses.dataclass
@@ -50,11 +54,12 @@ class Config:
     page_size: int = 16
     list_len: int = 0
     space_id: int = -1  # word-boundary label (sections 3.4.1/3.4.2), -1: none
+    max_boost: int = 0  # boosted labels per row (0: no label boosting)
 
     def c(self) -> _Cfg:
         return _Cfg(self.beam, self.beam if self.nbest is None else self.nbest, self.blank_id,
                     self.max_seq_len, self.blank_threshold, int(bool(self.paged)), self.page_size,
-                    self.list_len, 1 if self.space_id >= 0 else 0, max(self.space_id, 0))
+                    self.list_len, 1 if self.space_id >= 0 else 0, max(self.space_id, 0), self.max_boost)
 
 
 def lib_path() -> str:
@@ -80,6 +85,9 @@ def lib():
                 "ctcpb_decode_offline": (I, [cfgp, P, I64, I64, P, I, I, I, P, SZ, P, P, P, I, P]),
                 "ctcpb_decode_offline_staged": (I, [cfgp, P, I64, I64, P, I, I, I, P, SZ, P, P, P, I,
                                                     ctypes.c_uint32, P]),
+                "ctcpb_decode_offline_boosted": (I, [cfgp, ctypes.POINTER(_Boost), P, I64, I64, P, I, I, I, P, SZ,
+                                                     P, P, P, I, P]),
+                "ctcpb_stream_set_boost": (I, [cfgp, P, SZ, I, I, ctypes.POINTER(_Boost), P]),
                 "ctcpb_state_size": (I, [cfgp, I, I, ctypes.POINTER(SZ)]),
                 "ctcpb_stream_init": (I, [cfgp, P, SZ, I, I, P]),
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
@@ -158,14 +166,49 @@ def _outputs(B, nbest, out_len, device):
 STAGE_INIT, STAGE_SELECT, STAGE_RANK, STAGE_STEPS, STAGE_OUTPUT, STAGE_ALL = 0x1, 0x2, 0x4, 0x8, 0x10, 0x1f
 
 
+def boost_tables(boost, B: int, device):
+    """Label boosts in the compressed-row form of ``ctcpb_boost``: from one
+    {label: bonus} dict (or None) per row, or from (row_ptr, tokens, bonus)
+    tensors, which are moved to ``device``."""
+    if isinstance(boost, (tuple, list)) and len(boost) == 3 and all(isinstance(x, torch.Tensor) for x in boost):
+        rp, tk, bn = boost
+    else:
+        rows = list(boost)
+        if len(rows) != B:
+            raise ValueError("boost needs one entry per row")
+        rp, tk, bn = [0], [], []
+        for row in rows:
+            for c, v in (row or {}).items():
+                tk.append(int(c))
+                bn.append(float(v))
+            rp.append(len(tk))
+        rp, tk, bn = torch.tensor(rp, dtype=torch.int32), torch.tensor(tk, dtype=torch.int32), \
+            torch.tensor(bn, dtype=torch.float32)
+    rp = rp.to(device=device, dtype=torch.int32).contiguous()
+    tk = tk.to(device=device, dtype=torch.int32).contiguous()
+    bn = bn.to(device=device, dtype=torch.float32).contiguous()
+    if rp.numel() != B + 1:
+        raise ValueError("row_ptr must hold B + 1 offsets")
+    if tk.numel() == 0:  # the arrays must be non-null even when no row boosts a label
+        tk = torch.zeros(1, dtype=torch.int32, device=device)
+        bn = torch.zeros(1, dtype=torch.float32, device=device)
+    return rp, tk, bn
+
+
+def _boost_arg(tables):
+    rp, tk, bn = tables
+    return _Boost(rp.data_ptr(), tk.data_ptr(), bn.data_ptr())
+
+
 def decode_offline(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None, *,
                    workspace: Optional[torch.Tensor] = None, out_len: Optional[int] = None, outputs=None,
-                   stages: int = STAGE_ALL):
+                   stages: int = STAGE_ALL, boost=None):
     """Offline decode of a CUDA float32 [B, T, V] batch.
 
     Returns (tokens [B, nbest, out_len] int32 padded -1, lengths [B, nbest]
     int32, scores [B, nbest] float32), all on the device.  ``out_len``
-    defaults to min(max_seq_len, T) (T when the cap is unset).
+    defaults to min(max_seq_len, T) (T when the cap is unset).  ``boost``:
+    the rows' label boosts (``boost_tables``; needs ``cfg.max_boost``).
     """
     lp = _f32_3d(log_prob)
     B, T, V = lp.shape
@@ -181,7 +224,15 @@ def decode_offline(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[to
     if workspace is None:
         workspace = _alloc(need, lp.device)
     tok, ln, sc = _outputs(B, nbest, out_len, lp.device) if outputs is None else outputs
-    if stages == STAGE_ALL:
+    if boost is not None:
+        if stages != STAGE_ALL:
+            raise ValueError("a boosted decode runs every stage")
+        tables = boost_tables(boost, B, lp.device)
+        rc = lib().ctcpb_decode_offline_boosted(ctypes.byref(c), ctypes.byref(_boost_arg(tables)), _ptr(lp),
+                                                lp.stride(0), lp.stride(1), _ptr(seq_lengths), B, T, V,
+                                                _ptr(workspace), workspace.numel(), _ptr(tok), _ptr(ln), _ptr(sc),
+                                                out_len, _stream(lp.device))
+    elif stages == STAGE_ALL:
         rc = lib().ctcpb_decode_offline(ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
                                         _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
                                         _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(lp.device))
@@ -206,6 +257,13 @@ class StreamState:
     def init(self):
         _check(lib().ctcpb_stream_init(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
                                        self.V, _stream(self.buf.device)), "stream_init")
+
+    def set_boost(self, boost):
+        """Replace every stream's label boosts (``boost_tables``) from the next frame on."""
+        tables = boost_tables(boost, self.B, self.buf.device)
+        _check(lib().ctcpb_stream_set_boost(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
+                                            self.V, ctypes.byref(_boost_arg(tables)), _stream(self.buf.device)),
+               "stream_set_boost")
 
     def step_chunk(self, lp_chunk: torch.Tensor, n_frames: Optional[torch.Tensor] = None,
                    is_speech: Optional[torch.Tensor] = None):

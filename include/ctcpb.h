@@ -54,6 +54,7 @@ typedef struct CUstream_st* ctcpb_stream_t;
 #define CTCPB_DEV_PAGES 0x2u    /* paged token pool exhausted: the beam kept its prefix (section 13) */
 #define CTCPB_DEV_TIMEOUT 0x4u  /* a bounded inter-block wait gave up: results of the call are invalid */
 #define CTCPB_DEV_OVERFLOW 0x8u /* an internal candidate buffer overflowed: results are invalid */
+#define CTCPB_DEV_BOOST 0x10u   /* a label-boost entry was rejected and ignored (see ctcpb_boost) */
 
 /*
  * Decoder configuration (section 11).
@@ -81,6 +82,10 @@ typedef struct CUstream_st* ctcpb_stream_t;
  *                    of its own, and a space-ending beam has no stay path.
  *   space_id         the word-boundary label, 0..V-1 (no effect when it equals
  *                    blank_id); ignored when word_boundary is 0.
+ *   max_boost        0: no label boosting.  1..4096: every row (utterance or
+ *                    stream) may boost up to max_boost labels (ctcpb_boost);
+ *                    the workspace / state then holds a label-boost hash table
+ *                    per row, and the decode steps run on the block kernel.
  */
 typedef struct ctcpb_config {
   int32_t beam;
@@ -93,17 +98,49 @@ typedef struct ctcpb_config {
   int32_t list_len;
   int32_t word_boundary;
   int32_t space_id;
+  int32_t max_boost;
 } ctcpb_config;
 
 /*
+ * Label boosting: the per-utterance word-boosting table of "GPU-Accelerated
+ * WFST Beam Search Decoder for CTC-based Speech Recognition" (one hash table
+ * per utterance, consulted whenever an output label is emitted), applied to
+ * CTC labels at the extension point the decoder page names in section 15
+ * (scores added to the extension table before the top-K).  A label c that an
+ * extension emits -- including the repeat after a blank -- scores
+ * lp'[c] = lp[c] + bonus[c] (float32, clamped at -FLT_MAX) in place of
+ * lp[c]: in the per-frame label ranking (so step 0 seeds by lp'), in the
+ * section 3.4.1 extensions and in the 3.4.3 merge folds.  The blank and the
+ * stay path emit no label and keep lp.  Without pruning a prefix scores its
+ * CTC log-posterior plus the sum of its labels' bonuses; a positive bonus
+ * favours the label, a negative one penalises it.
+ *
+ * The table of every row is given in compressed-row form, all DEVICE arrays:
+ *   row_ptr  [B + 1] int32: row b's entries are [row_ptr[b], row_ptr[b+1])
+ *   tokens   [row_ptr[B]] int32: the boosted labels
+ *   bonus    [row_ptr[B]] float32: their bonuses
+ * Entries are taken in order.  One is rejected -- ignored, with
+ * CTCPB_DEV_BOOST set in the device status -- when its label is outside
+ * [0, V) or is the blank, repeats an earlier label of the row, its bonus is
+ * not finite or exceeds 1e6 in magnitude, or the row already holds max_boost
+ * labels; a row whose offsets decrease is ignored whole.
+ */
+typedef struct ctcpb_boost {
+  const int32_t* row_ptr;
+  const int32_t* tokens;
+  const float* bonus;
+} ctcpb_boost;
+
+/*
  * Diagnostic counters of the last call on a workspace or state (synchronises
- * the device): [0] decode steps of the warp path, [1] steps whose first
- * candidate set could not prove the selection, [2] of those, steps that fell
- * back to an exhaustive selection over the frame's list, [3] steps that also
- * scored every unlisted label of the frame, [4] merges proposed by prefix
- * hashes and checked on stored tokens, [5] launches that ran the pre-pass and
- * the steps of a tile as one cooperative kernel (CTCPB_NO_FUSE=1 in the
- * environment makes every call use two kernels instead).
+ * the device): [0] decode steps, [1] steps whose first candidate set could not
+ * prove the selection, [2] steps that fell back to an exhaustive selection
+ * (warp kernel: over the frame's list; block kernel: the chunked sort of every
+ * candidate), [3] steps that also scored every unlisted label of the frame,
+ * [4] merges proposed by prefix hashes and confirmed on stored tokens, [5]
+ * launches that ran the pre-pass and the steps of a tile as one cooperative
+ * kernel (CTCPB_NO_FUSE=1 in the environment makes every call use two kernels
+ * instead).
  */
 int ctcpb_read_counters(const void* ws_or_state, uint32_t counters[6]);
 
@@ -136,6 +173,18 @@ int ctcpb_decode_offline(const ctcpb_config* cfg, const float* log_prob, int64_t
                          const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
                          int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
                          ctcpb_stream_t stream);
+
+/*
+ * ctcpb_decode_offline with label boosting (ctcpb_boost): row b of the batch
+ * boosts the labels of boost's row b.  Requires cfg->max_boost >= 1.  A NULL
+ * boost is ctcpb_decode_offline.  Errors: CTCPB_EINVAL when max_boost is 0,
+ * CTCPB_ENULL for a NULL row_ptr, tokens or bonus, otherwise as
+ * ctcpb_decode_offline.
+ */
+int ctcpb_decode_offline_boosted(const ctcpb_config* cfg, const ctcpb_boost* boost, const float* log_prob,
+                                 int64_t stride_b, int64_t stride_t, const int32_t* seq_lengths, int B, int T,
+                                 int V, void* ws, size_t ws_bytes, int32_t* out_tokens, int32_t* out_lengths,
+                                 float* out_scores, int out_len, ctcpb_stream_t stream);
 
 /*
  * Offline decode for callers that cannot allocate device memory.  The pages
@@ -174,6 +223,16 @@ int ctcpb_state_size(const ctcpb_config* cfg, int B, int V, size_t* bytes);
  */
 int ctcpb_stream_init(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
                       ctcpb_stream_t stream);
+
+/*
+ * Set the label boosts of every stream of a state (ctcpb_boost; requires
+ * cfg->max_boost >= 1): they replace the streams' previous boosts and apply
+ * from the next decoded frame on (ctcpb_stream_init clears them).  Errors:
+ * CTCPB_EINVAL when max_boost is 0, CTCPB_ENULL for a NULL boost, row_ptr,
+ * tokens or bonus, otherwise as ctcpb_stream_step_chunk.
+ */
+int ctcpb_stream_set_boost(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                           const ctcpb_boost* boost, ctcpb_stream_t stream);
 
 /*
  * Decode one chunk of frames for every stream (section 8, ctc_beam_search_chunk).

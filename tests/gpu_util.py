@@ -27,7 +27,7 @@ def gpu_offline(cfg, lp: np.ndarray, lens: np.ndarray | None, out_len=None):
     return tok.cpu().numpy(), l.cpu().numpy(), s.cpu().numpy()
 
 
-def oracle_offline(cfg, lp, lens, out_len=None, rows=None):
+def oracle_offline(cfg, lp, lens, out_len=None, rows=None, boost=None):
     T = lp.shape[1]
     cap = cfg.max_seq_len if cfg.max_seq_len > 0 else T
     cap = min(cap, max(T, 1))
@@ -37,8 +37,9 @@ def oracle_offline(cfg, lp, lens, out_len=None, rows=None):
     if rows is not None:
         lp = lp[rows]
         lens = None if lens is None else lens[rows]
+        boost = None if boost is None else [boost[r] for r in rows]
     return O.decode(lp, lens, beam=cfg.beam, nbest=nb, blank=cfg.blank_id, cap=cap,
-                    thr=cfg.blank_threshold, out_len=out_len, space=cfg.space_id)
+                    thr=cfg.blank_threshold, out_len=out_len, space=cfg.space_id, boost=boost)
 
 
 def assert_same(g, o, what="", exact_scores=True):

@@ -118,3 +118,39 @@ def test_host_validation_before_any_launch(lib):
     assert lib.ctcpb_read_status(NULL, NULL) == D.ENULL
     assert lib.ctcpb_topk_prepass(ctypes.byref(c), NULL, 10, 5, 5000, NULL, NULL, NULL, NULL, NULL, NULL,
                                   NULL) == D.EINVAL
+
+
+def test_label_boost_config_and_host_validation(lib):
+    n0, n1 = ctypes.c_size_t(), ctypes.c_size_t()
+    c = cfg().c()
+    assert lib.ctcpb_workspace_size(ctypes.byref(c), 4, 50, 5000, ctypes.byref(n0)) == D.OK
+    c.max_boost = 100  # a label-boost table of 256 slots per row
+    assert lib.ctcpb_workspace_size(ctypes.byref(c), 4, 50, 5000, ctypes.byref(n1)) == D.OK
+    assert n1.value >= n0.value + 4 * 256 * 8
+    for bad in (-1, 4097):
+        c.max_boost = bad
+        assert lib.ctcpb_workspace_size(ctypes.byref(c), 4, 50, 5000, ctypes.byref(n1)) == D.EINVAL
+    NULL = None
+    big = ctypes.c_void_p(1 << 20)
+    tables = D._Boost(1 << 20, 1 << 20, 1 << 20)
+    no_tokens = D._Boost(1 << 20, None, 1 << 20)
+    args = (big, 50000, 5000, NULL, 2, 10, 5000, big, 1 << 40, big, big, big, 10, NULL)
+    c.max_boost = 0  # boosting not configured
+    assert lib.ctcpb_decode_offline_boosted(ctypes.byref(c), ctypes.byref(tables), *args) == D.EINVAL
+    assert lib.ctcpb_stream_set_boost(ctypes.byref(c), big, 1 << 40, 2, 5000, ctypes.byref(tables), NULL) == D.EINVAL
+    c.max_boost = 8
+    assert lib.ctcpb_decode_offline_boosted(ctypes.byref(c), ctypes.byref(no_tokens), *args) == D.ENULL
+    assert lib.ctcpb_stream_set_boost(ctypes.byref(c), big, 1 << 40, 2, 5000, NULL, NULL) == D.ENULL
+    assert lib.ctcpb_stream_set_boost(ctypes.byref(c), ctypes.c_void_p(512), 16, 2, 5000, ctypes.byref(tables),
+                                      NULL) == D.ESIZE
+
+
+def test_boost_tables_compressed_rows():
+    rp, tk, bn = D.boost_tables([{3: 1.5, 7: -2.0}, None, {1: 0.25}], 3, "cpu")
+    assert rp.tolist() == [0, 2, 2, 3]
+    assert tk.tolist() == [3, 7, 1]
+    assert bn.tolist() == [1.5, -2.0, 0.25]
+    rp, tk, bn = D.boost_tables([None, None], 2, "cpu")
+    assert rp.tolist() == [0, 0, 0] and tk.numel() == 1  # non-null arrays even when empty
+    with pytest.raises(ValueError):
+        D.boost_tables([{1: 1.0}], 2, "cpu")
