@@ -15,6 +15,7 @@
 
 #include "ctcpb_internal.cuh"
 #include "ctcpb_kernels.h"
+#include "ctcpb_sort.cuh"
 
 namespace ctcpb {
 
@@ -82,6 +83,37 @@ __device__ __forceinline__ u64 warp_max_u64(u64 v) {
     v = w > v ? w : v;
   }
   return v;
+}
+
+// Block-wide descending ranks of 2*NT keys held two per thread (0: no key;
+// the other keys are distinct).  Each warp sorts its 64 keys in registers
+// (lane l then holds places l and l + 32 of its run) and writes the run to
+// run[64 w ..]; a key's rank is its place in its own run plus, for every
+// other run, the number of keys above it there (branch-free binary search).
+// Ends with the keys in v (sorted within the warp) and their ranks in r.
+template <int NT>
+__device__ __forceinline__ void block_rank2(u64 (&v)[2], int (&r)[2], u64* run, int tid) {
+  const int lane = tid & 31, w = tid >> 5;
+  warp_sort_desc<2>(v, lane);
+  r[0] = lane;
+  r[1] = lane + 32;
+  if (NT > 32) {
+    run[64 * w + lane] = v[0];
+    run[64 * w + 32 + lane] = v[1];
+    gsync<NT>();
+#pragma unroll
+    for (int o = 1; o < NT / 32; ++o) {
+      const u64* other = run + 64 * ((w + o) % (NT / 32));
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        int c = 0;  // keys of `other` above v[e]: other is descending
+#pragma unroll
+        for (int step = 32; step >= 1; step >>= 1) c += other[c + step - 1] > v[e] ? step : 0;
+        c += other[c] > v[e] ? 1 : 0;  // all 64 above
+        r[e] += c;
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ int pow2_at_least(int n, int lo) {
@@ -747,24 +779,35 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         u64 m1 = kb > kr ? kb : kr, m2 = kb > kr ? kr : kb;
         if (ka > m1) { m2 = m1; m1 = ka; } else if (ka > m2) { m2 = ka; }
         if (kc > m1) { m2 = m1; m1 = kc; } else if (kc > m2) { m2 = kc; }
-        S.top2[2 * tid] = m1;
-        S.top2[2 * tid + 1] = m2;
         if (tid == 0) {
           S.nkeys = 0;
           S.tau = 0ull;  // every live key when fewer than beam are live
         }
-        gsync<NT>();
         // tau: the key that exactly beam-1 of the 2 nlive keys exceed (live
-        // keys are distinct: score, source, token)
-        if (tid < nlive) {
-          int r1 = 0, r2 = 0;
-          for (int j = 0; j < 2 * nlive; ++j) {
-            const u64 y = S.top2[j];
-            r1 += y > m1 ? 1 : 0;
-            r2 += y > m2 ? 1 : 0;
+        // keys are distinct: score, source, token).  Up to 128 keys each
+        // counts the keys above it; more are sorted per warp and searched.
+        if (2 * nlive <= 128) {
+          S.top2[2 * tid] = m1;
+          S.top2[2 * tid + 1] = m2;
+          gsync<NT>();
+          if (tid < nlive) {
+            int r1 = 0, r2 = 0;
+            for (int j = 0; j < 2 * nlive; ++j) {
+              const u64 y = S.top2[j];
+              r1 += y > m1 ? 1 : 0;
+              r2 += y > m2 ? 1 : 0;
+            }
+            if (m1 != 0ull && r1 == beam - 1) S.tau = m1;
+            if (m2 != 0ull && r2 == beam - 1) S.tau = m2;
           }
-          if (m1 != 0ull && r1 == beam - 1) S.tau = m1;
-          if (m2 != 0ull && r2 == beam - 1) S.tau = m2;
+        } else {
+          gsync<NT>();
+          u64 v2[2] = {m1, m2};
+          int r2[2];
+          block_rank2<NT>(v2, r2, S.top2, tid);
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (v2[e] != 0ull && r2[e] == beam - 1) S.tau = v2[e];
         }
         gsync<NT>();
         const u64 tau = S.tau;
@@ -786,7 +829,32 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         }
         gsync<NT>();
         const int nk = S.nkeys;
-        if (nk <= 4 * NT) {
+        if (nk <= NT) {
+          // the best beam in order by rank: each key counts the keys above it
+          const u64 mk = tid < nk ? keys[tid] : 0ull;
+          int mr = 0;
+          for (int j = 0; j < nk; ++j) mr += keys[j] > mk ? 1 : 0;
+          gsync<NT>();
+          if (mk != 0ull && mr < beam) keys[mr] = mk;
+          // the rest of the first NT slots holds no key (a frame scan sorts them)
+          for (int i = (nk < beam ? nk : beam) + tid; i < NT; i += NT) keys[i] = 0ull;
+          selected = true;
+        } else if (nk <= 2 * NT) {
+          // the best beam in order: block-wide ranks of the collected keys
+          u64 v2[2];
+          int r2[2];
+          const int i0 = 64 * (tid >> 5) + (tid & 31);
+          v2[0] = i0 < nk ? keys[i0] : 0ull;
+          v2[1] = i0 + 32 < nk ? keys[i0 + 32] : 0ull;
+          block_rank2<NT>(v2, r2, S.top2, tid);
+          gsync<NT>();  // every key is read before the first is placed
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (v2[e] != 0ull && r2[e] < beam) keys[r2[e]] = v2[e];
+          // the rest of the first NT slots holds no key (a frame scan sorts them)
+          for (int i = (nk < beam ? nk : beam) + tid; i < NT; i += NT) keys[i] = 0ull;
+          selected = true;
+        } else if (nk <= 4 * NT) {
           // the best beam in order by rank: each key counts the keys above it
           u64 mk[4];
           int mr[4];
