@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "ctcpb_async.cuh"
 #include "ctcpb_internal.cuh"
 #include "ctcpb_kernels.h"
 #include "ctcpb_sort.cuh"
@@ -297,9 +298,11 @@ struct StepSmem {
   float npb[NT], npnb[NT], nsc[NT];
   int nlast[NT], nlen[NT], nsrc[NT], ntok[NT];
   u64 nh[NT], nhp[NT];
-  // the frame's ranked labels
-  int ids[kMaxList + 2];
-  float lps[kMaxList + 2];
+  // the ranked-frame records of this step and the next (raw copies: header,
+  // ids, log-probs), and lp[frame][last] of every slot for those steps
+  static constexpr int kRecMax = 32 + 8 * ((kMaxList + 3) / 4 * 4);
+  alignas(16) unsigned char rec[2][kRecMax];
+  float lplf[2][NT];
   u32 excl[NT][(kMaxList + 31) / 32];
   int xu_k[NT], xu_c[NT];
   int pi[2 * NT], pj[2 * NT];
@@ -320,9 +323,8 @@ struct StepSmem {
   int uc[8 * NT];      // frame scan: unlisted labels that can reach the threshold ...
   float uv[8 * NT];    // ... and their log-probs
   u64 tau;  // the step's selection threshold
-  int cnt, front_id, nw, npairs, nxu, nkeys, ndfree, nuc;
+  int nw, npairs, nxu, nkeys, ndfree, nuc;
   int ptop, pnext;  // the row's page pool: LIFO top and bump pointer (paged)
-  float lpb, front_lp;
 };
 
 template <int NT>
@@ -602,41 +604,54 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
   }
   gsync<NT>();
 
+  // Asynchronous copies that step s waits for at its start: its record into
+  // rec[s & 1] (issued at the start of step s-1) and lp[its frame][last] of
+  // its n slots into lplf[s & 1] (issued once step s-1 has chosen them:
+  // lasts/lens are the slots' last labels and lengths).
+  const int rwords = (int)(Ly.rec_bytes >> 4);
+  auto prefetch_rec = [&](int s) {
+    const char* src = st.rec(b, s);
+    unsigned char* dst = S.rec[s & 1];
+    for (int i = tid; i < rwords; i += NT) cp_async16(dst + 16 * i, src + 16 * i);
+    cp_commit();
+  };
+  auto prefetch_lpl = [&](int s, int n, const int* lasts, const int* lens) {
+    const int srow = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
+    const float* frow = lp + (long long)b * sb + (long long)srow * stt;
+    for (int k = tid; k < n; k += NT)
+      if (lens[k] > 0) cp_async4(&S.lplf[s & 1][k], frow + lasts[k]);
+    cp_commit();
+  };
+  prefetch_rec(0);
+  prefetch_lpl(0, nlive, S.last, S.len);
+
   for (int s = 0; s < nsteps; ++s) {
     const int srow = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;  // batch or chunk row
     const int t = mode == 0 ? srow : (mode == 1 ? tcount + s : tcount + srow - tile_start);
     const float* row = lp + (long long)b * sb + (long long)srow * stt;
-    char* rec = st.rec(b, s);
-    {
-      const RecHdr* rhd = (const RecHdr*)rec;
-      const int cnt = rhd->cnt;
-      const int* rids = rec_ids(rec);
-      const float* rlps = rec_lps(rec, Ly.Lpad);
-      for (int i = tid; i < cnt; i += NT) {
-        S.ids[i] = rids[i];
-        S.lps[i] = rlps[i];
-      }
-      if (tid == 0) {
-        S.cnt = cnt;
-        S.front_id = rhd->front_id;
-        S.front_lp = rhd->front_lp;
-        S.lpb = rhd->lpb;
-      }
-    }
+    cp_wait_all();
     gsync<NT>();
+    if (s + 1 < nsteps) prefetch_rec(s + 1);  // rec[(s+1) & 1] was step s-1's, done
     BPHASE(0);
+    const unsigned char* rbuf = S.rec[s & 1];
+    const RecHdr& rhd = *reinterpret_cast<const RecHdr*>(rbuf);
+    const int* ids = reinterpret_cast<const int*>(rbuf + 32);
+    const float* lps = reinterpret_cast<const float*>(rbuf + 32 + 4 * Ly.Lpad);
+    const float* lplf = S.lplf[s & 1];
+    const float rec_lpb = rhd.lpb, front_lp = rhd.front_lp;
+    const int front_id = rhd.front_id;
     const bool gap = t > t_prev + 1;
-    const int cnt = S.cnt;
+    const int cnt = rhd.cnt;
 
     if (step == 0) {
       // ---- section 3.3: seed the top (beam-1) labels, then the empty prefix
       const int nb = beam > 1 ? beam - 1 : 1;
       const int ntok = cap >= 1 ? (nb < cnt ? nb : cnt) : 0;
-      const bool empty_live = beam > 1 && S.lpb > NEG;
+      const bool empty_live = beam > 1 && rec_lpb > NEG;
       for (int k = tid; k < beam; k += NT) {
         if (k < ntok) {
-          const int c = S.ids[k];
-          const float v = S.lps[k];
+          const int c = ids[k];
+          const float v = lps[k];
           S.npb[k] = gap ? v : NEG;
           S.npnb[k] = gap ? NEG : v;
           S.nsc[k] = v;
@@ -648,9 +663,9 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
           S.nsrc[k] = -1;
           S.nmsrc[k] = empty_live ? ntok : -1;  // l_k = empty prefix + c
         } else if (k == ntok && empty_live) {
-          S.npb[k] = S.lpb;
+          S.npb[k] = rec_lpb;
           S.npnb[k] = NEG;
-          S.nsc[k] = S.lpb;
+          S.nsc[k] = rec_lpb;
           S.nlast[k] = blank;
           S.nlen[k] = 0;
           S.nh[k] = kH0;
@@ -679,14 +694,14 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         }
         const float A = dlse(pb, pnb);
         const int L = S.len[k];
-        const float lpl = L > 0 ? rdlp(row[S.last[k]]) : NEG;
+        const float lpl = L > 0 ? rdlp(lplf[k]) : NEG;
         // the last label emitted again (the repeat path, a merge fold) carries its bonus
         const float lple = (L > 0 && bkeys) ? dadd(lpl, boost_of(bkeys, bvals, hmask, S.last[k])) : lpl;
         S.A[k] = A;
         S.pbg[k] = pb;
         S.lpl[k] = lpl;
         S.lple[k] = lple;
-        S.bpb[k] = dadd(S.lpb, A);
+        S.bpb[k] = dadd(rec_lpb, A);
         // a space-ending beam has no stay path, and its candidate (k, last)
         // extends from both paths (every space frame is a token)
         const bool spc = S.last[k] == space;
@@ -721,7 +736,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         } else {
           int p = -1;
           for (int q = 0; q < cnt; ++q)
-            if (S.ids[q] == c) {
+            if (ids[q] == c) {
               p = q;
               break;
             }
@@ -754,9 +769,9 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
       };
       auto list_key = [&](int k, int p) -> u64 {  // 0: not a candidate
         const int L = S.len[k];
-        const int c = S.ids[p];
+        const int c = ids[p];
         if (L < cap && !(L > 0 && c == S.last[k]) && !((S.excl[k][p >> 5] >> (p & 31)) & 1u)) {
-          const float sc = dadd(S.lps[p], S.A[k]);
+          const float sc = dadd(lps[p], S.A[k]);
           if (sc > NEG) return cand_key(sc, k, c);
         }
         return 0ull;
@@ -906,9 +921,9 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
             if (L > 0 && L < cap && !S.repdead[k] && S.rep[k] > NEG) key = cand_key(S.rep[k], k, S.last[k]);
           } else {
             const int p = r - 2;
-            const int c = S.ids[p];
+            const int c = ids[p];
             if (L < cap && !(L > 0 && c == S.last[k]) && !((S.excl[k][p >> 5] >> (p & 31)) & 1u)) {
-              const float sc = dadd(S.lps[p], S.A[k]);
+              const float sc = dadd(lps[p], S.A[k]);
               if (sc > NEG) key = cand_key(sc, k, c);
             }
           }
@@ -925,12 +940,12 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
 
       // ---- the list proves the selection unless an unlisted label could
       // reach the beam: then rank every unlisted label of this frame
-      if (S.front_lp > NEG) {
+      if (front_lp > NEG) {
         const u32 sstar = nw == beam ? (u32)(keys[beam - 1] >> 32) : 0u;
         bool bad = false;
         for (int k = tid; k < nlive; k += NT) {
           if (S.len[k] < cap) {
-            const float u = dadd(S.front_lp, S.A[k]);
+            const float u = dadd(front_lp, S.A[k]);
             if (u > NEG && (nw < beam || fkey(u) >= sstar)) bad = true;
           }
         }
@@ -942,7 +957,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
           // that can grow (adding is monotone), so only those labels are
           // kept and then paired with every hypothesis.
           u64 thr = nw == beam ? (keys[beam - 1] & 0xffffffff00000000ull) : 0ull;
-          const u64 kfront = lab_key(S.front_lp, S.front_id);
+          const u64 kfront = lab_key(front_lp, front_id);
           float amax = NEG;
           for (int k = 0; k < nlive; ++k)
             if (S.len[k] < cap) amax = fmaxf(amax, S.A[k]);
@@ -1101,6 +1116,8 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
       gsync<NT>();
     }
 
+    // the next step's lp[last] of the slots just chosen
+    if (s + 1 < nsteps) prefetch_lpl(s + 1, S.nw, S.nlast, S.nlen);
     BPHASE(5);
     // ---- the one merge relation the sources cannot show: a blank winner whose
     // parent prefix was just rebuilt by an extension winner (prefix hash
@@ -1292,6 +1309,8 @@ template <int NT>
 static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, long long stt, int mode,
                                  const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   const int sortcap = NT == 32 ? 1024 : 4096;
+  // records are copied whole into shared memory in 16-byte words
+  if (st.lay.rec_bytes > (size_t)StepSmem<NT>::kRecMax || (st.lay.rec_bytes & 15) != 0) return cudaErrorInvalidValue;
   const size_t smem = step_smem_bytes<NT>(sortcap);
   static bool attr_done = false;
   if (!attr_done) {

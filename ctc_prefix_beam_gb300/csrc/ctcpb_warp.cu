@@ -90,12 +90,6 @@ struct __align__(16) Tables {
 };
 static_assert(sizeof(Tables) % 16 == 0, "tables copy as 16-byte words");
 
-// 4-byte asynchronous copy global -> shared (completes at cp_wait_all)
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(saddr(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // 32-bit prefix hash (FNV-1a step).  Equal prefixes hash equal; a collision
 // only costs an extra exact comparison.
