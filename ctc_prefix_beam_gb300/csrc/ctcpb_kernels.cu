@@ -303,6 +303,11 @@ struct StepSmem {
   static constexpr int kRecMax = 32 + 8 * ((kMaxList + 3) / 4 * 4);
   alignas(16) unsigned char rec[2][kRecMax];
   float lplf[2][NT];
+  // the step's list positions by label: key (decode step + 1) << 32 | label
+  // (older steps' keys read as empty), open addressing
+  static constexpr int kLpos = 1024;  // a power of two >= 2 * list length
+  u64 lpkey[kLpos];
+  int lpval[kLpos];
   u32 excl[NT][(kMaxList + 31) / 32];
   int xu_k[NT], xu_c[NT];
   int pi[2 * NT], pj[2 * NT];
@@ -602,6 +607,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
     S.ptop = st.ptop()[b];
     S.pnext = st.pnext()[b];
   }
+  for (int i = tid; i < S.kLpos; i += NT) S.lpkey[i] = 0ull;
   gsync<NT>();
 
   // Asynchronous copies that step s waits for at its start: its record into
@@ -615,20 +621,22 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
     for (int i = tid; i < rwords; i += NT) cp_async16(dst + 16 * i, src + 16 * i);
     cp_commit();
   };
-  auto prefetch_lpl = [&](int s, int n, const int* lasts, const int* lens) {
-    const int srow = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;
+  auto prefetch_lpl = [&](int s, int srow, int n, const int* lasts, const int* lens) {
     const float* frow = lp + (long long)b * sb + (long long)srow * stt;
     for (int k = tid; k < n; k += NT)
       if (lens[k] > 0) cp_async4(&S.lplf[s & 1][k], frow + lasts[k]);
     cp_commit();
   };
+  auto srow_of = [&](int s) { return mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s; };
+  int srow_next = srow_of(0);  // the batch or chunk row of the coming step
   prefetch_rec(0);
-  prefetch_lpl(0, nlive, S.last, S.len);
+  prefetch_lpl(0, srow_next, nlive, S.last, S.len);
 
   for (int s = 0; s < nsteps; ++s) {
-    const int srow = mode != 1 ? st.sel()[(size_t)b * Ly.T_sel + s] : tile_start + s;  // batch or chunk row
+    const int srow = srow_next;  // batch or chunk row
     const int t = mode == 0 ? srow : (mode == 1 ? tcount + s : tcount + srow - tile_start);
     const float* row = lp + (long long)b * sb + (long long)srow * stt;
+    if (s + 1 < nsteps) srow_next = srow_of(s + 1);  // used at the winners: its load has time
     cp_wait_all();
     gsync<NT>();
     if (s + 1 < nsteps) prefetch_rec(s + 1);  // rec[(s+1) & 1] was step s-1's, done
@@ -708,19 +716,32 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         S.bpnb[k] = (L > 0 && !gap && !spc) ? dadd(lpl, pnb) : NEG;
         S.rep[k] = (L > 0 && L < cap) ? dadd(lple, spc ? A : pb) : NEG;
         S.repdead[k] = 0;
-        S.into[k] = -1;
+        // section 3.4.3: pairs (i shorter, j longer) with l_j = l_i + last_j,
+        // known from the merge sources tracked through the previous steps
+        S.into[k] = S.msrc[k];
         for (int w = 0; w < (kMaxList + 31) / 32; ++w) S.excl[k][w] = 0u;
+      }
+      for (int k = tid; k < NT; k += NT) S.bw[k] = -1;
+      // the list positions by label, for the folds (short lists are searched)
+      const u64 stamp = (u64)(step + 1);
+      const bool lpos = cnt > 96;
+      for (int p = tid; lpos && p < cnt; p += NT) {
+        const int c = ids[p];
+        int h = (int)(((u32)c * 0x9E3779B1u) & (u32)(S.kLpos - 1));
+        for (int n = 0; n < S.kLpos; ++n) {  // the table is at most half full
+          const u64 old = S.lpkey[h];
+          if ((old >> 32) != stamp && atomicCAS(&S.lpkey[h], old, (stamp << 32) | (u32)c) == old) {
+            S.lpval[h] = p;
+            break;
+          }
+          if ((S.lpkey[h] >> 32) == stamp) h = (h + 1) & (S.kLpos - 1);
+        }
       }
       if (tid == 0) {
         S.npairs = 0;
         S.nxu = 0;
         S.nkeys = 0;
       }
-      gsync<NT>();
-      // ---- section 3.4.3: pairs (i shorter, j longer) with l_j = l_i + last_j,
-      // known from the merge sources tracked through the previous steps
-      for (int j = tid; j < nlive; j += NT) S.into[j] = S.msrc[j];
-      for (int k = tid; k < NT; k += NT) S.bw[k] = -1;
       gsync<NT>();
       // fold (i, last_j) into j's blank slot; drop the folded candidate
       for (int j = tid; j < nlive; j += NT) {
@@ -734,12 +755,23 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         if (same) {
           S.repdead[i] = 1;
         } else {
-          int p = -1;
-          for (int q = 0; q < cnt; ++q)
-            if (ids[q] == c) {
-              p = q;
+          int p = -1;  // c's list position
+          if (!lpos) {
+            for (int q = 0; q < cnt; ++q)
+              if (ids[q] == c) {
+                p = q;
+                break;
+              }
+          }
+          for (int h = (int)(((u32)c * 0x9E3779B1u) & (u32)(S.kLpos - 1)), n = 0; lpos && n < S.kLpos;
+               h = (h + 1) & (S.kLpos - 1), ++n) {
+            const u64 k2 = S.lpkey[h];
+            if ((k2 >> 32) != stamp) break;
+            if ((u32)k2 == (u32)c) {
+              p = S.lpval[h];
               break;
             }
+          }
           if (p >= 0) {
             atomicOr(&S.excl[i][p >> 5], 1u << (p & 31));
           } else {
@@ -777,6 +809,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         return 0ull;
       };
       bool selected = false;
+      int nsel = 0;  // the winners, when the rank paths selected (keys are nonzero and distinct)
       {
         u64 kb = 0ull, kr = 0ull, ka = 0ull, kc = 0ull;
         if (tid < nlive) {
@@ -854,6 +887,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
           // the rest of the first NT slots holds no key (a frame scan sorts them)
           for (int i = (nk < beam ? nk : beam) + tid; i < NT; i += NT) keys[i] = 0ull;
           selected = true;
+          nsel = nk < beam ? nk : beam;
         } else if (nk <= 2 * NT) {
           // the best beam in order: block-wide ranks of the collected keys
           u64 v2[2];
@@ -869,6 +903,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
           // the rest of the first NT slots holds no key (a frame scan sorts them)
           for (int i = (nk < beam ? nk : beam) + tid; i < NT; i += NT) keys[i] = 0ull;
           selected = true;
+          nsel = nk < beam ? nk : beam;
         } else if (nk <= 4 * NT) {
           // the best beam in order by rank: each key counts the keys above it
           u64 mk[4];
@@ -934,8 +969,9 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         gsync<NT>();
         bitonic_desc<NT>(keys, P, tid);
       }
-      int nw = 0;
-      for (int w = 0; w < beam; ++w) nw += keys[w] != 0ull;
+      int nw = nsel;
+      if (nsel == 0)
+        for (int w = 0; w < beam; ++w) nw += keys[w] != 0ull;
       BPHASE(2);
 
       // ---- the list proves the selection unless an unlisted label could
@@ -1071,22 +1107,25 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         S.nsc[w] = score;
         S.nsrc[w] = src;
         S.ntok[w] = tk;
+        // the new slot of each source's blank winner
+        if (tk == blank) S.bw[src] = w;
+        // token store: the winner's (source, token) into the ring; the rows
+        // or pages are written at a flush
+        S.hist[s - win0][w] = ((u32)src << 24) | ((u32)tk & 0xffffffu);
+        S.norg[w] = S.org[src];
+        S.nlo[w] = S.lo[src];
+      }
+      for (int i = tid; i < 2 * NT; i += NT) {
+        S.hval[i] = -1;
+        S.hkey[i] = 0ull;
       }
       if (tid == 0) {
         S.nw = nw;
         S.ndfree = 0;
       }
       gsync<NT>();
-      // the new slot of each source's blank winner; then every winner's merge
-      // source: a blank winner keeps its source's relation, an extension of
-      // source s relates to s's blank winner
-      for (int w = tid; w < nw; w += NT)
-        if (S.ntok[w] == blank) S.bw[S.nsrc[w]] = w;
-      for (int i = tid; i < 2 * NT; i += NT) {
-        S.hval[i] = -1;
-        S.hkey[i] = 0ull;
-      }
-      gsync<NT>();
+      // every winner's merge source: a blank winner keeps its source's
+      // relation, an extension of source s relates to s's blank winner
       for (int w = tid; w < nw; w += NT) {
         const int src = S.nsrc[w];
         S.nmsrc[w] = S.ntok[w] == blank ? (S.msrc[src] >= 0 ? S.bw[S.msrc[src]] : -1) : S.bw[src];
@@ -1104,20 +1143,10 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
       if (tid == 0) S.npairs = 0;
       gsync<NT>();
       BPHASE(4);
-
-      // ---- token store: the winners' (source, token) into the ring; the
-      // rows or pages are written at a flush
-      for (int w = tid; w < nw; w += NT) {
-        const int src = S.nsrc[w];
-        S.hist[s - win0][w] = ((u32)src << 24) | ((u32)S.ntok[w] & 0xffffffu);
-        S.norg[w] = S.org[src];
-        S.nlo[w] = S.lo[src];
-      }
-      gsync<NT>();
     }
 
     // the next step's lp[last] of the slots just chosen
-    if (s + 1 < nsteps) prefetch_lpl(s + 1, S.nw, S.nlast, S.nlen);
+    if (s + 1 < nsteps) prefetch_lpl(s + 1, srow_next, S.nw, S.nlast, S.nlen);
     BPHASE(5);
     // ---- the one merge relation the sources cannot show: a blank winner whose
     // parent prefix was just rebuilt by an extension winner (prefix hash
