@@ -232,10 +232,11 @@ def run_stream(a, w, torch, D, dev):
     offsets = synth.stream_offsets(w)
     nt = synth.n_ticks(w, offsets)
     cache = {}
-    ticks = []
+    ticks, host_ticks = [], []
     for k in range(nt):
         c, nf = synth.stream_tick(w, k, offsets, cache, threads=os.cpu_count() or 8)
         ticks.append((torch.from_numpy(c).to(dev), torch.from_numpy(nf).to(dev)))
+        host_ticks.append((torch.from_numpy(c).pin_memory(), torch.from_numpy(nf).pin_memory()))
     cache.clear()
     cfg = D.Config(beam=w.beam, nbest=w.nbest, blank_id=w.blank_id, max_seq_len=w.max_seq_len)
     st = D.StreamState(cfg, w.B, w.V, device=dev)
@@ -260,6 +261,67 @@ def run_stream(a, w, torch, D, dev):
             torch.cuda.synchronize(dev)
             ts.append(e0.elapsed_time(e1))
     ms = statistics.mean(ts)
+
+    # end to end: every tick's chunk and frame counts copied from page-locked
+    # host memory (a copy stream runs one tick ahead of the decode, two device
+    # buffers), the N-best read back to host at the end of the session
+    cs = torch.cuda.Stream(dev)
+    bufs = [(torch.empty_like(ticks[0][0]), torch.empty_like(ticks[0][1])) for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    used = [torch.cuda.Event() for _ in range(2)]
+    out_len = w.max_seq_len if w.max_seq_len > 0 else 4096
+    c0 = cfg.c()
+    res_host = (torch.empty((w.B, c0.nbest, out_len), dtype=torch.int32).pin_memory(),
+                torch.empty((w.B, c0.nbest), dtype=torch.int32).pin_memory(),
+                torch.empty((w.B, c0.nbest), dtype=torch.float32).pin_memory())
+    res_dev = tuple(torch.empty(r.shape, dtype=r.dtype, device=dev) for r in res_host)
+
+    def session_host():
+        st.init()
+        for k, (hc, hn) in enumerate(host_ticks):
+            j = k % 2
+            with torch.cuda.stream(cs):
+                cs.wait_event(used[j])
+                bufs[j][0].copy_(hc, non_blocking=True)
+                bufs[j][1].copy_(hn, non_blocking=True)
+                copied[j].record(cs)
+            stream.wait_event(copied[j])
+            st.step_chunk(bufs[j][0], bufs[j][1])
+            used[j].record(stream)
+        st.read(out_len=out_len, outputs=res_dev)
+        for rh, rd in zip(res_host, res_dev):
+            rh.copy_(rd, non_blocking=True)
+
+    for _ in range(2):
+        session_host()
+    torch.cuda.synchronize(dev)
+    te = []
+    for _ in range(a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        session_host()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        te.append(e0.elapsed_time(e1))
+    e2e_ms = statistics.mean(te)
+    h2d = sum(hc.numel() * 4 + hn.numel() * 4 for hc, hn in host_ticks)
+    d2h = sum(r.numel() * r.element_size() for r in res_host)
+
+    # the oracle on the host cores: a bounded sample of whole streams decoded offline
+    cpu = None
+    if not a.no_cpu_baseline:
+        import oracle as O
+        O.lib()
+        ns = min(w.B, 16)
+        lp_s = np.stack([synth.gen_stream(w, i) for i in range(ns)])
+        cores = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        O.decode(lp_s, None, beam=w.beam, nbest=w.nbest, blank=w.blank_id,
+                 cap=w.max_seq_len if w.max_seq_len > 0 else 4096, threads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": ns * w.T / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
+               "sample": f"{ns} whole streams of {w.T} frames decoded offline, {cores} threads, {dt:.2f} s"}
+
     frames = w.B * w.T
     tick_bytes = w.B * w.chunk * w.V * 4
     gbs = nt * tick_bytes / (ms / 1e3) / 1e9
@@ -274,6 +336,9 @@ def run_stream(a, w, torch, D, dev):
         "ms_per_tick": ms / nt, "fused": fused,
         "roofline": {"kernel": "k_fused" if fused else "k_step_warp", "bound": "hbm", "achieved": gbs, "peak": peak,
                      "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_kind": peak_kind},
+        "e2e": {"value": frames / (e2e_ms / 1e3), "unit": "frames/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "cpu_baseline": cpu,
         "gpu_launches": a.steps * (1 + nt),
         "clocks": clk.summary(),
     }), flush=True)
@@ -384,20 +449,27 @@ def main():
             sp["steps"].append(ev[1].elapsed_time(ev[2]))
         split_ms = {k: statistics.mean(v) for k, v in sp.items()}
 
-    # end to end through the public call with host buffers
+    # end to end through the public host-buffer call (ctcpb_decode_offline_host):
+    # every step copies the valid frames and the lengths from page-locked host
+    # memory (in chunks, overlapped with the decode) and the N-best back
     out_host = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs)
-    h2d = lp_host.numel() * 4 + lens_host.numel() * 4
+    ws_host = torch.empty(D.host_workspace_size(cfg, Bn, T, V, out_len), dtype=torch.uint8, device=dev)
+    h2d = int(np.clip(lens_np, 0, T).sum()) * V * 4 + lens_host.numel() * 4
     d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def decode_host():
+        D.decode_offline_host(cfg, lp_host, lens_host, workspace=ws_host, out_len=out_len, outputs=out_host,
+                              device=dev, synchronize=False)
+
+    for _ in range(2):
+        decode_host()
+    torch.cuda.synchronize(dev)
     e2e_ms = []
     for i in range(a.steps):
         flush.fill_(1.0)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        lp.copy_(lp_host, non_blocking=True)
-        lens.copy_(lens_host, non_blocking=True)
-        decode()
-        for oh, od in zip(out_host, outs):
-            oh.copy_(od, non_blocking=True)
+        decode_host()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms.append(e0.elapsed_time(e1))

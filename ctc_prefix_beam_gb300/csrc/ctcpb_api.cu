@@ -1,8 +1,11 @@
 // C ABI of the decoder (include/ctcpb.h): argument validation on the host,
 // workspace/state layout, and the launch sequence of each call.
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
+#include <vector>
 
 #include "ctcpb.h"
 #include "ctcpb_internal.cuh"
@@ -334,6 +337,201 @@ int ctcpb_topk_prepass(const ctcpb_config* cfg, const float* log_prob, int64_t s
   const int L = default_list_len(cfg->beam, V, cfg->list_len);
   return cuda_rc(launch_prepass_rows(log_prob, stride_r, R, V, cfg->blank_id, L, ids, lps, cnt, lpb, front_lp,
                                      front_id, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ host-buffer offline decode
+namespace {
+
+constexpr size_t kHostSegment = 1u << 20;  // bytes of a row a chunk copies at least: host-to-device
+                                           // copies run at full speed from about 1 MB per segment
+constexpr int kHostBufs = 3;             // chunk buffers in the workspace
+constexpr int kCopyStreams = 1;          // chunks arrive in order (the copy bandwidth is shared, not added)
+
+// Workspace of ctcpb_decode_offline_host: a decode state with streaming tiles
+// and the offline cap, the row lengths, the per-chunk frame counts, the chunk
+// buffers [kHostBufs][B][F][V] and the device outputs.
+struct HostLayout {
+  Layout st;
+  int F, nchunks;
+  size_t o_lens, o_plan, o_buf, buf_elems, o_tok, o_len, o_sc, total;
+};
+
+HostLayout host_layout(const ctcpb_config* c, int B, int T, int V, int out_len) {
+  HostLayout h{};
+  h.st = make_layout(B, V, c->beam, offline_cap(c, T), c->paged, c->paged ? c->page_size : 16, c->blank_id,
+                     default_list_len(c->beam, V, c->list_len), kStreamTile, kStreamTile, space_of(c),
+                     c->max_boost);
+  // frames per chunk: whole streaming tiles covering >= kHostSegment bytes of a row
+  const size_t row_bytes = 4 * (size_t)V;
+  int F = (int)((kHostSegment + row_bytes - 1) / row_bytes);
+  F = (F + kStreamTile - 1) / kStreamTile * kStreamTile;
+  h.F = T < F ? (T > 0 ? T : 1) : F;
+  h.nchunks = T > 0 ? (T + h.F - 1) / h.F : 0;
+  size_t off = h.st.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = align_up(off, 256);
+    off = at + bytes;
+    return at;
+  };
+  const size_t nb = (size_t)B * c->nbest;
+  h.o_lens = take(4 * (size_t)B);
+  h.o_plan = take(4 * (size_t)B * (size_t)(h.nchunks > 0 ? h.nchunks : 1));
+  h.buf_elems = (size_t)B * h.F * V;
+  h.o_buf = take(4 * h.buf_elems * kHostBufs);
+  h.o_tok = take(4 * nb * (size_t)(out_len > 0 ? out_len : 0));
+  h.o_len = take(4 * nb);
+  h.o_sc = take(4 * nb);
+  h.total = align_up(off, 256);
+  return h;
+}
+
+// The copy streams and the events that order them against the decode, one
+// set per device, made on first use and kept for the process.
+struct HostRes {
+  cudaStream_t cs[kCopyStreams];
+  cudaEvent_t start, lens, ready[kHostBufs], done[kHostBufs];
+};
+
+std::mutex g_host_mu;
+
+HostRes* host_res(int dev) {
+  static HostRes res[64];
+  static bool made[64];
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!made[dev]) {
+    HostRes& r = res[dev];
+    const unsigned ef = cudaEventDisableTiming;
+    bool ok = true;
+    for (int i = 0; i < kCopyStreams; ++i) ok = ok && cudaStreamCreateWithFlags(&r.cs[i], cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&r.start, ef) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&r.lens, ef) == cudaSuccess;
+    for (int i = 0; i < kHostBufs; ++i) {
+      ok = ok && cudaEventCreateWithFlags(&r.ready[i], ef) == cudaSuccess;
+      ok = ok && cudaEventCreateWithFlags(&r.done[i], ef) == cudaSuccess;
+    }
+    if (!ok) return nullptr;
+    made[dev] = true;
+  }
+  return &res[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int ctcpb_host_workspace_size(const ctcpb_config* cfg, int B, int T, int V, int out_len, size_t* bytes) {
+  int rc = check_cfg(cfg, V);
+  if (rc) return rc;
+  if (!bytes) return CTCPB_ENULL;
+  if (B < 0 || T < 0 || out_len < 0) return CTCPB_EINVAL;
+  *bytes = host_layout(cfg, B, T, V, out_len).total;
+  return CTCPB_OK;
+}
+
+// The frames go to the device chunk by chunk on the copy streams; `stream`
+// decodes chunk c (the streaming tile path, every frame or the frames the
+// blank threshold keeps) once its copies are done, and chunk c's buffer is
+// copied into again only after that decode.  Row b's chunk c holds its frames
+// [cF, cF + F) that are below len_b; the others are never read.
+int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                              const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                              int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                              ctcpb_stream_t stream) {
+  int rc = check_cfg(cfg, V);
+  if (rc) return rc;
+  if (B < 0 || T < 0 || out_len < 0) return CTCPB_EINVAL;
+  if (B == 0) return CTCPB_OK;
+  if (T > 0 && (stride_t < V || stride_b < V)) return CTCPB_EINVAL;
+  if ((T > 0 && !log_prob) || !out_lengths || !out_scores || (out_len > 0 && !out_tokens)) return CTCPB_ENULL;
+  const HostLayout hl = host_layout(cfg, B, T, V, out_len);
+  if ((rc = check_buf(ws, ws_bytes, hl.total))) return rc;
+  int dev = 0;
+  TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostRes* R = host_res(dev);
+  if (!R) return CTCPB_ECUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* base = (char*)ws;
+  View st{base, hl.st};
+  int* lens_d = (int*)(base + hl.o_lens);
+  int* plan = (int*)(base + hl.o_plan);
+  float* bufs = (float*)(base + hl.o_buf);
+  int* tok_d = (int*)(base + hl.o_tok);
+  int* len_d = (int*)(base + hl.o_len);
+  float* sc_d = (float*)(base + hl.o_sc);
+  const int F = hl.F;
+  std::vector<int> len_h(B);
+  for (int b = 0; b < B; ++b) {
+    const int L = seq_lengths ? seq_lengths[b] : T;
+    len_h[b] = L < 0 ? 0 : (L > T ? T : L);
+  }
+  auto frames = [&](int b, int c0) {
+    const int f = len_h[b] - c0;
+    return f < 0 ? 0 : (f > F ? F : f);
+  };
+
+  // the copies start after the caller's earlier work on `stream`
+  TRY(cudaEventRecord(R->start, s));
+  for (int i = 0; i < kCopyStreams; ++i) TRY(cudaStreamWaitEvent(R->cs[i], R->start, 0));
+  if (seq_lengths) {
+    TRY(cudaMemcpyAsync(lens_d, seq_lengths, 4 * (size_t)B, cudaMemcpyHostToDevice, R->cs[0]));
+    TRY(cudaEventRecord(R->lens, R->cs[0]));
+    TRY(cudaStreamWaitEvent(s, R->lens, 0));
+  }
+  TRY(launch_host_plan(seq_lengths ? lens_d : nullptr, B, T, F, hl.nchunks, plan, s));
+  TRY(launch_init(st, s));
+
+  const float thr = cfg->blank_threshold;
+  // every frame (mode 1), or the frames the threshold keeps (mode 2; thr <= 0 keeps none)
+  const bool all = thr >= 1.0f;
+  const float log_thr = thr > 0.0f ? (float)std::log((double)thr) : -FLT_MAX;
+  const long long dsb = (long long)F * V;  // chunk buffer [B][F][V]
+  const bool merge = stride_t == V && stride_b >= dsb;
+  for (int c = 0; c < hl.nchunks; ++c) {
+    const int k = c % kHostBufs, c0 = c * F;
+    cudaStream_t cs = R->cs[c % kCopyStreams];
+    float* buf = bufs + (size_t)k * hl.buf_elems;
+    TRY(cudaStreamWaitEvent(cs, R->done[k], 0));  // the buffer's previous chunk is decoded
+    for (int b = 0; b < B;) {
+      const int n = frames(b, c0);
+      if (n == 0) {
+        ++b;
+        continue;
+      }
+      const float* src = log_prob + (size_t)b * (size_t)stride_b + (size_t)c0 * (size_t)stride_t;
+      if (n == F && merge) {  // a run of rows whose whole chunk is valid: one copy
+        int e = b + 1;
+        while (e < B && frames(e, c0) == F) ++e;
+        TRY(cudaMemcpy2DAsync(buf + (size_t)b * dsb, (size_t)dsb * 4, src, (size_t)stride_b * 4, (size_t)dsb * 4,
+                              (size_t)(e - b), cudaMemcpyHostToDevice, cs));
+        b = e;
+      } else {
+        TRY(cudaMemcpy2DAsync(buf + (size_t)b * dsb, (size_t)V * 4, src, (size_t)stride_t * 4, (size_t)V * 4,
+                              (size_t)n, cudaMemcpyHostToDevice, cs));
+        ++b;
+      }
+    }
+    TRY(cudaEventRecord(R->ready[k], cs));
+    TRY(cudaStreamWaitEvent(s, R->ready[k], 0));
+    const int* nf = plan + (size_t)c * B;
+    const int mode = all ? 1 : 2;
+    for (int t0 = 0; t0 < F; t0 += kStreamTile) {  // the chunk's streaming tiles
+      const int tl = F - t0 < kStreamTile ? F - t0 : kStreamTile;
+      if (!all) TRY(launch_select_tile_thr(st, buf, dsb, V, log_thr, nf, F, t0, tl, s));
+      if (try_fused(st, buf, dsb, V, mode, nf, F, t0, tl, s)) continue;
+      TRY(launch_prepass(st, buf, dsb, V, mode, nf, F, t0, tl, s));
+      TRY(launch_step(st, buf, dsb, V, mode, nf, F, t0, tl, s));
+    }
+    TRY(cudaEventRecord(R->done[k], s));
+  }
+  TRY(launch_output(st, cfg->nbest, tok_d, len_d, sc_d, out_len, s));
+  const size_t nb = (size_t)B * cfg->nbest;
+  TRY(cudaMemcpyAsync(out_lengths, len_d, 4 * nb, cudaMemcpyDeviceToHost, s));
+  TRY(cudaMemcpyAsync(out_scores, sc_d, 4 * nb, cudaMemcpyDeviceToHost, s));
+  if (out_len > 0) TRY(cudaMemcpyAsync(out_tokens, tok_d, 4 * nb * (size_t)out_len, cudaMemcpyDeviceToHost, s));
+  return CTCPB_OK;
 }
 
 }  // extern "C"

@@ -216,6 +216,20 @@ __global__ void __launch_bounds__(64) k_boost_build(View st, const int* __restri
   if (bad) set_status(st, CTCPB_DEV_BOOST);
 }
 
+// ------------------------------------------------------------------ host-buffer decode plan
+// plan[c * B + b] = the frames of row b in chunk c (chunks of F frames):
+// clamp(len_b - c F, 0, F), len_b = clamp(lens[b], 0, T) (T when lens is null).
+__global__ void k_host_plan(const int* __restrict__ lens, int B, int T, int F, int nchunks, int* __restrict__ plan) {
+  const long long n = (long long)nchunks * B;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i / B), b = (int)(i - (long long)c * B);
+    int L = lens ? lens[b] : T;
+    L = L < 0 ? 0 : (L > T ? T : L);
+    int f = L - c * F;
+    plan[i] = f < 0 ? 0 : (f > F ? F : f);
+  }
+}
+
 // ------------------------------------------------------------------ select
 // Section 3.5: keep t < len_b iff lp[b,t,blank] < log_thr (mode 1), all
 // frames (mode 0) or none (mode 2); ordered compaction with warp ballots.
@@ -261,9 +275,12 @@ __global__ void __launch_bounds__(256) k_select(View st, const float* __restrict
 // Speech-masked streaming: the chunk rows of tile [tile_start, tile_start +
 // tile_len) that stream b decodes (mask != 0), in order, into sel/nsel.  One
 // warp per stream.
+// Without a mask the rows are kept by the blank threshold of section 3.5
+// instead: lp[b, j, blank] < log_thr, read from the chunk (lp, sb, stt).
 __global__ void __launch_bounds__(32) k_select_tile(View st, const uint8_t* __restrict__ mask, long long mstride,
-                                                    const int* __restrict__ nframes, int chunk_T, int tile_start,
-                                                    int tile_len) {
+                                                    const float* __restrict__ lp, long long sb, long long stt,
+                                                    float log_thr, const int* __restrict__ nframes, int chunk_T,
+                                                    int tile_start, int tile_len) {
   const int b = blockIdx.x, lane = threadIdx.x;
   int nf = nframes ? nframes[b] : chunk_T;
   nf = nf < 0 ? 0 : (nf > chunk_T ? chunk_T : nf);
@@ -272,7 +289,10 @@ __global__ void __launch_bounds__(32) k_select_tile(View st, const uint8_t* __re
   int n = 0;
   for (int j0 = tile_start; j0 < end; j0 += 32) {
     const int j = j0 + lane;
-    const bool keep = j < end && mask[(long long)b * mstride + j] != 0;
+    bool keep = false;
+    if (j < end)
+      keep = mask ? mask[(long long)b * mstride + j] != 0
+                  : rdlp(lp[(long long)b * sb + (long long)j * stt + st.lay.blank]) < log_thr;
     const unsigned m = __ballot_sync(FULL, keep);
     if (keep) sel[n + __popc(m & ((1u << lane) - 1u))] = j;
     n += __popc(m);
@@ -1363,7 +1383,24 @@ cudaError_t launch_step(const View& st, const float* lp, long long sb, long long
 cudaError_t launch_select_tile(const View& st, const uint8_t* mask, long long mstride, const int* nframes,
                                int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (st.lay.B == 0) return cudaSuccess;
-  k_select_tile<<<st.lay.B, 32, 0, s>>>(st, mask, mstride, nframes, chunk_T, tile_start, tile_len);
+  k_select_tile<<<st.lay.B, 32, 0, s>>>(st, mask, mstride, nullptr, 0, 0, 0.0f, nframes, chunk_T, tile_start,
+                                        tile_len);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_tile_thr(const View& st, const float* lp, long long sb, long long stt, float log_thr,
+                                   const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+  if (st.lay.B == 0) return cudaSuccess;
+  k_select_tile<<<st.lay.B, 32, 0, s>>>(st, nullptr, 0, lp, sb, stt, log_thr, nframes, chunk_T, tile_start,
+                                        tile_len);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_host_plan(const int* lens, int B, int T, int F, int nchunks, int* plan, cudaStream_t s) {
+  const long long n = (long long)nchunks * B;
+  if (n == 0) return cudaSuccess;
+  const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  k_host_plan<<<blocks, 256, 0, s>>>(lens, B, T, F, nchunks, plan);
   return cudaGetLastError();
 }
 

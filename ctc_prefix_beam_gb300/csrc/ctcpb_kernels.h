@@ -12,6 +12,11 @@ cudaError_t launch_boost_build(const View& st, const int* row_ptr, const int* to
 // Speech-masked streaming: the tile's selected chunk rows per stream.
 cudaError_t launch_select_tile(const View& st, const uint8_t* mask, long long mstride, const int* nframes,
                                int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+// The same selection by the blank threshold (lp[b, j, blank] < log_thr, section 3.5) of the chunk.
+cudaError_t launch_select_tile_thr(const View& st, const float* lp, long long sb, long long stt, float log_thr,
+                                   const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s);
+// Frames of each row in each chunk of F frames, for the host-buffer decode: plan [nchunks][B].
+cudaError_t launch_host_plan(const int* lens, int B, int T, int F, int nchunks, int* plan, cudaStream_t s);
 cudaError_t launch_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
                           int mode, float log_thr, int* sel, int* nsel, cudaStream_t s);
 cudaError_t launch_prepass(const View& st, const float* lp, long long sb, long long stt, int mode,

@@ -88,6 +88,8 @@ def lib():
                 "ctcpb_decode_offline_boosted": (I, [cfgp, ctypes.POINTER(_Boost), P, I64, I64, P, I, I, I, P, SZ,
                                                      P, P, P, I, P]),
                 "ctcpb_stream_set_boost": (I, [cfgp, P, SZ, I, I, ctypes.POINTER(_Boost), P]),
+                "ctcpb_host_workspace_size": (I, [cfgp, I, I, I, I, ctypes.POINTER(SZ)]),
+                "ctcpb_decode_offline_host": (I, [cfgp, P, I64, I64, P, I, I, I, P, SZ, P, P, P, I, P]),
                 "ctcpb_state_size": (I, [cfgp, I, I, ctypes.POINTER(SZ)]),
                 "ctcpb_stream_init": (I, [cfgp, P, SZ, I, I, P]),
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
@@ -242,6 +244,50 @@ def decode_offline(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[to
                                                _ptr(tok), _ptr(ln), _ptr(sc), out_len, stages,
                                                _stream(lp.device))
     _check(rc, "decode_offline")
+    return tok, ln, sc
+
+
+def host_workspace_size(cfg: Config, B: int, T: int, V: int, out_len: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().ctcpb_host_workspace_size(ctypes.byref(cfg.c()), B, T, V, out_len, ctypes.byref(n)),
+           "host_workspace_size")
+    return n.value
+
+
+def decode_offline_host(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None, *,
+                        workspace: Optional[torch.Tensor] = None, out_len: Optional[int] = None, outputs=None,
+                        device="cuda", synchronize: bool = True):
+    """Offline decode of a HOST float32 [B, T, V] batch into host outputs
+    (``ctcpb_decode_offline_host``): the frames are copied in chunks while the
+    decode runs.  Page-locked tensors (``pin_memory()``) keep the call
+    asynchronous; the outputs are valid once the device's current stream is
+    synchronised, which this function does unless ``synchronize`` is False."""
+    if log_prob.dtype != torch.float32 or log_prob.dim() != 3 or log_prob.is_cuda or log_prob.stride(2) != 1:
+        raise ValueError("log_prob must be a host float32 tensor [B, T, V] with V contiguous")
+    B, T, V = log_prob.shape
+    c = cfg.c()
+    if out_len is None:
+        out_len = min(cfg.max_seq_len, T) if cfg.max_seq_len > 0 else T
+    if seq_lengths is not None:
+        if seq_lengths.dtype != torch.int32 or seq_lengths.is_cuda:
+            raise ValueError("seq_lengths must be a host int32 tensor [B]")
+        seq_lengths = seq_lengths.contiguous()
+    dev = torch.device(device)
+    need = host_workspace_size(cfg, B, T, V, out_len)
+    if workspace is None:
+        workspace = _alloc(need, dev)
+    if outputs is None:
+        pin = log_prob.is_pinned()
+        outputs = (torch.empty((B, c.nbest, out_len), dtype=torch.int32, pin_memory=pin),
+                   torch.empty((B, c.nbest), dtype=torch.int32, pin_memory=pin),
+                   torch.empty((B, c.nbest), dtype=torch.float32, pin_memory=pin))
+    tok, ln, sc = outputs
+    _check(lib().ctcpb_decode_offline_host(ctypes.byref(c), _ptr(log_prob), log_prob.stride(0), log_prob.stride(1),
+                                           _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
+                                           _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev)),
+           "decode_offline_host")
+    if synchronize:
+        torch.cuda.current_stream(dev).synchronize()
     return tok, ln, sc
 
 

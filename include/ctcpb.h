@@ -187,6 +187,35 @@ int ctcpb_decode_offline_boosted(const ctcpb_config* cfg, const ctcpb_boost* boo
                                  float* out_scores, int out_len, ctcpb_stream_t stream);
 
 /*
+ * Offline decode of a batch that lives in HOST memory, results written to
+ * host memory: the only call of this header whose data pointers are host
+ * pointers (the workspace is device memory, as everywhere).  The frames go
+ * to the device in chunks (whole 64-frame tiles, at least 1 MB of each row)
+ * on the library's own copy stream (valid frames only: row b's first
+ * seq_lengths[b]), while `stream` decodes every chunk already there; the
+ * results come back on `stream`.  The output
+ * is exactly ctcpb_decode_offline's on the same frames.
+ *   log_prob      host [B, T, V] float32, element strides stride_b, stride_t.
+ *   seq_lengths   host [B] int32, or NULL (T for every row).
+ *   ws, ws_bytes  DEVICE workspace of ctcpb_host_workspace_size() bytes
+ *                 (its size depends on out_len).
+ *   out_tokens / out_lengths / out_scores   host, the layout of
+ *                 ctcpb_decode_offline.
+ * Asynchrony: with page-locked log_prob, seq_lengths and outputs the call
+ * returns once everything is enqueued and completes on `stream` (synchronise
+ * it before reading the outputs); pageable buffers make CUDA stage the copies
+ * and the call may block.  The host buffers must stay valid until `stream`
+ * completes.  Calls are serialised on each device (a lock guards the copy
+ * stream and its events).
+ */
+int ctcpb_host_workspace_size(const ctcpb_config* cfg, int B, int T, int V, int out_len, size_t* bytes);
+int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                              const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                              int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                              ctcpb_stream_t stream);
+
+/*
+ * Offline decode for callers that cannot allocate device memory./*
  * Offline decode for callers that cannot allocate device memory.  The pages
  * have no counterpart: it exists for code that may not call cudaMalloc (inside
  * a stream capture that must stay allocation-free, in an engine plugin whose

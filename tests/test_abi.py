@@ -154,3 +154,25 @@ def test_boost_tables_compressed_rows():
     assert rp.tolist() == [0, 0, 0] and tk.numel() == 1  # non-null arrays even when empty
     with pytest.raises(ValueError):
         D.boost_tables([{1: 1.0}], 2, "cpu")
+
+
+def test_host_decode_sizes_and_validation(lib):
+    c = cfg()
+    a = D.host_workspace_size(c, 4, 200, 5000, 10)
+    b = D.host_workspace_size(c, 4, 200, 5000, 200)
+    assert 0 < a < b and a % 256 == 0
+    NULL = None
+    cc = c.c()
+    big = ctypes.c_void_p(1 << 20)
+    outs = (big, big, big, 10, NULL)
+    # B = 0 is a no-op; a null input, a bad stride, a small workspace
+    assert lib.ctcpb_decode_offline_host(ctypes.byref(cc), NULL, 5000, 5000, NULL, 0, 10, 5000, NULL, 0,
+                                         *outs) == D.OK
+    assert lib.ctcpb_decode_offline_host(ctypes.byref(cc), NULL, 50000, 5000, NULL, 2, 10, 5000, big, 1 << 40,
+                                         *outs) == D.ENULL
+    assert lib.ctcpb_decode_offline_host(ctypes.byref(cc), big, 50000, 10, NULL, 2, 10, 5000, big, 1 << 40,
+                                         *outs) == D.EINVAL
+    assert lib.ctcpb_decode_offline_host(ctypes.byref(cc), big, 50000, 5000, NULL, 2, 10, 5000,
+                                         ctypes.c_void_p(512), 1024, *outs) == D.ESIZE
+    assert lib.ctcpb_decode_offline_host(ctypes.byref(cc), big, 50000, 5000, NULL, 2, 10, 5000,
+                                         ctypes.c_void_p(260), 1 << 40, *outs) == D.EALIGN

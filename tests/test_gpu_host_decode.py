@@ -1,0 +1,97 @@
+"""ctcpb_decode_offline_host (host input and outputs, chunked copies overlapped
+with the decode) against ctcpb_decode_offline and the oracle, element by
+element: tokens, lengths and scores bit-identical."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from ctc_prefix_beam_gb300 import decoder as D
+from ctc_prefix_beam_gb300 import synth
+from gpu_util import assert_same, cfg_of, gpu_offline, oracle_offline
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from ctc_prefix_beam_gb300 import build
+    build.build()
+    D.lib()
+    O.lib()
+    assert torch.cuda.is_available()
+
+
+def host_decode(cfg, lp, lens, pinned=True, out_len=None):
+    x = torch.from_numpy(np.ascontiguousarray(lp))
+    ln = None if lens is None else torch.from_numpy(np.ascontiguousarray(lens, np.int32))
+    if pinned:
+        x = x.pin_memory()
+        ln = None if ln is None else ln.pin_memory()
+    out = D.decode_offline_host(cfg, x, ln, out_len=out_len)
+    return tuple(o.numpy() for o in out)
+
+
+CASES = [
+    ("bpe", dict(B=6, T=200), {}),                                  # warp kernel, fused tiles
+    ("bpe", dict(B=5, T=150), dict(beam=24, nbest=24)),             # block kernel
+    ("char", dict(B=3, T=150), {}),                                 # paged, V % 4 != 0: plain pre-pass
+    ("char", dict(B=3, T=130), dict(paged=False, beam=20, nbest=5)),
+    ("skip", dict(B=8, T=300), {}),                                 # threshold 0.999
+    ("skip", dict(B=6, T=200), dict(blank_threshold=0.5)),
+    ("skip", dict(B=4, T=100), dict(blank_threshold=0.0)),          # no frame kept
+    ("tiny", {}, {}),                                               # T = 50 < one chunk
+]
+
+
+@pytest.mark.parametrize("name,shape,over", CASES)
+def test_host_decode_equals_device_decode_and_oracle(name, shape, over):
+    w = synth.workload(name, **shape)
+    lp, lens = synth.gen_batch(w)
+    cfg = cfg_of(w, **over)
+    h = host_decode(cfg, lp, lens)
+    assert_same(h, gpu_offline(cfg, lp, lens), f"{name}{shape}{over} vs device")
+    assert_same(h, oracle_offline(cfg, lp, lens), f"{name}{shape}{over} vs oracle")
+
+
+def test_pageable_buffers_no_lengths_and_short_output():
+    w = synth.workload("bpe", B=4, T=140)
+    lp, _ = synth.gen_batch(w)
+    cfg = cfg_of(w, beam=10, nbest=3)
+    h = host_decode(cfg, lp, None, pinned=False, out_len=7)
+    assert_same(h, oracle_offline(cfg, lp, None, out_len=7), "pageable")
+
+
+def test_lengths_zero_one_and_full():
+    w = synth.workload("bpe", B=5, T=130)
+    lp, _ = synth.gen_batch(w)
+    lens = np.array([0, 1, 64, 65, 130], np.int32)  # chunk edges at 64 and 128
+    cfg = cfg_of(w)
+    assert_same(host_decode(cfg, lp, lens), oracle_offline(cfg, lp, lens), "lengths")
+
+
+def test_strided_host_rows():
+    w = synth.workload("bpe", B=3, T=100)
+    lp, lens = synth.gen_batch(w)
+    B, T, V = lp.shape
+    big = np.full((B, T, V + 12), np.nan, np.float32)
+    big[:, :, :V] = lp
+    x = torch.from_numpy(big).pin_memory()[:, :, :V]  # stride_t = V + 12
+    cfg = cfg_of(w)
+    out = D.decode_offline_host(cfg, x, torch.from_numpy(lens).pin_memory())
+    assert_same(tuple(o.numpy() for o in out), oracle_offline(cfg, lp, lens), "strided")
+
+
+def test_repeated_calls_share_the_workspace():
+    w = synth.workload("bpe", B=4, T=260)
+    lp, lens = synth.gen_batch(w)
+    cfg = cfg_of(w)
+    B, T, V = lp.shape
+    ws = torch.empty(D.host_workspace_size(cfg, B, T, V, T), dtype=torch.uint8, device="cuda")
+    x = torch.from_numpy(lp).pin_memory()
+    ln = torch.from_numpy(lens).pin_memory()
+    ref = oracle_offline(cfg, lp, lens)
+    outs = [D.decode_offline_host(cfg, x, ln, workspace=ws, synchronize=False) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert_same(tuple(t.numpy() for t in o), ref, "repeat")
