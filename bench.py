@@ -144,14 +144,15 @@ def algorithmic_bytes(w, lp, lens, kept, L):
     return dict(rank=rank, select=select, steps=steps, decode=n_kept * 4 * V + select + state)
 
 
-def traffic_record(kernel: str):
-    """ncu DRAM bytes per launch from profiles/traffic.json when it matches the current sources."""
+def traffic_record(kernel: str, workload: str):
+    """ncu DRAM bytes per launch of ``kernel`` on ``workload`` from profiles/traffic.json, when the
+    record was taken on the current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         d = json.load(open(path))
-        rec = d.get(kernel)
+        rec = d.get(f"{kernel}/{workload}")
         if rec and rec.get("sources_sha") == sources_sha():
             return rec.get("bytes_per_launch")
     except Exception:
@@ -409,7 +410,7 @@ def main():
                                                                           ("steps", D.STAGE_STEPS)]
     stages = [("init", D.STAGE_INIT), ("select", D.STAGE_SELECT)] + core + [("output", D.STAGE_OUTPUT)]
     warp_path = w.beam <= 16 and not w.paged and 32 + 8 * ((L + 3) // 4 * 4) <= 576
-    kernel_of = {"init": "k_init", "select": "k_select", "rank": "k_rank_tma" if V % 4 == 0 and L + 1 <= 64 else "k_prepass",
+    kernel_of = {"init": "k_init", "select": "k_select", "rank": "k_rank_tma" if V % 4 == 0 and L + 1 <= 512 else "k_prepass",
                  "steps": "k_step_warp" if warp_path else "k_step", "rank+steps": "k_fused", "output": "k_output"}
     per_stage = {n: [] for n, _ in stages}
     totals = []
@@ -500,7 +501,7 @@ def main():
         "stage_ms": stage_ms,
         "unfused_stage_ms": split_ms,
         "roofline": {"kernel": kernel_of[dom], "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic_record(kernel_of[dom]),
+                     "frac": achieved / peak, "traffic": traffic_record(kernel_of[dom], w.name),
                      "peak_kind": peak_kind},
         "decode_roofline": {"achieved": decode_gbs, "peak": peak, "unit": "GB/s", "frac": decode_gbs / peak,
                             "bytes_per_step": by["decode"], "peak_kind": peak_kind},
