@@ -34,8 +34,8 @@ cudaError_t launch_fused(const View& st, const float* lp, long long sb, long lon
 bool rank_tma_ok(const float* lp, long long s1, long long s2, int V, int L);
 int rank_tma_warps(int V);
 
-// The warp-per-row step kernel takes flat storage, beam <= 16, no label
-// boosting and a ranked record of at most 32 + 8*68 bytes (list length <= 66).
+// The warp-per-row step kernel takes flat storage, beam <= 16 and a ranked
+// record of at most 32 + 8*68 bytes (list length <= 66).
 bool step_warp_fits(const Layout& lay);
 cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s);

@@ -199,7 +199,8 @@ __device__ __forceinline__ void push_key(WarpSmem& W, u64 key, u64 thr, int lane
 // best.  Returns how many are live, plus 1 << 16 when the frame's unlisted
 // labels were scanned.
 __device__ __noinline__ int warp_collect_select(WarpSmem& W, const char* rec, int Lpad, int n, int beam, int cap,
-                                                int blank, int V, const float* __restrict__ row, int lane, u64 thr) {
+                                                int blank, int V, const float* __restrict__ row, int lane, u64 thr,
+                                                BoostTab bt) {
   const RecHdr* h = (const RecHdr*)rec;
   const int cnt = h->cnt;
   const int* ids = (const int*)(rec + 32);
@@ -268,6 +269,8 @@ __device__ __noinline__ int warp_collect_select(WarpSmem& W, const char* rec, in
         for (int u = 0; u < 4; ++u) {
           const int c = c0 + 32 * u + lane;
           v[u] = c < V ? rdlp(row[c]) : CTCPB_NEG;
+          // labels as emitted: the list ranks them by the boosted log-prob
+          if (bt.keys && c < V) v[u] = dadd(v[u], boost_of(bt.keys, bt.vals, bt.hmask, c));
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -499,7 +502,7 @@ template <int KB>
 __device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const float* row, u32 sstar, int nw1, float A,
                                         int last, int len, bool live, float Rrep, int my_id, float my_lp, float scB,
                                         float bpb, float bpnb, int mi, bool anyfold, int n, int cnt, int cap, int beam,
-                                        int blank, int V, int Lpad, bool gap, int hrow, int lane) {
+                                        int blank, int V, int Lpad, bool gap, int hrow, int lane, BoostTab bt) {
   const RecHdr* hd = (const RecHdr*)Rc;
   if (nw1 == beam) {
     const int plan = round2_plan(A, len, live, my_lp, cnt, n, cap, hd->front_lp, sstar, lane);
@@ -537,7 +540,7 @@ __device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const fl
   W.bw[lane] = -1;
   __syncwarp();
   const u64 thr = nw1 == beam ? ((u64)sstar << 32) : 0ull;
-  const int res = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr);
+  const int res = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr, bt);
   const int nw = res & 0xffff;
   const u64 key = lane < nw ? W.keys[lane] : 0ull;
   const int gsrc = ck_src(key), gtk = ck_tok(key);
@@ -566,7 +569,7 @@ constexpr long long kFlagSpins = 1ll << 20;  // bounded wait for published recor
 // block's other warps only help build the tables).  KB: beam bucket (8, 16 or
 // 32), the bound of the per-hypothesis compares.  flags: the records' ready
 // flags when the pre-pass runs concurrently (null: the records are complete).
-template <int KB>
+template <int KB, bool BOOST>
 __device__ __forceinline__ void step_warp_body(const View& st, const float* __restrict__ lp, long long sb,
                                                long long stt, int mode, const int* __restrict__ nframes,
                                                int chunk_T, int tile_start, int tile_len, unsigned char* smem,
@@ -582,6 +585,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   const Layout& Ly = st.lay;
   const int b = row_block * kWPC + wid;
   if (wid >= kWPC || b >= Ly.B) return;
+  // the row's label-boost table (keys null: no boosting; BOOST instantiations only)
+  const BoostTab bt{BOOST ? st.bkey(b) : nullptr, BOOST ? st.bval(b) : nullptr, Ly.hcap - 1};
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V, Lpad = Ly.Lpad;
   const int space = Ly.space;  // word-boundary label, -1: none
   const float NEG = CTCPB_NEG;
@@ -630,6 +635,19 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     msrc = st.msrc()[rb + lane];
   }
   int origin = lane, lo = len, nnew = 0, gl = -1;
+  // BOOST: the first two slots of the last label's probe sequence, loaded a
+  // step before they are used and without a branch on the loaded values (a
+  // branch would wait for the loads); a label further along is looked up then
+  int bk0 = -1, bk1 = -1;
+  float bv0 = 0.0f, bv1 = 0.0f;
+  auto bonus_prefetch = [&](bool want) {
+    const int h0 = boost_slot(want ? last : 0, bt.hmask), h1 = (h0 + 1) & bt.hmask;
+    bk0 = want ? __ldg(bt.keys + h0) : -1;
+    bk1 = want ? __ldg(bt.keys + h1) : -1;
+    bv0 = want ? __ldg(bt.vals + h0) : 0.0f;
+    bv1 = want ? __ldg(bt.vals + h1) : 0.0f;
+  };
+  if (BOOST) bonus_prefetch(lane < nlive && len > 0);
   int win0 = 0;  // call step index of the ring's first entry
   u32 c_steps = 0, c_fb = 0, c_gen = 0, c_scan = 0, c_hash = 0;
 #ifdef CTCPB_PHASE_PROF
@@ -789,6 +807,18 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         const bool gathered = s >= 1 && gl >= 0;
         if (live && len > 0) lpl = gathered ? rdlp(gcur) : rdlp(__ldg(row + last));
       }
+      // the last label emitted again (the repeat path, a fold) carries its bonus
+      float lple = lpl;
+      if (BOOST && live && len > 0) {
+        float bon = 0.0f;  // an empty slot ends the probe: not boosted
+        if (bk0 == last)
+          bon = bv0;
+        else if (bk0 >= 0 && bk1 == last)
+          bon = bv1;
+        else if (bk0 >= 0 && bk1 >= 0)
+          bon = boost_of(bt.keys, bt.vals, bt.hmask, last);
+        lple = dadd(lpl, bon);
+      }
       const float bpb = dadd(lpb, A);
       // (a space-ending beam has no stay path: every space frame is a token)
       const float stay = (live && len > 0 && !gap && last != space) ? dadd(lpl, pnbx) : NEG;
@@ -799,10 +829,10 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
       const int len_i = __shfl_sync(WFULL, len, mil);
       const bool rep_i = mi >= 0 && len_i > 0 && last_i == last && last != space;
       // the extension of l_i folded into this blank slot (NEG when there is none)
-      const float mterm = mi >= 0 ? dadd(lpl, rep_i ? pb_i : A_i) : NEG;
+      const float mterm = mi >= 0 ? dadd(lple, rep_i ? pb_i : A_i) : NEG;
       // candidate (k, last): the repeat path (pb only); the word-boundary label
       // extends from both paths
-      const float Rrep = (live && len > 0 && len < cap) ? dadd(lpl, last == space ? A : pbx) : NEG;
+      const float Rrep = (live && len > 0 && len < cap) ? dadd(lple, last == space ? A : pbx) : NEG;
       const int n = nlive;
       // blank slot (3.4.1-3.4.3), branch-free so it overlaps the candidates below
       const bool anyfold = __any_sync(WFULL, mi >= 0);
@@ -849,7 +879,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         __syncwarp();  // (also: the optimistic slots are written before they are rewritten)
         ++c_fb;
         const int res = slow_select<KB>(W, W.rec1, row, sstar, nw, A, last, len, live, Rrep, my_id, my_lp, scB, bpb, bpnb,
-                                        mi, anyfold, n, cnt, cap, beam, blank, V, Lpad, gap, s - win0, lane);
+                                        mi, anyfold, n, cnt, cap, beam, blank, V, Lpad, gap, s - win0, lane, bt);
         nw = res & 0xff;
         c_gen += (u32)((res >> 8) & 1);
         c_scan += (u32)((res >> 9) & 1);
@@ -879,6 +909,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     // ---- the one merge relation the sources cannot show: a blank winner
     // whose parent prefix equals an extension winner (hash proposal, exact check)
     nlive = nw;
+    if (BOOST) bonus_prefetch(lane < nw && len > 0);
     {
       const bool wl = lane < nw;
       const bool want = wl && step > 0 && isb_w && msrc < 0 && len >= 1;
@@ -949,12 +980,12 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   }
 }
 
-template <int KB>
+template <int KB, bool BOOST>
 __global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float* __restrict__ lp, long long sb,
                                                          long long stt, int mode, const int* __restrict__ nframes,
                                                          int chunk_T, int tile_start, int tile_len) {
   extern __shared__ __align__(128) unsigned char smem[];
-  step_warp_body<KB>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x, nullptr);
+  step_warp_body<KB, BOOST>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x, nullptr);
 }
 
 // Pre-pass and steps in one cooperative launch: blocks [0, nsb) run the rows'
@@ -962,14 +993,15 @@ __global__ void __launch_bounds__(32 * kWPC, 1) k_step_warp(View st, const float
 // release flag that the step warps acquire before copying it.  Every block is
 // resident at once (cooperative launch), so the waits always end; each one is
 // bounded all the same.
-template <int KB>
+template <int KB, bool BOOST>
 __global__ void __launch_bounds__(256, 1) k_fused(View st, const float* __restrict__ lp, long long sb, long long stt,
                                                   int mode, const int* __restrict__ nframes, int chunk_T,
                                                   int tile_start, int tile_len, int nsb, int rank_warps) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&st.hdr()->fused_launches, 1u);
   if ((int)blockIdx.x < nsb) {
-    step_warp_body<KB>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x, st.rflag());
+    step_warp_body<KB, BOOST>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, smem, blockIdx.x,
+                              st.rflag());
   } else {
     RecItems items{st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, st.rflag()};
     rank_tma_body_small(items, st.lay.V, st.lay.blank, st.lay.L, &st.hdr()->status, smem, (int)blockIdx.x - nsb,
@@ -981,33 +1013,38 @@ __global__ void __launch_bounds__(256, 1) k_fused(View st, const float* __restri
 // few lanes for extensions to prove a selection (the block kernel is faster
 // from beam 17 on: 9.2 vs 17.4 ms at beam 20 on the bpe workload).
 bool step_warp_fits(const Layout& lay) {
-  return lay.beam <= 16 && !lay.paged && lay.hcap == 0 && lay.rec_bytes <= (size_t)kMaxRec;
+  return lay.beam <= 16 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
 }
 
 size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem); }
 
-template <int KB>
+template <int KB, bool BOOST>
 static cudaError_t launch_kb(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   const size_t smem = step_warp_smem_bytes();
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_step_warp<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_step_warp<KB, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int blocks = (st.lay.B + kWPC - 1) / kWPC;
-  k_step_warp<KB><<<blocks, 32 * kWPC, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
+  k_step_warp<KB, BOOST><<<blocks, 32 * kWPC, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
   return cudaGetLastError();
 }
 
 cudaError_t launch_step_warp(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
-  if (st.lay.beam <= 8) return launch_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
-  return launch_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  // label boosting has instantiations of its own, so the plain kernels carry none of its code
+  const bool bo = st.lay.hcap > 0;
+  if (st.lay.beam <= 8)
+    return bo ? launch_kb<8, true>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s)
+              : launch_kb<8, false>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return bo ? launch_kb<16, true>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s)
+            : launch_kb<16, false>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }
 
-template <int KB>
+template <int KB, bool BOOST>
 static cudaError_t launch_fused_kb(const View& st, const float* lp, long long sb, long long stt, int mode,
                                   const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   const Layout& Ly = st.lay;
@@ -1023,26 +1060,30 @@ static cudaError_t launch_fused_kb(const View& st, const float* lp, long long sb
   if (!coop || rw < 1 || smem > (size_t)maxsm) return cudaErrorNotSupported;
   static size_t attr_smem = 0;
   if (attr_smem != smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_fused<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_fused<KB, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_smem = smem;
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<KB>, 256, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<KB, BOOST>, 256, smem);
   if (e != cudaSuccess) return e;
   const int grid = per_sm * sms;
   int nsb = (Ly.B + kWPC - 1) / kWPC;
   if (per_sm < 1 || nsb + 8 > grid) return cudaErrorNotSupported;  // keep at least 8 ranking blocks
   View stv = st;
   void* args[] = {&stv, (void*)&lp, &sb, &stt, &mode, (void*)&nframes, &chunk_T, &tile_start, &tile_len, &nsb, &rw};
-  return cudaLaunchCooperativeKernel((const void*)k_fused<KB>, grid, 256, args, smem, s);
+  return cudaLaunchCooperativeKernel((const void*)k_fused<KB, BOOST>, grid, 256, args, smem, s);
 }
 
 cudaError_t launch_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                          int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (!step_warp_fits(st.lay) || !rank_tma_ok(lp, sb, stt, st.lay.V, st.lay.L)) return cudaErrorNotSupported;
-  if (st.lay.beam <= 8) return launch_fused_kb<8>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
-  return launch_fused_kb<16>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  const bool bo = st.lay.hcap > 0;
+  if (st.lay.beam <= 8)
+    return bo ? launch_fused_kb<8, true>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s)
+              : launch_fused_kb<8, false>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  return bo ? launch_fused_kb<16, true>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s)
+            : launch_fused_kb<16, false>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
 }
 
 }  // namespace ctcpb

@@ -85,7 +85,8 @@ typedef struct CUstream_st* ctcpb_stream_t;
  *   max_boost        0: no label boosting.  1..4096: every row (utterance or
  *                    stream) may boost up to max_boost labels (ctcpb_boost);
  *                    the workspace / state then holds a label-boost hash table
- *                    per row, and the decode steps run on the block kernel.
+ *                    per row, and the decode runs kernel instantiations that
+ *                    read it (the plain ones carry no boosting code).
  */
 typedef struct ctcpb_config {
   int32_t beam;
