@@ -435,12 +435,17 @@ int ctcpb_host_workspace_size(const ctcpb_config* cfg, int B, int T, int V, int 
 // blank threshold keeps) once its copies are done, and chunk c's buffer is
 // copied into again only after that decode.  Row b's chunk c holds its frames
 // [cF, cF + F) that are below len_b; the others are never read.
-int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
-                              const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
-                              int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
-                              ctcpb_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int decode_offline_host_impl(const ctcpb_config* cfg, const ctcpb_boost* boost, const float* log_prob,
+                             int64_t stride_b, int64_t stride_t, const int32_t* seq_lengths, int B, int T, int V,
+                             void* ws, size_t ws_bytes, int32_t* out_tokens, int32_t* out_lengths, float* out_scores,
+                             int out_len, ctcpb_stream_t stream) {
   int rc = check_cfg(cfg, V);
   if (rc) return rc;
+  if (boost && (rc = check_boost(cfg, boost))) return rc;
   if (B < 0 || T < 0 || out_len < 0) return CTCPB_EINVAL;
   if (B == 0) return CTCPB_OK;
   if (T > 0 && (stride_t < V || stride_b < V)) return CTCPB_EINVAL;
@@ -482,6 +487,7 @@ int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, in
   }
   TRY(launch_host_plan(seq_lengths ? lens_d : nullptr, B, T, F, hl.nchunks, plan, s));
   TRY(launch_init(st, s));
+  if (boost) TRY(launch_boost_build(st, boost->row_ptr, boost->tokens, boost->bonus, s));
 
   const float thr = cfg->blank_threshold;
   // every frame (mode 1), or the frames the threshold keeps (mode 2; thr <= 0 keeps none)
@@ -532,6 +538,26 @@ int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, in
   TRY(cudaMemcpyAsync(out_scores, sc_d, 4 * nb, cudaMemcpyDeviceToHost, s));
   if (out_len > 0) TRY(cudaMemcpyAsync(out_tokens, tok_d, 4 * nb * (size_t)out_len, cudaMemcpyDeviceToHost, s));
   return CTCPB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
+                              const int32_t* seq_lengths, int B, int T, int V, void* ws, size_t ws_bytes,
+                              int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
+                              ctcpb_stream_t stream) {
+  return decode_offline_host_impl(cfg, nullptr, log_prob, stride_b, stride_t, seq_lengths, B, T, V, ws, ws_bytes,
+                                  out_tokens, out_lengths, out_scores, out_len, stream);
+}
+
+int ctcpb_decode_offline_host_boosted(const ctcpb_config* cfg, const ctcpb_boost* boost, const float* log_prob,
+                                      int64_t stride_b, int64_t stride_t, const int32_t* seq_lengths, int B, int T,
+                                      int V, void* ws, size_t ws_bytes, int32_t* out_tokens, int32_t* out_lengths,
+                                      float* out_scores, int out_len, ctcpb_stream_t stream) {
+  return decode_offline_host_impl(cfg, boost, log_prob, stride_b, stride_t, seq_lengths, B, T, V, ws, ws_bytes,
+                                  out_tokens, out_lengths, out_scores, out_len, stream);
 }
 
 }  // extern "C"

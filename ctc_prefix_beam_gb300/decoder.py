@@ -90,6 +90,8 @@ def lib():
                 "ctcpb_stream_set_boost": (I, [cfgp, P, SZ, I, I, ctypes.POINTER(_Boost), P]),
                 "ctcpb_host_workspace_size": (I, [cfgp, I, I, I, I, ctypes.POINTER(SZ)]),
                 "ctcpb_decode_offline_host": (I, [cfgp, P, I64, I64, P, I, I, I, P, SZ, P, P, P, I, P]),
+                "ctcpb_decode_offline_host_boosted": (I, [cfgp, ctypes.POINTER(_Boost), P, I64, I64, P, I, I, I, P,
+                                                          SZ, P, P, P, I, P]),
                 "ctcpb_state_size": (I, [cfgp, I, I, ctypes.POINTER(SZ)]),
                 "ctcpb_stream_init": (I, [cfgp, P, SZ, I, I, P]),
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
@@ -256,12 +258,13 @@ def host_workspace_size(cfg: Config, B: int, T: int, V: int, out_len: int) -> in
 
 def decode_offline_host(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None, *,
                         workspace: Optional[torch.Tensor] = None, out_len: Optional[int] = None, outputs=None,
-                        device="cuda", synchronize: bool = True):
+                        device="cuda", synchronize: bool = True, boost=None):
     """Offline decode of a HOST float32 [B, T, V] batch into host outputs
     (``ctcpb_decode_offline_host``): the frames are copied in chunks while the
     decode runs.  Page-locked tensors (``pin_memory()``) keep the call
     asynchronous; the outputs are valid once the device's current stream is
-    synchronised, which this function does unless ``synchronize`` is False."""
+    synchronised, which this function does unless ``synchronize`` is False.
+    ``boost``: the rows' label boosts (``boost_tables``; needs ``cfg.max_boost``)."""
     if log_prob.dtype != torch.float32 or log_prob.dim() != 3 or log_prob.is_cuda or log_prob.stride(2) != 1:
         raise ValueError("log_prob must be a host float32 tensor [B, T, V] with V contiguous")
     B, T, V = log_prob.shape
@@ -282,10 +285,17 @@ def decode_offline_host(cfg: Config, log_prob: torch.Tensor, seq_lengths: Option
                    torch.empty((B, c.nbest), dtype=torch.int32, pin_memory=pin),
                    torch.empty((B, c.nbest), dtype=torch.float32, pin_memory=pin))
     tok, ln, sc = outputs
-    _check(lib().ctcpb_decode_offline_host(ctypes.byref(c), _ptr(log_prob), log_prob.stride(0), log_prob.stride(1),
-                                           _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
-                                           _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev)),
-           "decode_offline_host")
+    if boost is not None:
+        tables = boost_tables(boost, B, dev)
+        rc = lib().ctcpb_decode_offline_host_boosted(ctypes.byref(c), ctypes.byref(_boost_arg(tables)),
+                                                     _ptr(log_prob), log_prob.stride(0), log_prob.stride(1),
+                                                     _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
+                                                     _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
+    else:
+        rc = lib().ctcpb_decode_offline_host(ctypes.byref(c), _ptr(log_prob), log_prob.stride(0), log_prob.stride(1),
+                                             _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
+                                             _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
+    _check(rc, "decode_offline_host")
     if synchronize:
         torch.cuda.current_stream(dev).synchronize()
     return tok, ln, sc

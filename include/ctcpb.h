@@ -215,6 +215,13 @@ int ctcpb_decode_offline_host(const ctcpb_config* cfg, const float* log_prob, in
                               int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
                               ctcpb_stream_t stream);
 
+/* The same with label boosting (ctcpb_boost: DEVICE arrays, as in
+ * ctcpb_decode_offline_boosted; requires cfg->max_boost >= 1). */
+int ctcpb_decode_offline_host_boosted(const ctcpb_config* cfg, const ctcpb_boost* boost, const float* log_prob,
+                                      int64_t stride_b, int64_t stride_t, const int32_t* seq_lengths, int B, int T,
+                                      int V, void* ws, size_t ws_bytes, int32_t* out_tokens, int32_t* out_lengths,
+                                      float* out_scores, int out_len, ctcpb_stream_t stream);
+
 /*
  * Offline decode for callers that cannot allocate device memory./*
  * Offline decode for callers that cannot allocate device memory.  The pages

@@ -135,3 +135,16 @@ def test_streaming_boost_equals_offline(paged):
         torch.cuda.synchronize()
         assert_same(tuple(v.cpu().numpy() for v in out), ref, f"chunks {chunks[:3]}")
         assert st.status() == 0
+
+
+@pytest.mark.parametrize("name,over", [("bpe", dict(beam=10)), ("char", dict(paged=True, beam=40, nbest=5))])
+def test_boosted_host_buffer_decode_matches_oracle(name, over):
+    w = synth.workload(name, B=4, T=180)
+    lp, lens = synth.gen_batch(w)
+    cfg = cfg_of(w, max_boost=16, **over)
+    rng = np.random.default_rng(11)
+    boost = random_boosts(rng, lp.shape[0], lp.shape[2], cfg.blank_id, 16, frames=lp)
+    x = torch.from_numpy(np.ascontiguousarray(lp)).pin_memory()
+    ln = torch.from_numpy(np.ascontiguousarray(lens, np.int32)).pin_memory()
+    out = D.decode_offline_host(cfg, x, ln, boost=boost)
+    assert_same(tuple(o.numpy() for o in out), oracle_offline(cfg, lp, lens, boost=boost), f"host {name}")
