@@ -1374,7 +1374,7 @@ static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, 
 cudaError_t launch_step(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                         int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   if (st.lay.B == 0) return cudaSuccess;
-  if (st.lay.beam <= 32 && !st.lay.paged && step_warp_fits(st.lay))
+  if (step_warp_fits(st.lay))  // beam <= 16, flat storage, short lists
     return launch_step_warp(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   if (st.lay.beam <= 32) return launch_step_t<32>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
   return launch_step_t<128>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);

@@ -566,9 +566,10 @@ __device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const fl
 constexpr long long kFlagSpins = 1ll << 20;  // bounded wait for published records (about 1 s)
 
 // The steps of rows row_block*kWPC + warp (warps 0..kWPC-1 of the block; the
-// block's other warps only help build the tables).  KB: beam bucket (8, 16 or
-// 32), the bound of the per-hypothesis compares.  flags: the records' ready
-// flags when the pre-pass runs concurrently (null: the records are complete).
+// block's other warps only help build the tables).  KB: beam bucket (8 or 16),
+// the bound of the per-hypothesis compares.  BOOST: the rows have label-boost
+// tables.  flags: the records' ready flags when the pre-pass runs concurrently
+// (null: the records are complete).
 template <int KB, bool BOOST>
 __device__ __forceinline__ void step_warp_body(const View& st, const float* __restrict__ lp, long long sb,
                                                long long stt, int mode, const int* __restrict__ nframes,
