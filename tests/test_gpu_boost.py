@@ -148,3 +148,26 @@ def test_boosted_host_buffer_decode_matches_oracle(name, over):
     ln = torch.from_numpy(np.ascontiguousarray(lens, np.int32)).pin_memory()
     out = D.decode_offline_host(cfg, x, ln, boost=boost)
     assert_same(tuple(o.numpy() for o in out), oracle_offline(cfg, lp, lens, boost=boost), f"host {name}")
+
+
+def test_streaming_boost_with_speech_mask_equals_offline():
+    """Label boosts and a speech mask together (masked streaming on the boosted
+    kernels) against the oracle decoding the same frames with the same mask."""
+    w = synth.workload("bpe", B=3, T=150)
+    lp, _ = synth.gen_batch(w)
+    cfg = cfg_of(w, beam=10, nbest=10, max_seq_len=150, max_boost=12)
+    rng = np.random.default_rng(21)
+    boost = random_boosts(rng, 3, lp.shape[2], 0, 12, frames=lp)
+    mask = (rng.random((3, 150)) > 0.3).astype(np.uint8)
+    ref = O.decode(lp, None, beam=10, nbest=10, cap=150, out_len=150, mask=mask, boost=boost)
+    st = D.StreamState(cfg, 3, lp.shape[2])
+    st.set_boost(boost)
+    t0 = 0
+    for c in (16, 40, 94):
+        st.step_chunk(torch.from_numpy(np.ascontiguousarray(lp[:, t0:t0 + c])).cuda(),
+                      is_speech=torch.from_numpy(np.ascontiguousarray(mask[:, t0:t0 + c])).cuda())
+        t0 += c
+    out = st.read(out_len=150)
+    torch.cuda.synchronize()
+    assert_same(tuple(v.cpu().numpy() for v in out), ref, "boost + mask")
+    assert st.status() == 0
