@@ -265,8 +265,10 @@ def decode_offline_host(cfg: Config, log_prob: torch.Tensor, seq_lengths: Option
     asynchronous; the outputs are valid once the device's current stream is
     synchronised, which this function does unless ``synchronize`` is False.
     ``boost``: the rows' label boosts (``boost_tables``; needs ``cfg.max_boost``)."""
-    if log_prob.dtype != torch.float32 or log_prob.dim() != 3 or log_prob.is_cuda or log_prob.stride(2) != 1:
-        raise ValueError("log_prob must be a host float32 tensor [B, T, V] with V contiguous")
+    if log_prob.dtype != torch.float32 or log_prob.dim() != 3 or log_prob.is_cuda:
+        raise ValueError("log_prob must be a host float32 tensor [B, T, V]")
+    if log_prob.stride(2) != 1:
+        log_prob = log_prob.contiguous()
     B, T, V = log_prob.shape
     c = cfg.c()
     if out_len is None:

@@ -8,7 +8,7 @@ import torch
 import oracle as O
 from ctc_prefix_beam_gb300 import decoder as D
 from ctc_prefix_beam_gb300 import synth
-from gpu_util import assert_same, cfg_of, gpu_offline, oracle_offline
+from gpu_util import NEG, assert_same, cfg_of, gpu_offline, oracle_offline
 
 pytestmark = pytest.mark.gpu
 
@@ -107,3 +107,24 @@ def test_full_size_host_decode_sampled_rows(name, rows):
     h = host_decode(cfg, lp, lens)
     o = oracle_offline(cfg, lp, lens, rows=rows)
     assert_same(tuple(x[rows] for x in h), o, f"{name} rows {rows}")
+
+
+@pytest.mark.parametrize("B,T,V,over", [(1, 1, 2, dict(beam=1, nbest=1)),
+                                        (3, 65, 7, dict(beam=3, nbest=3, paged=True, page_size=2,
+                                                        blank_threshold=0.9)),
+                                        (2, 0, 5, dict(beam=2, nbest=2))])
+def test_host_decode_edge_shapes(B, T, V, over):
+    rng = np.random.default_rng(B * 100 + T + V)
+    x = rng.normal(0.0, 2.0, size=(B, T, V))
+    if T:
+        x[:, :, 0] += 1.5
+    lp = (x - np.log(np.exp(x).sum(-1, keepdims=True))).astype(np.float32) if T else np.zeros((B, 0, V), np.float32)
+    cfg = D.Config(**over)
+    h = host_decode(cfg, lp, None)
+    if T == 0:  # no decoded frame: the empty prefix with score 0, then dead slots
+        nb = cfg.nbest
+        exp_sc = np.full((B, nb), NEG, np.float32)
+        exp_sc[:, 0] = 0.0
+        assert_same(h, (np.zeros((B, nb, 0), np.int32), np.zeros((B, nb), np.int32), exp_sc), "T=0")
+        return
+    assert_same(h, oracle_offline(cfg, lp, None), f"B={B} T={T} V={V} {over}")
