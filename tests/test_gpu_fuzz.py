@@ -70,3 +70,45 @@ def test_random_configuration_matches_oracle(seed):
     g = (tok.cpu().numpy(), l.cpu().numpy(), sc.cpu().numpy())
     assert_same(g, oracle_offline(cfg, lp, lens, boost=boost), f"seed {seed}: {cfg}")
     assert D.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_streaming_matches_oracle(seed):
+    """The same configurations streamed in random chunkings, half of them
+    with a random speech mask, against the oracle decoding every frame (the
+    masked ones skipped) offline."""
+    cfg, lp, _, boost = draw(seed)
+    cfg.blank_threshold = 1.0  # streaming never skips by threshold
+    B, T, V = lp.shape
+    rng = np.random.default_rng(20_000 + seed)
+    mask = (rng.random((B, T)) > 0.3).astype(np.uint8) if rng.random() < 0.5 else None
+    st = D.StreamState(cfg, B, V)
+    if boost is not None:
+        st.set_boost(boost)
+    t0 = 0
+    while t0 < T:
+        c = int(min(T - t0, rng.integers(1, 90)))
+        chunk = torch.from_numpy(np.ascontiguousarray(lp[:, t0:t0 + c])).cuda()
+        if mask is None:
+            st.step_chunk(chunk)
+        else:
+            st.step_chunk(chunk, is_speech=torch.from_numpy(np.ascontiguousarray(mask[:, t0:t0 + c])).cuda())
+        t0 += c
+    out = st.read(out_len=T)
+    torch.cuda.synchronize()
+    cap = cfg.max_seq_len if cfg.max_seq_len > 0 else 4096
+    ref = O.decode(lp, None, beam=cfg.beam, nbest=cfg.c().nbest, blank=cfg.blank_id, cap=cap, out_len=T,
+                   mask=mask, space=cfg.space_id, boost=boost)
+    assert_same(tuple(v.cpu().numpy() for v in out), ref, f"seed {seed}: {cfg}")
+    assert st.status() == 0
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_host_buffer_decode_matches_oracle(seed):
+    """The same configurations through the host-buffer call (chunked copies,
+    streaming tiles, threshold skipping per tile)."""
+    cfg, lp, lens, boost = draw(seed)
+    x = torch.from_numpy(lp).pin_memory()
+    ln = None if lens is None else torch.from_numpy(lens).pin_memory()
+    out = D.decode_offline_host(cfg, x, ln, boost=boost)
+    assert_same(tuple(o.numpy() for o in out), oracle_offline(cfg, lp, lens, boost=boost), f"seed {seed}: {cfg}")
