@@ -429,6 +429,9 @@ __device__ void flush_flat(StepSmem<NT>& S, const View& st, int b, int par, int 
         reinterpret_cast<int4*>(st.clist(to, b, w))[x] = v[u];
       }
   }
+  // every word copy has read its slot's origin and length before the owners
+  // below reset them
+  gsync<NT>();
   // the prefix tail after the last whole word, then the gained labels
   for (int w = tid; w < nw; w += NT) {
     const int o = S.norg[w], l0 = S.nlo[w];

@@ -304,3 +304,38 @@ def test_state_header_mismatch_sets_status():
         pytest.skip("state for V=60 does not fit")
     bad.step_chunk(torch.zeros((2, 3, 60), device="cuda"))
     assert st.status() & D.DEV_HEADER
+
+
+@pytest.mark.parametrize("beam,paged", [(128, False), (64, False), (128, True)])
+def test_long_rows_with_mid_window_token_writes(beam, paged):
+    """Long utterances on the 128-thread block kernel with label boosts, whose
+    merges are proposed by prefix hashes: the token store is written in the
+    middle of a ring window (before each check) as well as every 64 steps, by
+    several warps at once; tokens and scores must match the oracle."""
+    # the draws of the randomised sweep's case that found a race in the flat
+    # token-store write: the shape and options first, then boosts and frames
+    rng = np.random.default_rng(777_001)
+    V = int(rng.choice([29, 100, 1024, 5000]))
+    assert int(rng.choice([8, 10, 16, 20, 32, 64, 128])) == 128
+    T = int(rng.integers(100, 700))
+    B = int(rng.integers(1, 5))
+    rng.integers(1, 16)
+    rng.random(4)  # (storage, cap, threshold and word-boundary draws: none applied)
+    assert (V, T, B) == (100, 507, 2) and rng.random() < 0.3
+    nb = min(int(rng.integers(1, 40)), V - 1)
+    boost = [{int(c): float(np.float32(rng.uniform(-3, 5))) for c in rng.choice(np.arange(1, V), nb, replace=False)}
+             for _ in range(B)]
+    x = rng.normal(0, float(rng.choice([1.0, 2.0])), size=(B, T, V))
+    x[:, :, 0] += np.where(rng.random((B, T)) < 0.7, 6.0, 0.0)
+    lp = x - x.max(-1, keepdims=True)
+    lp = (lp - np.log(np.exp(lp).sum(-1, keepdims=True))).astype(np.float32)
+    lens = rng.integers(T // 2, T + 1, size=B).astype(np.int32)
+    cfg = D.Config(beam=beam, nbest=3, max_boost=nb, paged=paged)
+    dev = torch.device("cuda")
+    ws = torch.empty(D.workspace_size(cfg, B, T, V), dtype=torch.uint8, device=dev)
+    tok, ln, sc = D.decode_offline(cfg, torch.from_numpy(lp).to(dev), torch.from_numpy(lens).to(dev),
+                                   workspace=ws, boost=boost)
+    torch.cuda.synchronize()
+    assert D.read_counters(ws)["hash_merges"] > 0
+    assert_same((tok.cpu().numpy(), ln.cpu().numpy(), sc.cpu().numpy()),
+                oracle_offline(cfg, lp, lens, boost=boost), f"beam {beam} paged {paged}")
