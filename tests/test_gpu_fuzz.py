@@ -112,3 +112,72 @@ def test_random_host_buffer_decode_matches_oracle(seed):
     ln = None if lens is None else torch.from_numpy(lens).pin_memory()
     out = D.decode_offline_host(cfg, x, ln, boost=boost)
     assert_same(tuple(o.numpy() for o in out), oracle_offline(cfg, lp, lens, boost=boost), f"seed {seed}: {cfg}")
+
+
+def draw_long(seed):
+    """A long-utterance configuration: rows of 150-800 frames (token-store
+    writes in many rounds, several 64-step windows), beams up to 128."""
+    rng = np.random.default_rng(999_000 + seed)
+    V = int(rng.choice([29, 100, 1024, 5000]))
+    beam = int(rng.choice([4, 10, 16, 20, 32, 48, 64, 128]))
+    T = int(rng.integers(150, 800))
+    if beam * V * T > 120_000_000:
+        T = max(60, 120_000_000 // (beam * V))
+    B = int(rng.integers(1, 4))
+    cfg = dict(beam=beam, nbest=min(beam, int(rng.integers(1, 12))))
+    if rng.random() < 0.4:
+        cfg.update(paged=True, page_size=int(rng.choice([1, 2, 8, 16])))
+    if rng.random() < 0.25:
+        cfg["max_seq_len"] = int(rng.integers(5, 300))
+    if rng.random() < 0.25:
+        cfg["space_id"] = int(rng.integers(1, V))
+    boost = None
+    if rng.random() < 0.4:
+        nb = min(int(rng.integers(1, 30)), V - 1)
+        boost = [{int(c): float(np.float32(rng.uniform(-3, 5))) for c in rng.choice(np.arange(1, V), nb, replace=False)}
+                 for _ in range(B)]
+        cfg["max_boost"] = nb
+    x = rng.normal(0, float(rng.choice([1.0, 2.0])), size=(B, T, V))
+    x[:, :, 0] += np.where(rng.random((B, T)) < 0.7, 6.0, 0.0)
+    lp = x - x.max(-1, keepdims=True)
+    lp = (lp - np.log(np.exp(lp).sum(-1, keepdims=True))).astype(np.float32)
+    return rng, D.Config(**cfg), lp, boost
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_long_utterances_match_oracle(seed):
+    """Even seeds decode offline (with lengths, maybe a threshold); odd seeds
+    stream in random chunks, maybe masked."""
+    rng, cfg, lp, boost = draw_long(seed)
+    B, T, V = lp.shape
+    if seed % 2 == 0:
+        lens = rng.integers(T // 3, T + 1, size=B).astype(np.int32)
+        if rng.random() < 0.3:
+            cfg.blank_threshold = float(rng.choice([0.9, 0.99, 0.999]))
+        ws = torch.empty(D.workspace_size(cfg, B, T, V), dtype=torch.uint8, device="cuda")
+        out = D.decode_offline(cfg, torch.from_numpy(lp).cuda(), torch.from_numpy(lens).cuda(), workspace=ws,
+                               boost=boost)
+        torch.cuda.synchronize()
+        assert_same(tuple(o.cpu().numpy() for o in out), oracle_offline(cfg, lp, lens, boost=boost), f"seed {seed}")
+        assert D.read_status(ws) == 0
+        return
+    mask = (rng.random((B, T)) > 0.25).astype(np.uint8) if rng.random() < 0.5 else None
+    st = D.StreamState(cfg, B, V)
+    if boost is not None:
+        st.set_boost(boost)
+    t = 0
+    while t < T:
+        c = int(min(T - t, rng.integers(1, 130)))
+        ch = torch.from_numpy(np.ascontiguousarray(lp[:, t:t + c])).cuda()
+        if mask is None:
+            st.step_chunk(ch)
+        else:
+            st.step_chunk(ch, is_speech=torch.from_numpy(np.ascontiguousarray(mask[:, t:t + c])).cuda())
+        t += c
+    out = st.read(out_len=T)
+    torch.cuda.synchronize()
+    cap = cfg.max_seq_len if cfg.max_seq_len > 0 else 4096
+    ref = O.decode(lp, None, beam=cfg.beam, nbest=cfg.c().nbest, blank=0, cap=cap, out_len=T, mask=mask,
+                   space=cfg.space_id, boost=boost)
+    assert_same(tuple(v.cpu().numpy() for v in out), ref, f"seed {seed}")
+    assert st.status() == 0
