@@ -272,6 +272,16 @@ int ctcpb_stream_step_chunk_masked(const ctcpb_config* cfg, void* state, size_t 
   return CTCPB_OK;
 }
 
+int ctcpb_stream_step(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V, const float* lp_frame,
+                      int64_t stride_b, const uint8_t* is_speech, ctcpb_stream_t stream) {
+  // a chunk of one frame; its frame stride is never stepped over, so it is
+  // given the row stride, which keeps the row addresses' alignment the same
+  if (!is_speech)
+    return ctcpb_stream_step_chunk(cfg, state, state_bytes, B, V, lp_frame, stride_b, stride_b, nullptr, 1, stream);
+  return ctcpb_stream_step_chunk_masked(cfg, state, state_bytes, B, V, lp_frame, stride_b, stride_b, nullptr,
+                                        is_speech, 1, 1, stream);
+}
+
 int ctcpb_read_state(const ctcpb_config* cfg, const void* state, size_t state_bytes, int B, int V,
                      int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
                      ctcpb_stream_t stream) {

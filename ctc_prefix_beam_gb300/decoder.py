@@ -96,6 +96,7 @@ def lib():
                 "ctcpb_stream_init": (I, [cfgp, P, SZ, I, I, P]),
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
                 "ctcpb_stream_step_chunk_masked": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, P, I64, I, P]),
+                "ctcpb_stream_step": (I, [cfgp, P, SZ, I, I, P, I64, P, P]),
                 "ctcpb_read_state": (I, [cfgp, P, SZ, I, I, P, P, P, I, P]),
                 "ctcpb_read_status": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
                 "ctcpb_read_counters": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -346,6 +347,21 @@ class StreamState:
         _check(lib().ctcpb_stream_step_chunk(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
                                              self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames),
                                              lp.shape[1], _stream(lp.device)), "stream_step_chunk")
+
+    def step(self, lp_frame: torch.Tensor, is_speech: Optional[torch.Tensor] = None):
+        """Decode one frame [B, V] for every stream.  ``is_speech`` (CUDA uint8
+        [B]) skips the streams it marks 0; their frame counters still advance."""
+        if lp_frame.dtype != torch.float32 or not lp_frame.is_cuda or lp_frame.dim() != 2:
+            raise ValueError("frame must be a CUDA float32 tensor [B, V]")
+        lp = lp_frame if lp_frame.stride(1) == 1 else lp_frame.contiguous()
+        if lp.shape[0] != self.B or lp.shape[1] != self.V:
+            raise ValueError("frame must be [B, V] for this state")
+        if is_speech is not None:
+            if is_speech.dtype != torch.uint8 or not is_speech.is_cuda or is_speech.shape != (self.B,):
+                raise ValueError("is_speech must be a CUDA uint8 tensor [B]")
+            is_speech = is_speech.contiguous()
+        _check(lib().ctcpb_stream_step(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B, self.V,
+                                       _ptr(lp), lp.stride(0), _ptr(is_speech), _stream(lp.device)), "stream_step")
 
     def read(self, out_len: Optional[int] = None, outputs=None):
         c = self.cfg.c()

@@ -305,6 +305,22 @@ int ctcpb_stream_step_chunk_masked(const ctcpb_config* cfg, void* state, size_t 
                                    int chunk_T, ctcpb_stream_t stream);
 
 /*
+ * Decode one frame for every stream (section 9, ctc_beam_search_step: one
+ * streaming frame).
+ *   lp_frame   [B, V] float32, row stride stride_b (>= V) elements.
+ *   is_speech  [B] uint8 device array or NULL: stream b decodes the frame iff
+ *              is_speech[b] != 0; NULL decodes it for every stream.  A stream
+ *              whose flag is 0 still advances its frame counter, like a masked
+ *              frame of ctcpb_stream_step_chunk_masked: this is how a caller
+ *              that drops frames marks the gap that the pages' step call takes
+ *              as actual_frame_index.
+ * The same as ctcpb_stream_step_chunk (ctcpb_stream_step_chunk_masked when
+ * is_speech is given) with chunk_T = 1, and with the same errors.
+ */
+int ctcpb_stream_step(const ctcpb_config* cfg, void* state, size_t state_bytes, int B, int V,
+                      const float* lp_frame, int64_t stride_b, const uint8_t* is_speech, ctcpb_stream_t stream);
+
+/*
  * Write the current N best of every stream (section 8, read_streaming_results)
  * in the output layout of ctcpb_decode_offline.  Does not modify the state.
  */

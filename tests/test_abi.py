@@ -115,6 +115,11 @@ def test_host_validation_before_any_launch(lib):
                                               16, 16, NULL) == D.ENULL
     assert lib.ctcpb_stream_step_chunk_masked(ctypes.byref(c), big, 1 << 40, 4, 5000, big, 5000, 5000, NULL, big,
                                               8, 16, NULL) == D.EINVAL
+    # single-frame step: a null frame, a row stride below V, a state too small, B = 0
+    assert lib.ctcpb_stream_step(ctypes.byref(c), big, 1 << 40, 4, 5000, NULL, 5000, NULL, NULL) == D.ENULL
+    assert lib.ctcpb_stream_step(ctypes.byref(c), big, 1 << 40, 4, 5000, big, 4999, big, NULL) == D.EINVAL
+    assert lib.ctcpb_stream_step(ctypes.byref(c), big, 16, 4, 5000, big, 5000, NULL, NULL) == D.ESIZE
+    assert lib.ctcpb_stream_step(ctypes.byref(c), NULL, 0, 0, 5000, NULL, 5000, NULL, NULL) == D.OK
     assert lib.ctcpb_read_status(NULL, NULL) == D.ENULL
     assert lib.ctcpb_topk_prepass(ctypes.byref(c), NULL, 10, 5, 5000, NULL, NULL, NULL, NULL, NULL, NULL,
                                   NULL) == D.EINVAL

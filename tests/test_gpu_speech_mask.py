@@ -100,3 +100,58 @@ def test_masked_partial_chunks():
         o = O.decode(lp[b:b + 1, :n], None, beam=cfg.beam, nbest=cfg.nbest, cap=w.T, out_len=w.T,
                      mask=mask[b:b + 1, :n])
         assert_same((tok[b:b + 1], ln[b:b + 1], sc[b:b + 1]), o, f"stream {b}")
+
+
+@pytest.mark.parametrize("name,over,paged", [("bpe", dict(B=4, T=70), False),
+                                             ("char", dict(B=3, T=60), True),
+                                             ("tiny", dict(B=4, T=50), False)])
+def test_single_frame_steps_match_oracle(name, over, paged):
+    """The one-frame call (section 9's ctc_beam_search_step), fed column views
+    of a [B, T, V] tensor (row stride T*V), mixed with chunk calls, some
+    frames flagged as non-speech per stream: the same result as the oracle
+    decoding every frame with that mask."""
+    w = synth.workload(name, **over)
+    lp, _ = synth.gen_batch(w, pad="zero")
+    rng = np.random.default_rng(4242 + w.B)
+    mask = (rng.random((w.B, w.T)) < 0.7).astype(np.uint8)
+    mask[:, 0] = 1
+    cfg = cfg_of(w, max_seq_len=w.T, blank_threshold=1.0)
+    if paged:
+        cfg.paged, cfg.page_size = True, 16
+    dev = torch.device("cuda")
+    x = torch.from_numpy(np.ascontiguousarray(lp)).to(dev)
+    m = torch.from_numpy(mask).to(dev)
+    st = D.StreamState(cfg, w.B, w.V, device=dev)
+    t = 0
+    while t < w.T:
+        if t % 3 == 2:                      # a chunk of up to 7 frames
+            c = min(7, w.T - t)
+            st.step_chunk(x[:, t:t + c], is_speech=m[:, t:t + c])
+            t += c
+            continue
+        col = x[:, t]
+        assert col.stride(0) == w.T * w.V
+        st.step(col, is_speech=None if mask[:, t].all() else m[:, t].contiguous())
+        t += 1
+    got = st.read(out_len=cfg.max_seq_len)
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    assert_same(tuple(v.cpu().numpy() for v in got), oracle_masked(cfg, lp, mask), f"{name}{over}")
+
+
+def test_single_frame_steps_equal_one_chunk():
+    """Every frame by the one-frame call, no mask, equals one chunk call over
+    the same frames (bit-identical outputs)."""
+    w = synth.workload("bpe", B=3, T=40)
+    lp, _ = synth.gen_batch(w, pad="zero")
+    cfg = cfg_of(w, max_seq_len=w.T, blank_threshold=1.0)
+    x = torch.from_numpy(np.ascontiguousarray(lp)).cuda()
+    a = D.StreamState(cfg, w.B, w.V)
+    for t in range(w.T):
+        a.step(x[:, t])
+    b = D.StreamState(cfg, w.B, w.V)
+    b.step_chunk(x)
+    ra, rb = a.read(out_len=w.T), b.read(out_len=w.T)
+    torch.cuda.synchronize()
+    for u, v in zip(ra, rb):
+        assert torch.equal(u, v)
