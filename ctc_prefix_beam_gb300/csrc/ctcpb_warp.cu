@@ -181,6 +181,7 @@ __device__ const Tables g_tables = make_tables();
 __device__ __forceinline__ void push_key(WarpSmem& W, u64 key, u64 thr, int lane) {
   const bool take = key != 0ull && key >= thr;
   const unsigned m = __ballot_sync(WFULL, take);
+  if (m == 0u) return;
   const int base = W.nkeys;
   if (take) W.keys[32 + base + __popc(m & ((1u << lane) - 1u))] = key;
   __syncwarp();
@@ -223,10 +224,15 @@ __device__ __noinline__ int warp_collect_select(WarpSmem& W, const char* rec, in
     push_key(W, kb, thr, lane);
     push_key(W, kr, thr, lane);
   }
-  // listed labels, one hypothesis at a time, one list position per lane
+  // listed labels, one hypothesis at a time, one list position per lane; a
+  // hypothesis whose best listed label scores below thr has none to add (the
+  // list is sorted)
+  const u32 thr_hi = (u32)(thr >> 32);
+  const float lp0 = cnt > 0 ? lps[0] : CTCPB_NEG;
   for (int k = 0; k < n; ++k) {
     const int L = W.len[k], lastk = W.last[k];
     const float Ak = W.A[k];
+    if (fkey(dadd(lp0, Ak)) < thr_hi) continue;
     for (int p0 = 0; p0 < cnt; p0 += 32) {
       const int p = p0 + lane;
       u64 key = 0ull;
