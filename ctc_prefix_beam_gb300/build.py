@@ -19,7 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libctcpb.so")
-SOURCES = ["ctcpb_kernels.cu", "ctcpb_warp.cu", "ctcpb_rank.cu", "ctcpb_api.cu", "ctcpb_noalloc.cu"]
+SOURCES = ["ctcpb_kernels.cu", "ctcpb_warp.cu", "ctcpb_rank.cu", "ctcpb_api.cu", "ctcpb_noalloc.cu",
+           "ctcpb_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -fmad=false: no implicit multiply-add contraction anywhere (the decoder's
 # float arithmetic is written with explicit round-to-nearest intrinsics).

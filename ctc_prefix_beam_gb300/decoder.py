@@ -97,6 +97,7 @@ def lib():
                 "ctcpb_stream_step_chunk": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, I, P]),
                 "ctcpb_stream_step_chunk_masked": (I, [cfgp, P, SZ, I, I, P, I64, I64, P, P, I64, I, P]),
                 "ctcpb_stream_step": (I, [cfgp, P, SZ, I, I, P, I64, P, P]),
+                "ctcpb_selftest_waits": (I, [P, I, ctypes.c_longlong, P, P]),
                 "ctcpb_read_state": (I, [cfgp, P, SZ, I, I, P, P, P, I, P]),
                 "ctcpb_read_status": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
                 "ctcpb_read_counters": (I, [P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -381,6 +382,19 @@ def read_status(buf: torch.Tensor) -> int:
     v = ctypes.c_uint32()
     _check(lib().ctcpb_read_status(_ptr(buf), ctypes.byref(v)), "read_status")
     return v.value
+
+
+def selftest_waits(flags: torch.Tensor, max_spins: int = 1000) -> tuple:
+    """Run the bounded-wait self-test (``ctcpb_selftest_waits``) on a CUDA
+    uint32 flag array; returns (flags found set in order, flag-wait status,
+    barrier-wait status), the statuses CTCPB_DEV_TIMEOUT when a wait gave up."""
+    if flags.dtype != torch.int32 or not flags.is_cuda or flags.dim() != 1:
+        raise ValueError("flags must be a 1-D CUDA int32 tensor (read as uint32)")
+    flags = flags.contiguous()
+    out = torch.zeros(3, dtype=torch.int32, device=flags.device)
+    _check(lib().ctcpb_selftest_waits(_ptr(flags), flags.numel(), max_spins, _ptr(out), _stream(flags.device)),
+           "selftest_waits")
+    return tuple(int(v) for v in out.cpu())
 
 
 def read_counters(buf: torch.Tensor) -> dict:

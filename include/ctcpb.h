@@ -329,6 +329,26 @@ int ctcpb_read_state(const ctcpb_config* cfg, const void* state, size_t state_by
                      ctcpb_stream_t stream);
 
 /*
+ * Self-test of the bounded waits (failure detection without a GPU fault).
+ * One warp runs the two forms of wait the kernels use against conditions
+ * that never complete, and gives up as the kernels do:
+ *   flags      [nflags] uint32 device array: ready flags acquired up to 32 at
+ *              a time, as the fused launch waits for ranked records; the wait
+ *              stops at the first flag still 0 after max_spins tries
+ *              (1 <= max_spins <= 2^20, about 100 ns a try);
+ *   then an mbarrier phase that expects two arrivals and gets one, waited on
+ *   with the pre-pass's bounded barrier wait (under a second).
+ *   out        [3] uint32 device array: out[0] = flags found set in order,
+ *              out[1] = CTCPB_DEV_TIMEOUT if the flag wait gave up, out[2] =
+ *              CTCPB_DEV_TIMEOUT if the barrier wait gave up (it always does).
+ * Asynchronous on `stream`; the context stays usable.  Errors: CTCPB_EINVAL
+ * for nflags < 0 or max_spins out of range, CTCPB_ENULL for a NULL out (or
+ * NULL flags with nflags > 0), CTCPB_ECUDA for a failed launch.
+ */
+int ctcpb_selftest_waits(const uint32_t* flags, int nflags, long long max_spins, uint32_t* out,
+                         ctcpb_stream_t stream);
+
+/*
  * Copy the device status word of a workspace or state to *device_status.
  * Synchronises the device (for tests and error reporting, not the hot path).
  */

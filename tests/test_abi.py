@@ -120,6 +120,12 @@ def test_host_validation_before_any_launch(lib):
     assert lib.ctcpb_stream_step(ctypes.byref(c), big, 1 << 40, 4, 5000, big, 4999, big, NULL) == D.EINVAL
     assert lib.ctcpb_stream_step(ctypes.byref(c), big, 16, 4, 5000, big, 5000, NULL, NULL) == D.ESIZE
     assert lib.ctcpb_stream_step(ctypes.byref(c), NULL, 0, 0, 5000, NULL, 5000, NULL, NULL) == D.OK
+    # wait self-test: counts, spin bounds and pointers are checked before the launch
+    assert lib.ctcpb_selftest_waits(big, -1, 10, big, NULL) == D.EINVAL
+    assert lib.ctcpb_selftest_waits(big, 4, 0, big, NULL) == D.EINVAL
+    assert lib.ctcpb_selftest_waits(big, 4, (1 << 20) + 1, big, NULL) == D.EINVAL
+    assert lib.ctcpb_selftest_waits(NULL, 4, 10, big, NULL) == D.ENULL
+    assert lib.ctcpb_selftest_waits(big, 4, 10, NULL, NULL) == D.ENULL
     assert lib.ctcpb_read_status(NULL, NULL) == D.ENULL
     assert lib.ctcpb_topk_prepass(ctypes.byref(c), NULL, 10, 5, 5000, NULL, NULL, NULL, NULL, NULL, NULL,
                                   NULL) == D.EINVAL
