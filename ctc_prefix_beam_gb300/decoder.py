@@ -21,7 +21,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, EINVAL, ENULL, EALIGN, ESIZE, ECUDA = 0, -1, -2, -3, -4, -5
-DEV_HEADER, DEV_PAGES, DEV_TIMEOUT, DEV_OVERFLOW = 0x1, 0x2, 0x4, 0x8
+DEV_HEADER, DEV_PAGES, DEV_TIMEOUT, DEV_OVERFLOW, DEV_BOOST = 0x1, 0x2, 0x4, 0x8, 0x10
 NEG = -3.4028234663852886e38
 
 
