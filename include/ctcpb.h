@@ -376,12 +376,16 @@ int ctcpb_decode_offline_staged(const ctcpb_config* cfg, const float* log_prob, 
                                 int32_t* out_tokens, int32_t* out_lengths, float* out_scores, int out_len,
                                 uint32_t stage_mask, ctcpb_stream_t stream);
 
-/* Number of labels the pre-pass ranks per frame for this config and V. */
+/* Number of labels the pre-pass ranks per frame for this config and V (>= 1),
+ * or a negative status for an invalid config. */
 int ctcpb_list_len(const ctcpb_config* cfg, int V);
 
 /*
  * Frame selection (section 3.5): sel [B, T] int32 receives the kept frames of
- * each row in order (the rest of the row is -1), nsel [B] their count.
+ * each row in order (the rest of the row is -1), nsel [B] their count.  The
+ * frames, lengths and threshold are read as in ctcpb_decode_offline.  Errors:
+ * CTCPB_EINVAL for B or T < 0 or a stride below V, CTCPB_ENULL for a NULL
+ * nsel (or log_prob or sel with T > 0); B == 0 is a no-op.
  */
 int ctcpb_select_frames(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
                         const int32_t* seq_lengths, int B, int T, int V, int32_t* sel, int32_t* nsel,
@@ -394,7 +398,8 @@ int ctcpb_select_frames(const ctcpb_config* cfg, const float* log_prob, int64_t 
  * with -1 / -FLT_MAX), cnt [R], the blank log-prob lpb [R], and the next
  * ranked label after the list (front_id [R], front_lp [R]; -1 / -FLT_MAX when
  * none).  A label is live iff its log-prob is > -FLT_MAX (NaN and -inf are
- * read as -FLT_MAX).
+ * read as -FLT_MAX).  Errors: CTCPB_EINVAL for R < 0 or stride_r < V,
+ * CTCPB_ENULL for any NULL array; R == 0 is a no-op.
  */
 int ctcpb_topk_prepass(const ctcpb_config* cfg, const float* log_prob, int64_t stride_r, int R, int V,
                        int32_t* ids, float* lps, int32_t* cnt, float* lpb, float* front_lp, int32_t* front_id,
