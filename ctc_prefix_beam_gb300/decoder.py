@@ -139,6 +139,44 @@ def _f32_3d(lp: torch.Tensor) -> torch.Tensor:
     return lp
 
 
+def _cuda_device(device) -> torch.device:
+    """``device`` as an indexed CUDA device (``"cuda"`` is the current one)."""
+    d = torch.device(device)
+    if d.type != "cuda":
+        raise ValueError(f"{device} is not a CUDA device")
+    return d if d.index is not None else torch.device("cuda", torch.cuda.current_device())
+
+
+def _call(dev: torch.device, fn, *args):
+    """Call a library entry point with ``dev`` current: the library launches on
+    the current CUDA device."""
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
+def _check_buf(buf: torch.Tensor, need: int, device: torch.device, what: str) -> int:
+    """A caller's workspace or state: contiguous, on ``device``, at least
+    ``need`` bytes.  Returns its size in bytes."""
+    if not isinstance(buf, torch.Tensor) or buf.device != device or not buf.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous tensor on {device}")
+    nbytes = buf.numel() * buf.element_size()
+    if nbytes < need:
+        raise ValueError(f"{what} holds {nbytes} bytes, {need} are needed")
+    return nbytes
+
+
+def _check_outputs(outputs, B: int, nbest: int, out_len: int, device: torch.device):
+    """Caller-supplied (tokens, lengths, scores): the library writes exactly
+    B*nbest*out_len, B*nbest and B*nbest elements through plain pointers."""
+    tok, ln, sc = outputs
+    for t, dt, n, name in ((tok, torch.int32, B * nbest * out_len, "tokens"), (ln, torch.int32, B * nbest, "lengths"),
+                           (sc, torch.float32, B * nbest, "scores")):
+        if not isinstance(t, torch.Tensor) or t.dtype != dt or t.device != device or not t.is_contiguous() \
+                or t.numel() != n:
+            raise ValueError(f"output {name} must be a contiguous {dt} tensor of {n} elements on {device}")
+    return tok, ln, sc
+
+
 def _alloc(nbytes: int, device) -> torch.Tensor:
     # torch's caching allocator returns 512-byte aligned blocks
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
@@ -217,36 +255,37 @@ def decode_offline(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[to
     the rows' label boosts (``boost_tables``; needs ``cfg.max_boost``).
     """
     lp = _f32_3d(log_prob)
+    dev = lp.device
     B, T, V = lp.shape
     c = cfg.c()
     nbest = c.nbest
     if out_len is None:
         out_len = min(cfg.max_seq_len, T) if cfg.max_seq_len > 0 else T
     if seq_lengths is not None:
-        if seq_lengths.dtype != torch.int32 or not seq_lengths.is_cuda:
-            raise ValueError("seq_lengths must be a CUDA int32 tensor [B]")
+        if seq_lengths.dtype != torch.int32 or seq_lengths.device != dev or seq_lengths.numel() != B:
+            raise ValueError(f"seq_lengths must be an int32 tensor [B] on {dev}")
         seq_lengths = seq_lengths.contiguous()
     need = workspace_size(cfg, B, T, V)
     if workspace is None:
-        workspace = _alloc(need, lp.device)
-    tok, ln, sc = _outputs(B, nbest, out_len, lp.device) if outputs is None else outputs
+        workspace = _alloc(need, dev)
+    ws_bytes = _check_buf(workspace, need, dev, "workspace")
+    tok, ln, sc = _outputs(B, nbest, out_len, dev) if outputs is None else _check_outputs(outputs, B, nbest, out_len,
+                                                                                          dev)
     if boost is not None:
         if stages != STAGE_ALL:
             raise ValueError("a boosted decode runs every stage")
-        tables = boost_tables(boost, B, lp.device)
-        rc = lib().ctcpb_decode_offline_boosted(ctypes.byref(c), ctypes.byref(_boost_arg(tables)), _ptr(lp),
-                                                lp.stride(0), lp.stride(1), _ptr(seq_lengths), B, T, V,
-                                                _ptr(workspace), workspace.numel(), _ptr(tok), _ptr(ln), _ptr(sc),
-                                                out_len, _stream(lp.device))
+        tables = boost_tables(boost, B, dev)
+        rc = _call(dev, lib().ctcpb_decode_offline_boosted, ctypes.byref(c), ctypes.byref(_boost_arg(tables)),
+                   _ptr(lp), lp.stride(0), lp.stride(1), _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes,
+                   _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
     elif stages == STAGE_ALL:
-        rc = lib().ctcpb_decode_offline(ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
-                                        _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
-                                        _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(lp.device))
+        rc = _call(dev, lib().ctcpb_decode_offline, ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
+                   _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln), _ptr(sc), out_len,
+                   _stream(dev))
     else:
-        rc = lib().ctcpb_decode_offline_staged(ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
-                                               _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
-                                               _ptr(tok), _ptr(ln), _ptr(sc), out_len, stages,
-                                               _stream(lp.device))
+        rc = _call(dev, lib().ctcpb_decode_offline_staged, ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
+                   _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln), _ptr(sc), out_len,
+                   stages, _stream(dev))
     _check(rc, "decode_offline")
     return tok, ln, sc
 
@@ -276,29 +315,29 @@ def decode_offline_host(cfg: Config, log_prob: torch.Tensor, seq_lengths: Option
     if out_len is None:
         out_len = min(cfg.max_seq_len, T) if cfg.max_seq_len > 0 else T
     if seq_lengths is not None:
-        if seq_lengths.dtype != torch.int32 or seq_lengths.is_cuda:
+        if seq_lengths.dtype != torch.int32 or seq_lengths.is_cuda or seq_lengths.numel() != B:
             raise ValueError("seq_lengths must be a host int32 tensor [B]")
         seq_lengths = seq_lengths.contiguous()
-    dev = torch.device(device)
+    dev = _cuda_device(device)
     need = host_workspace_size(cfg, B, T, V, out_len)
     if workspace is None:
         workspace = _alloc(need, dev)
+    ws_bytes = _check_buf(workspace, need, dev, "workspace")
     if outputs is None:
         pin = log_prob.is_pinned()
         outputs = (torch.empty((B, c.nbest, out_len), dtype=torch.int32, pin_memory=pin),
                    torch.empty((B, c.nbest), dtype=torch.int32, pin_memory=pin),
                    torch.empty((B, c.nbest), dtype=torch.float32, pin_memory=pin))
-    tok, ln, sc = outputs
+    tok, ln, sc = _check_outputs(outputs, B, c.nbest, out_len, torch.device("cpu"))
     if boost is not None:
         tables = boost_tables(boost, B, dev)
-        rc = lib().ctcpb_decode_offline_host_boosted(ctypes.byref(c), ctypes.byref(_boost_arg(tables)),
-                                                     _ptr(log_prob), log_prob.stride(0), log_prob.stride(1),
-                                                     _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
-                                                     _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
+        rc = _call(dev, lib().ctcpb_decode_offline_host_boosted, ctypes.byref(c), ctypes.byref(_boost_arg(tables)),
+                   _ptr(log_prob), log_prob.stride(0), log_prob.stride(1), _ptr(seq_lengths), B, T, V,
+                   _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
     else:
-        rc = lib().ctcpb_decode_offline_host(ctypes.byref(c), _ptr(log_prob), log_prob.stride(0), log_prob.stride(1),
-                                             _ptr(seq_lengths), B, T, V, _ptr(workspace), workspace.numel(),
-                                             _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
+        rc = _call(dev, lib().ctcpb_decode_offline_host, ctypes.byref(c), _ptr(log_prob), log_prob.stride(0),
+                   log_prob.stride(1), _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln),
+                   _ptr(sc), out_len, _stream(dev))
     _check(rc, "decode_offline_host")
     if synchronize:
         torch.cuda.current_stream(dev).synchronize()
@@ -311,67 +350,86 @@ class StreamState:
     def __init__(self, cfg: Config, B: int, V: int, device="cuda"):
         self.cfg, self.B, self.V = cfg, B, V
         self.nbytes = state_size(cfg, B, V)
-        self.buf = _alloc(self.nbytes, device)
+        self.buf = _alloc(self.nbytes, _cuda_device(device))
         self.init()
 
+    def _state(self):
+        """(device, state bytes) of the buffer, checked before every call."""
+        dev = self.buf.device
+        return dev, _check_buf(self.buf, self.nbytes, dev, "state")
+
+    def _on(self, t: Optional[torch.Tensor], dev: torch.device, what: str):
+        if t is not None and t.device != dev:
+            raise ValueError(f"{what} must be on the state's device {dev}")
+
     def init(self):
-        _check(lib().ctcpb_stream_init(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
-                                       self.V, _stream(self.buf.device)), "stream_init")
+        dev, nb = self._state()
+        _check(_call(dev, lib().ctcpb_stream_init, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb, self.B, self.V,
+                     _stream(dev)), "stream_init")
 
     def set_boost(self, boost):
         """Replace every stream's label boosts (``boost_tables``) from the next frame on."""
-        tables = boost_tables(boost, self.B, self.buf.device)
-        _check(lib().ctcpb_stream_set_boost(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
-                                            self.V, ctypes.byref(_boost_arg(tables)), _stream(self.buf.device)),
-               "stream_set_boost")
+        dev, nb = self._state()
+        tables = boost_tables(boost, self.B, dev)
+        _check(_call(dev, lib().ctcpb_stream_set_boost, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb, self.B,
+                     self.V, ctypes.byref(_boost_arg(tables)), _stream(dev)), "stream_set_boost")
 
     def step_chunk(self, lp_chunk: torch.Tensor, n_frames: Optional[torch.Tensor] = None,
                    is_speech: Optional[torch.Tensor] = None):
-        """Decode one chunk [B, chunk_T, V] for every stream.  ``is_speech``
-        (CUDA uint8 [B, chunk_T]) skips the frames it marks 0."""
+        """Decode one chunk [B, chunk_T, V] for every stream.  ``n_frames``
+        (CUDA int32 [B]) limits stream b to its first n_frames[b] rows;
+        ``is_speech`` (CUDA uint8 [B, chunk_T]) skips the frames it marks 0."""
+        dev, nb = self._state()
         lp = _f32_3d(lp_chunk)
+        self._on(lp, dev, "the chunk")
         if lp.shape[0] != self.B or lp.shape[2] != self.V:
             raise ValueError("chunk must be [B, chunk_T, V] for this state")
         if n_frames is not None:
-            if n_frames.dtype != torch.int32 or not n_frames.is_cuda:
-                raise ValueError("n_frames must be a CUDA int32 tensor [B]")
+            if n_frames.dtype != torch.int32 or n_frames.numel() != self.B:
+                raise ValueError("n_frames must be an int32 tensor [B]")
+            self._on(n_frames, dev, "n_frames")
             n_frames = n_frames.contiguous()
         if is_speech is not None:
-            if is_speech.dtype != torch.uint8 or not is_speech.is_cuda or is_speech.dim() != 2 \
-                    or is_speech.shape[0] != self.B or is_speech.shape[1] < lp.shape[1] or is_speech.stride(1) != 1:
-                raise ValueError("is_speech must be a CUDA uint8 tensor [B, >= chunk_T] with unit column stride")
-            _check(lib().ctcpb_stream_step_chunk_masked(
-                ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B, self.V, _ptr(lp), lp.stride(0),
-                lp.stride(1), _ptr(n_frames), _ptr(is_speech), is_speech.stride(0), lp.shape[1],
-                _stream(lp.device)), "stream_step_chunk_masked")
+            if is_speech.dtype != torch.uint8 or is_speech.dim() != 2 or is_speech.shape[0] != self.B \
+                    or is_speech.shape[1] < lp.shape[1] or is_speech.stride(1) != 1:
+                raise ValueError("is_speech must be a uint8 tensor [B, >= chunk_T] with unit column stride")
+            self._on(is_speech, dev, "is_speech")
+            _check(_call(dev, lib().ctcpb_stream_step_chunk_masked, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb,
+                         self.B, self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames), _ptr(is_speech),
+                         is_speech.stride(0), lp.shape[1], _stream(dev)), "stream_step_chunk_masked")
             return
-        _check(lib().ctcpb_stream_step_chunk(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B,
-                                             self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames),
-                                             lp.shape[1], _stream(lp.device)), "stream_step_chunk")
+        _check(_call(dev, lib().ctcpb_stream_step_chunk, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb, self.B,
+                     self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames), lp.shape[1], _stream(dev)),
+               "stream_step_chunk")
 
     def step(self, lp_frame: torch.Tensor, is_speech: Optional[torch.Tensor] = None):
         """Decode one frame [B, V] for every stream.  ``is_speech`` (CUDA uint8
         [B]) skips the streams it marks 0; their frame counters still advance."""
+        dev, nb = self._state()
         if lp_frame.dtype != torch.float32 or not lp_frame.is_cuda or lp_frame.dim() != 2:
             raise ValueError("frame must be a CUDA float32 tensor [B, V]")
         lp = lp_frame if lp_frame.stride(1) == 1 else lp_frame.contiguous()
+        self._on(lp, dev, "the frame")
         if lp.shape[0] != self.B or lp.shape[1] != self.V:
             raise ValueError("frame must be [B, V] for this state")
         if is_speech is not None:
-            if is_speech.dtype != torch.uint8 or not is_speech.is_cuda or is_speech.shape != (self.B,):
-                raise ValueError("is_speech must be a CUDA uint8 tensor [B]")
+            if is_speech.dtype != torch.uint8 or is_speech.shape != (self.B,):
+                raise ValueError("is_speech must be a uint8 tensor [B]")
+            self._on(is_speech, dev, "is_speech")
             is_speech = is_speech.contiguous()
-        _check(lib().ctcpb_stream_step(ctypes.byref(self.cfg.c()), _ptr(self.buf), self.buf.numel(), self.B, self.V,
-                                       _ptr(lp), lp.stride(0), _ptr(is_speech), _stream(lp.device)), "stream_step")
+        _check(_call(dev, lib().ctcpb_stream_step, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb, self.B, self.V,
+                     _ptr(lp), lp.stride(0), _ptr(is_speech), _stream(dev)), "stream_step")
 
     def read(self, out_len: Optional[int] = None, outputs=None):
+        """The current N best of every stream; the state is not modified."""
+        dev, nb = self._state()
         c = self.cfg.c()
         if out_len is None:
             out_len = self.cfg.max_seq_len if self.cfg.max_seq_len > 0 else 4096
-        tok, ln, sc = _outputs(self.B, c.nbest, out_len, self.buf.device) if outputs is None else outputs
-        _check(lib().ctcpb_read_state(ctypes.byref(c), _ptr(self.buf), self.buf.numel(), self.B, self.V,
-                                      _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(self.buf.device)),
-               "read_state")
+        tok, ln, sc = _outputs(self.B, c.nbest, out_len, dev) if outputs is None else \
+            _check_outputs(outputs, self.B, c.nbest, out_len, dev)
+        _check(_call(dev, lib().ctcpb_read_state, ctypes.byref(c), _ptr(self.buf), nb, self.B, self.V, _ptr(tok),
+                     _ptr(ln), _ptr(sc), out_len, _stream(dev)), "read_state")
         return tok, ln, sc
 
     def status(self) -> int:
@@ -380,7 +438,7 @@ class StreamState:
 
 def read_status(buf: torch.Tensor) -> int:
     v = ctypes.c_uint32()
-    _check(lib().ctcpb_read_status(_ptr(buf), ctypes.byref(v)), "read_status")
+    _check(_call(buf.device, lib().ctcpb_read_status, _ptr(buf), ctypes.byref(v)), "read_status")
     return v.value
 
 
@@ -392,25 +450,29 @@ def selftest_waits(flags: torch.Tensor, max_spins: int = 1000) -> tuple:
         raise ValueError("flags must be a 1-D CUDA int32 tensor (read as uint32)")
     flags = flags.contiguous()
     out = torch.zeros(3, dtype=torch.int32, device=flags.device)
-    _check(lib().ctcpb_selftest_waits(_ptr(flags), flags.numel(), max_spins, _ptr(out), _stream(flags.device)),
-           "selftest_waits")
+    _check(_call(flags.device, lib().ctcpb_selftest_waits, _ptr(flags), flags.numel(), max_spins, _ptr(out),
+                 _stream(flags.device)), "selftest_waits")
     return tuple(int(v) for v in out.cpu())
 
 
 def read_counters(buf: torch.Tensor) -> dict:
     v = (ctypes.c_uint32 * 6)()
-    _check(lib().ctcpb_read_counters(_ptr(buf), v), "read_counters")
+    _check(_call(buf.device, lib().ctcpb_read_counters, _ptr(buf), v), "read_counters")
     return dict(steps=v[0], unproven=v[1], exhaustive=v[2], frame_scans=v[3], hash_merges=v[4], fused=v[5])
 
 
 def select_frames(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[torch.Tensor] = None):
     lp = _f32_3d(log_prob)
+    dev = lp.device
     B, T, V = lp.shape
-    sel = torch.empty((B, T), dtype=torch.int32, device=lp.device)
-    nsel = torch.empty((B,), dtype=torch.int32, device=lp.device)
-    _check(lib().ctcpb_select_frames(ctypes.byref(cfg.c()), _ptr(lp), lp.stride(0), lp.stride(1),
-                                     _ptr(seq_lengths), B, T, V, _ptr(sel), _ptr(nsel), _stream(lp.device)),
-           "select_frames")
+    if seq_lengths is not None:
+        if seq_lengths.dtype != torch.int32 or seq_lengths.device != dev or seq_lengths.numel() != B:
+            raise ValueError(f"seq_lengths must be an int32 tensor [B] on {dev}")
+        seq_lengths = seq_lengths.contiguous()
+    sel = torch.empty((B, T), dtype=torch.int32, device=dev)
+    nsel = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(_call(dev, lib().ctcpb_select_frames, ctypes.byref(cfg.c()), _ptr(lp), lp.stride(0), lp.stride(1),
+                 _ptr(seq_lengths), B, T, V, _ptr(sel), _ptr(nsel), _stream(dev)), "select_frames")
     return sel, nsel
 
 
@@ -427,7 +489,6 @@ def topk_prepass(cfg: Config, rows: torch.Tensor):
     lpb = torch.empty((R,), dtype=torch.float32, device=dev)
     flp = torch.empty((R,), dtype=torch.float32, device=dev)
     fid = torch.empty((R,), dtype=torch.int32, device=dev)
-    _check(lib().ctcpb_topk_prepass(ctypes.byref(cfg.c()), _ptr(rows), rows.stride(0), R, V, _ptr(ids),
-                                    _ptr(lps), _ptr(cnt), _ptr(lpb), _ptr(flp), _ptr(fid), _stream(dev)),
-           "topk_prepass")
+    _check(_call(dev, lib().ctcpb_topk_prepass, ctypes.byref(cfg.c()), _ptr(rows), rows.stride(0), R, V, _ptr(ids),
+                 _ptr(lps), _ptr(cnt), _ptr(lpb), _ptr(flp), _ptr(fid), _stream(dev)), "topk_prepass")
     return dict(ids=ids, lps=lps, cnt=cnt, lpb=lpb, front_lp=flp, front_id=fid)

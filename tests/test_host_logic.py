@@ -91,3 +91,29 @@ def test_config_maps_the_word_boundary_label():
     assert (c.beam, c.nbest, c.word_boundary) == (8, 3, 0)
     c = D.Config(beam=8, space_id=5).c()
     assert (c.word_boundary, c.space_id, c.nbest) == (1, 5, 8)
+
+
+def test_caller_buffers_are_validated():
+    """The library writes through plain pointers, so the binding checks every
+    caller-supplied buffer: outputs of exactly the written sizes and types,
+    workspaces of enough bytes, all on the call's device."""
+    cpu = torch.device("cpu")
+    good = (torch.empty((2, 3, 5), dtype=torch.int32), torch.empty((2, 3), dtype=torch.int32),
+            torch.empty((2, 3), dtype=torch.float32))
+    assert D._check_outputs(good, 2, 3, 5, cpu) is good
+    bad = [(torch.empty((2, 3, 4), dtype=torch.int32),) + good[1:],              # too short
+           (good[0], torch.empty((2, 3), dtype=torch.int64), good[2]),            # wrong type
+           (good[0], good[1], torch.empty((3, 2), dtype=torch.float32).t()),      # not contiguous
+           good[:2] + (torch.empty((2, 4), dtype=torch.float32),)]                 # too long
+    for outs in bad:
+        with pytest.raises(ValueError):
+            D._check_outputs(outs, 2, 3, 5, cpu)
+    ws = torch.empty(1024, dtype=torch.uint8)
+    assert D._check_buf(ws, 1000, cpu, "workspace") == 1024
+    assert D._check_buf(torch.empty(256, dtype=torch.float32), 1000, cpu, "workspace") == 1024
+    with pytest.raises(ValueError):
+        D._check_buf(ws, 2048, cpu, "workspace")
+    with pytest.raises(ValueError):
+        D._check_buf(ws[::2], 100, cpu, "workspace")
+    with pytest.raises(ValueError):
+        D._cuda_device("cpu")
