@@ -100,7 +100,7 @@ def test_caller_buffers_are_validated():
     cpu = torch.device("cpu")
     good = (torch.empty((2, 3, 5), dtype=torch.int32), torch.empty((2, 3), dtype=torch.int32),
             torch.empty((2, 3), dtype=torch.float32))
-    assert D._check_outputs(good, 2, 3, 5, cpu) is good
+    assert all(a is b for a, b in zip(D._check_outputs(good, 2, 3, 5, cpu), good))
     bad = [(torch.empty((2, 3, 4), dtype=torch.int32),) + good[1:],              # too short
            (good[0], torch.empty((2, 3), dtype=torch.int64), good[2]),            # wrong type
            (good[0], good[1], torch.empty((3, 2), dtype=torch.float32).t()),      # not contiguous
