@@ -1,7 +1,8 @@
 """Seeded random sweep of the oracle against the float64 enumeration of every
 alignment ("GPU CTC Prefix Beam Search Decoder", sections 3.1-3.5): tiny
 vocabularies and lengths with every option combined -- the blank id, a cap,
-frame skipping by threshold, a word-boundary label, label bonuses -- decoded
+frame skipping by threshold, a speech mask, a word-boundary label, label
+bonuses -- decoded
 with a beam wide enough to hold every reachable prefix, so the N best must be
 the exact posteriors."""
 import math
@@ -34,6 +35,8 @@ def draw(seed):
         opt["space"] = int(rng.choice(labels))
     if rng.random() < 0.3 and labels:
         opt["bonus"] = {int(c): float(np.float32(rng.uniform(-2, 2))) for c in labels if rng.random() < 0.7}
+    if rng.random() < 0.3:
+        opt["mask"] = (rng.random(T) < 0.7).astype(np.uint8)
     return lp, blank, opt
 
 
@@ -42,14 +45,17 @@ def test_unpruned_decode_equals_enumeration(seed):
     lp, blank, opt = draw(seed)
     T, V = lp.shape
     frames, kept = lp, list(range(T))
-    if "thr" in opt:
-        frames, kept = skip_augmented(lp, blank, opt["thr"])
+    if "thr" in opt or "mask" in opt:  # the kept frames: below the threshold and marked as speech
+        kept = skip_augmented(lp, blank, opt.get("thr", 1.0))[1]
+        if "mask" in opt:
+            kept = [t for t in kept if opt["mask"][t]]
+        frames, kept = skip_augmented(lp, blank, 1.0, kept=kept)
     exact = posteriors(frames, blank, cap=opt.get("cap"), space=opt.get("space"), bonus=opt.get("bonus"))
     if not kept:  # every frame skipped: the empty prefix with score 0
         exact = {(): 0.0}
     beam = min(128, max(V, sum((V - 1) ** k for k in range(len(kept) + 1))))
     tok, ln, sc = O.decode(lp[None], None, beam=beam, blank=blank, cap=opt.get("cap", T), thr=opt.get("thr", 1.0),
-                           space=opt.get("space", -1),
+                           space=opt.get("space", -1), mask=None if "mask" not in opt else opt["mask"][None],
                            boost=None if "bonus" not in opt else [opt["bonus"]])
     got = {}
     for n in range(ln.shape[1]):
