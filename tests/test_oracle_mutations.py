@@ -1,10 +1,11 @@
 """The oracle's pins catch plausible mistakes.  Each case plants one mistake
 in a copy of oracle/ctcpb_oracle.cpp (a dropped term, a wrong path, a wrong
-coefficient, an off-by-one), compiles it into a temporary library, and runs
+coefficient, an off-by-one, a reversed tie-break), compiles it into a temporary library, and runs
 the independent pins on it: exp/log1p/lse against float64, and the unpruned
 decode against the float64 enumeration of every alignment, plain and with a
 cap, frame skipping, a word-boundary label and label bonuses ("GPU CTC Prefix
-Beam Search Decoder", sections 3.1-3.5).  The real oracle passes every pin;
+Beam Search Decoder", sections 3.1-3.5), and the hand-derived tie cases of
+tests/tie_cases.py (sections 3.3, 3.4.4-3.4.6).  The real oracle passes every pin;
 every mutant must fail at least one."""
 import subprocess
 
@@ -12,6 +13,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+import tie_cases
 from bruteforce import NEG32, posteriors, skip_augmented
 
 NEG = np.float32(NEG32)
@@ -84,6 +86,9 @@ def pins_hold():
     lp = frames(41, 4, 3)
     bonus = {1: 1.25, 2: -0.5}
     res["bonus"] = unpruned_matches(lp, posteriors(lp, 0, bonus=bonus), boost=[bonus])
+    # the tie-break rule and step 0's slot order, on hand-derived decodes
+    res.update(tie_cases.check(lambda lp, beam, nbest, blank: O.decode(lp, None, beam=beam, nbest=nbest,
+                                                                       blank=blank)))
     return res
 
 
@@ -114,14 +119,34 @@ MUTATIONS = {
     "log1p: wrong series coefficient": ("q = std::fmaf(q, z, (float)(1.0 / 3.0));",
                                         "q = std::fmaf(q, z, (float)(1.0 / 4.0));"),
     "lse: signed difference": ("float d = std::fabs(a - b);", "float d = a - b;"),
+    "ties: source slot descending": ("if (x.src != y.src) return x.src < y.src;",
+                                     "if (x.src != y.src) return x.src > y.src;"),
+    "ties: token descending": ("return x.tok < y.tok;", "return x.tok > y.tok;"),
+    "ties: source slot and token both descending": (
+        "if (x.src != y.src) return x.src < y.src;\n  return x.tok < y.tok;",
+        "if (x.src != y.src) return x.src > y.src;\n  return x.tok > y.tok;"),
+    "ties: the blank slot ranks after every label": [
+        ("if (sc > NEG) cands.push_back(Cand{sc, k, a.blank, bpb, bpnb});",
+         "if (sc > NEG) cands.push_back(Cand{sc, k, a.V, bpb, bpnb});"),
+        ("if (c.tok != a.blank) h.pre.push_back(c.tok);",
+         "if (c.tok != a.blank && c.tok != a.V) h.pre.push_back(c.tok);")],
+    "step 0: the empty prefix in the first slot": (
+        "if (lpb > NEG) beams.push_back(Hyp{{}, lpb, NEG});",
+        "if (lpb > NEG) beams.insert(beams.begin(), Hyp{{}, lpb, NEG});"),
+    "step 0: equal labels by id descending": ("return a.second < b.second;", "return a.second > b.second;"),
+    "output: equal scores in reverse slot order": (
+        "[&](int x, int y) { return sc[x] > sc[y]; }",
+        "[&](int x, int y) { return sc[x] > sc[y] || (sc[x] == sc[y] && x > y); }"),
 }
 
 
-def build_variant(tmp_path, old, new):
+def build_variant(tmp_path, edits):
     src = open(O._SRC).read()
-    assert src.count(old) == 1, old
+    for old, new in edits:
+        assert src.count(old) == 1, old
+        src = src.replace(old, new)
     path = tmp_path / "mutant.cpp"
-    path.write_text(src.replace(old, new))
+    path.write_text(src)
     lib = str(tmp_path / "libmutant.so")
     cmd = O.build_cmd()
     cmd[cmd.index(O._LIB)] = lib
@@ -142,8 +167,8 @@ def test_the_oracle_passes_every_pin():
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_mistake_fails_a_pin(name, tmp_path, monkeypatch):
-    old, new = MUTATIONS[name]
-    use_library(monkeypatch, build_variant(tmp_path, old, new))
+    edits = MUTATIONS[name]
+    use_library(monkeypatch, build_variant(tmp_path, edits if isinstance(edits, list) else [edits]))
     try:
         res = pins_hold()
     except (AssertionError, ValueError, FloatingPointError):
