@@ -81,17 +81,29 @@ int check_boost(const ctcpb_config* c, const ctcpb_boost* bo) {
 
 // Pre-pass and steps of one tile in one cooperative launch when the device and
 // the problem allow it; CTCPB_NO_FUSE=1 in the environment turns it off.
-bool try_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
-               int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
+// Returns 1 when launched, 0 when not available (the caller launches the two
+// kernels one after the other), CTCPB_ECUDA on a real CUDA failure.
+int try_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
+              int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   static const bool off = [] {
     const char* e = std::getenv("CTCPB_NO_FUSE");
     return e && e[0] == '1';
   }();
-  if (off) return false;
-  if (launch_fused(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s) == cudaSuccess) return true;
-  cudaGetLastError();  // a refused cooperative launch: take the two-kernel path
-  return false;
+  if (off) return 0;
+  const cudaError_t e = launch_fused(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, s);
+  if (e == cudaSuccess) return 1;
+  return e == cudaErrorNotSupported ? 0 : CTCPB_ECUDA;
 }
+
+#define FUSED_OR_TWO_KERNELS(st, lp, sb, stt, mode, nf, cT, t0, tl, s)                     \
+  do {                                                                                    \
+    const int f_ = try_fused(st, lp, sb, stt, mode, nf, cT, t0, tl, s);                    \
+    if (f_ < 0) return f_;                                                                \
+    if (f_ == 0) {                                                                        \
+      TRY(launch_prepass(st, lp, sb, stt, mode, nf, cT, t0, tl, s));                       \
+      TRY(launch_step(st, lp, sb, stt, mode, nf, cT, t0, tl, s));                          \
+    }                                                                                     \
+  } while (0)
 
 }  // namespace
 
@@ -156,7 +168,9 @@ int decode_offline_impl(const ctcpb_config* cfg, const ctcpb_boost* boost, const
     if (stage_mask & CTCPB_STAGE_SELECT)
       TRY(launch_select(st, log_prob, stride_b, stride_t, seq_lengths, T, mode, log_thr, st.sel(), st.nsel(), s));
     const bool both = (stage_mask & CTCPB_STAGE_RANK) && (stage_mask & CTCPB_STAGE_STEPS);
-    if (!(both && try_fused(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s))) {
+    const int fused = both ? try_fused(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s) : 0;
+    if (fused < 0) return fused;
+    if (fused == 0) {
       if (stage_mask & CTCPB_STAGE_RANK) TRY(launch_prepass(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s));
       if (stage_mask & CTCPB_STAGE_STEPS) TRY(launch_step(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s));
     }
@@ -241,9 +255,7 @@ int ctcpb_stream_step_chunk(const ctcpb_config* cfg, void* state, size_t state_b
   cudaStream_t s = (cudaStream_t)stream;
   for (int t0 = 0; t0 < chunk_T; t0 += kStreamTile) {
     const int tl = chunk_T - t0 < kStreamTile ? chunk_T - t0 : kStreamTile;
-    if (try_fused(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s)) continue;
-    TRY(launch_prepass(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s));
-    TRY(launch_step(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s));
+    FUSED_OR_TWO_KERNELS(st, lp_chunk, stride_b, stride_t, 1, n_frames, chunk_T, t0, tl, s);
   }
   return CTCPB_OK;
 }
@@ -265,9 +277,7 @@ int ctcpb_stream_step_chunk_masked(const ctcpb_config* cfg, void* state, size_t 
   for (int t0 = 0; t0 < chunk_T; t0 += kStreamTile) {
     const int tl = chunk_T - t0 < kStreamTile ? chunk_T - t0 : kStreamTile;
     TRY(launch_select_tile(st, is_speech, mask_stride, n_frames, chunk_T, t0, tl, s));
-    if (try_fused(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s)) continue;
-    TRY(launch_prepass(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s));
-    TRY(launch_step(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s));
+    FUSED_OR_TWO_KERNELS(st, lp_chunk, stride_b, stride_t, 2, n_frames, chunk_T, t0, tl, s);
   }
   return CTCPB_OK;
 }
@@ -536,9 +546,7 @@ int decode_offline_host_impl(const ctcpb_config* cfg, const ctcpb_boost* boost, 
     for (int t0 = 0; t0 < F; t0 += kStreamTile) {  // the chunk's streaming tiles
       const int tl = F - t0 < kStreamTile ? F - t0 : kStreamTile;
       if (!all) TRY(launch_select_tile_thr(st, buf, dsb, V, log_thr, nf, F, t0, tl, s));
-      if (try_fused(st, buf, dsb, V, mode, nf, F, t0, tl, s)) continue;
-      TRY(launch_prepass(st, buf, dsb, V, mode, nf, F, t0, tl, s));
-      TRY(launch_step(st, buf, dsb, V, mode, nf, F, t0, tl, s));
+      FUSED_OR_TWO_KERNELS(st, buf, dsb, V, mode, nf, F, t0, tl, s);
     }
     TRY(cudaEventRecord(R->done[k], s));
   }

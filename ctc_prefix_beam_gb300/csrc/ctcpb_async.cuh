@@ -7,6 +7,7 @@
 namespace ctcpb {
 
 constexpr long long kWaitSpins = 1ll << 18;  // bounded mbarrier wait (each try sleeps <= 2 us)
+constexpr int kExitWaits = 8;  // further bounded waits for a copy in flight before a warp exits on a timeout
 
 __device__ __forceinline__ unsigned saddr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ void mbar_init(u64* bar) {

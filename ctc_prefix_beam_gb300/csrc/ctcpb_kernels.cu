@@ -1364,12 +1364,8 @@ static cudaError_t launch_step_t(const View& st, const float* lp, long long sb, 
   // records are copied whole into shared memory in 16-byte words
   if (st.lay.rec_bytes > (size_t)StepSmem<NT>::kRecMax || (st.lay.rec_bytes & 15) != 0) return cudaErrorInvalidValue;
   const size_t smem = step_smem_bytes<NT>(sortcap);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_step<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = smem_optin<k_step<NT>>(smem);
+  if (e != cudaSuccess) return e;
   k_step<NT><<<st.lay.B, NT, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len, sortcap);
   return cudaGetLastError();
 }

@@ -1,9 +1,31 @@
 // Host-side launchers of the decoder kernels (ctcpb_kernels.cu).
 #pragma once
 
+#include <mutex>
+
 #include "ctcpb_internal.cuh"
 
 namespace ctcpb {
+
+// Raise kernel K's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The limit is an attribute of the kernel on each device, so
+// it is set once per device (and again when a launch needs more); the mutex
+// makes first launches from several host threads safe.
+template <auto K>
+cudaError_t smem_optin(size_t bytes) {
+  constexpr int kDevices = 128;
+  static std::mutex mu;
+  static size_t done[kDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const bool known = dev >= 0 && dev < kDevices;
+  if (known && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && known) done[dev] = bytes;
+  return e;
+}
 
 cudaError_t launch_init(const View& st, cudaStream_t s);
 // Every row's label-boost hash table from compressed-row (row_ptr, tokens, bonus) device arrays.
@@ -27,8 +49,10 @@ cudaError_t launch_step(const View& st, const float* lp, long long sb, long long
                         int chunk_T, int tile_start, int tile_len, cudaStream_t s);
 // Pre-pass and steps of one tile in a single cooperative launch (the pre-pass
 // publishes records that the step warps consume as they arrive).  Returns
-// cudaErrorNotSupported when the problem or the device does not allow it;
-// the caller then launches the two kernels one after the other.
+// cudaErrorNotSupported, launching nothing and leaving no error pending, when
+// the problem or the device does not allow it (a cooperative grid too large
+// for the device included); the caller then launches the two kernels one
+// after the other.  Any other error is a real failure.
 cudaError_t launch_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,
                          int chunk_T, int tile_start, int tile_len, cudaStream_t s);
 bool rank_tma_ok(const float* lp, long long s1, long long s2, int V, int L);

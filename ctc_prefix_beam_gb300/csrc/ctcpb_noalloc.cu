@@ -1,15 +1,15 @@
 // Offline decode that allocates nothing (ctcpb_decode_offline_noalloc).
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA
-// stream capture that must not allocate, plugins of engines that own the
-// device heap and forbid outside allocation, and real-time paths that may not
-// block in the allocator.  For them the decode's workspace lives in a
+// Some callers cannot call cudaMalloc at all: plugins of engines that own the
+// device heap and forbid allocations from outside it, and real-time paths that
+// may not block in the allocator.  For them the decode's workspace lives in a
 // file-scope device array of fixed size that every device loading this
 // library holds until the process exits.
 //
 // Host code cannot use the array's name as a device address (it names a host
 // stand-in), so the first call on each device looks the address up with
-// cudaGetSymbolAddress while that device is current, and caches it.
+// cudaGetSymbolAddress while that device is current, and caches it (the
+// cached address does not survive cudaDeviceReset).
 #include <mutex>
 
 #include "ctcpb.h"
@@ -55,4 +55,14 @@ extern "C" int ctcpb_decode_offline_noalloc(const ctcpb_config* cfg, const float
   return ctcpb_decode_offline(cfg, log_prob, stride_b, stride_t, seq_lengths, B, T, V, ws,
                               (size_t)CTCPB_NOALLOC_SCRATCH_BYTES, out_tokens, out_lengths, out_scores, out_len,
                               stream);
+}
+
+// The status word of the array's header: the CTCPB_DEV_* bits of the last
+// decode on the current device (synchronises the device).
+extern "C" int ctcpb_noalloc_read_status(uint32_t* device_status) {
+  if (!device_status) return CTCPB_ENULL;
+  void* ws = nullptr;
+  int rc = scratch_address(&ws);
+  if (rc != CTCPB_OK) return rc;
+  return ctcpb_read_status(ws, device_status);
 }

@@ -487,7 +487,12 @@ __device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int b
   while (have) {
     if (!mbar_wait(bar, phase)) {
       if (lane == 0 && status) atomicOr(status, CTCPB_DEV_TIMEOUT);
-      mbar_wait(bar, phase);  // a last bounded chance for the copy in flight
+      // A warp has one bulk copy in flight at most (the next row's is issued
+      // only after this one is read), and it issues no other after a timeout.
+      // Before the warp retires, that copy must land in its shared memory:
+      // wait for it again, each wait bounded, the last giving up for good.
+      for (int i = 0; i < kExitWaits && !mbar_wait(bar, phase); ++i) {
+      }
       return;
     }
     phase ^= 1u;

@@ -1029,12 +1029,8 @@ template <int KB, bool BOOST>
 static cudaError_t launch_kb(const View& st, const float* lp, long long sb, long long stt, int mode,
                              const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   const size_t smem = step_warp_smem_bytes();
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_step_warp<KB, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = smem_optin<k_step_warp<KB, BOOST>>(smem);
+  if (e != cudaSuccess) return e;
   const int blocks = (st.lay.B + kWPC - 1) / kWPC;
   k_step_warp<KB, BOOST><<<blocks, 32 * kWPC, smem, s>>>(st, lp, sb, stt, mode, nframes, chunk_T, tile_start, tile_len);
   return cudaGetLastError();
@@ -1056,30 +1052,32 @@ static cudaError_t launch_fused_kb(const View& st, const float* lp, long long sb
                                   const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s) {
   const Layout& Ly = st.lay;
   int dev = 0, coop = 0, sms = 0, maxsm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
   int rw = rank_tma_warps(Ly.V);
   if (rw > 8) rw = 8;
   const size_t rank_smem = rank_tma_per_warp(Ly.V) * (size_t)rw;
   const size_t smem = rank_smem > step_warp_smem_bytes() ? rank_smem : step_warp_smem_bytes();
   if (!coop || rw < 1 || smem > (size_t)maxsm) return cudaErrorNotSupported;
-  static size_t attr_smem = 0;
-  if (attr_smem != smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_fused<KB, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_smem = smem;
-  }
+  e = smem_optin<k_fused<KB, BOOST>>(smem);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<KB, BOOST>, 256, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_fused<KB, BOOST>, 256, smem);
   if (e != cudaSuccess) return e;
   const int grid = per_sm * sms;
   int nsb = (Ly.B + kWPC - 1) / kWPC;
   if (per_sm < 1 || nsb + 8 > grid) return cudaErrorNotSupported;  // keep at least 8 ranking blocks
   View stv = st;
   void* args[] = {&stv, (void*)&lp, &sb, &stt, &mode, (void*)&nframes, &chunk_T, &tile_start, &tile_len, &nsb, &rw};
-  return cudaLaunchCooperativeKernel((const void*)k_fused<KB, BOOST>, grid, 256, args, smem, s);
+  e = cudaLaunchCooperativeKernel((const void*)k_fused<KB, BOOST>, grid, 256, args, smem, s);
+  if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
+    cudaGetLastError();  // this launch's own refusal, just recorded: consume it
+    return cudaErrorNotSupported;
+  }
+  return e;
 }
 
 cudaError_t launch_fused(const View& st, const float* lp, long long sb, long long stt, int mode, const int* nframes,

@@ -223,28 +223,35 @@ int ctcpb_decode_offline_host_boosted(const ctcpb_config* cfg, const ctcpb_boost
                                       float* out_scores, int out_len, ctcpb_stream_t stream);
 
 /*
- * Offline decode for callers that cannot allocate device memory./*
  * Offline decode for callers that cannot allocate device memory.  The pages
- * have no counterpart: it exists for code that may not call cudaMalloc (inside
- * a stream capture that must stay allocation-free, in an engine plugin whose
- * host owns the device heap, on a real-time path that must not block in the
- * allocator).  Same arguments and results as ctcpb_decode_offline without the
- * workspace: the workspace is a fixed device array of
- * CTCPB_NOALLOC_SCRATCH_BYTES inside this library, held by every device that
- * loads the library until the process exits.
+ * have no counterpart.  It is for code that may not call cudaMalloc: a plugin
+ * of an engine that owns the device heap and forbids allocations from outside
+ * it, or a real-time path that must not block in the allocator.  Same
+ * arguments and results as ctcpb_decode_offline without the workspace: the
+ * workspace is a fixed device array of CTCPB_NOALLOC_SCRATCH_BYTES inside this
+ * library, held by every device that loads the library until the process
+ * exits.
  *   - Returns CTCPB_ESIZE when the problem's workspace (ctcpb_workspace_size)
  *     exceeds CTCPB_NOALLOC_SCRATCH_BYTES; nothing is launched then.
  *   - Calls no allocator.  The first call on each device looks up the array's
- *     device address (cudaGetSymbolAddress) with that device current; make
- *     that first call before any stream capture.
- *   - All calls on a device share the one array: calls whose work overlaps on
- *     the GPU (different streams, or several host threads) race and corrupt
- *     each other's results.  Serialise them, e.g. on one stream.
+ *     device address (cudaGetSymbolAddress) with that device current, and
+ *     keeps it for the process; make that first call before any stream
+ *     capture.  The kept address does not survive cudaDeviceReset: do not use
+ *     this call on a device after resetting it.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents (each call resets what it reads before reading it).  Calls
+ *     whose work overlaps on the GPU (different streams, or several host
+ *     threads) race and corrupt each other's results.  Serialise them, e.g. on
+ *     one stream.
+ *   - ctcpb_noalloc_read_status reads the array's device status word (the
+ *     CTCPB_DEV_* bits of the last call on the current device, as
+ *     ctcpb_read_status does for a workspace).  It synchronises the device.
  */
 #define CTCPB_NOALLOC_SCRATCH_BYTES (32u << 20)
 int ctcpb_decode_offline_noalloc(const ctcpb_config* cfg, const float* log_prob, int64_t stride_b, int64_t stride_t,
                                  const int32_t* seq_lengths, int B, int T, int V, int32_t* out_tokens,
                                  int32_t* out_lengths, float* out_scores, int out_len, ctcpb_stream_t stream);
+int ctcpb_noalloc_read_status(uint32_t* device_status);
 
 /*
  * Streaming state bytes for B independent streams of vocabulary V (section 5,

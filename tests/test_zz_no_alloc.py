@@ -1,13 +1,14 @@
 """The no-allocation offline decode (for callers that may not call cudaMalloc).
 
-Some callers cannot allocate device memory -- code inside an allocation-free
-stream capture, engine plugins whose host owns the device heap, real-time
-paths that must not block in the allocator -- so ctcpb_decode_offline_noalloc
-keeps its workspace in a fixed device array inside the library.  This test
-calls it through the C ABI twice in a row, on two different batches, and
-checks each result against ctcpb_decode_offline with a caller-owned workspace
-(tokens and lengths exact, scores within the 1e-4 tolerance of the parity
-tests).  It sits in a file of its own that pytest collects last.
+Some callers cannot allocate device memory -- engine plugins whose host owns
+the device heap and forbids allocations from outside it, real-time paths that
+must not block in the allocator -- so ctcpb_decode_offline_noalloc keeps its
+workspace in a fixed device array inside the library.  This test calls it
+through the C ABI twice in a row, on two different batches, and checks each
+result against ctcpb_decode_offline with a caller-owned workspace (tokens and
+lengths exact, scores within the 1e-4 tolerance of the parity tests) and the
+array's device status word (ctcpb_noalloc_read_status) against zero.  It sits
+in a file of its own that pytest collects last.
 """
 import ctypes
 
@@ -32,6 +33,16 @@ def noalloc_fn():
     fn.restype = I
     fn.argtypes = [ctypes.POINTER(D._Cfg), P, I64, I64, P, I, I, I, P, P, P, I, P]
     return fn
+
+
+def noalloc_status():
+    fn = D.lib().ctcpb_noalloc_read_status
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    st = ctypes.c_uint32(0xFFFFFFFF)
+    rc = fn(ctypes.byref(st))
+    assert rc == D.OK, D.status_string(rc)
+    return st.value
 
 
 def call_noalloc(fn, cfg, lp, lens, out_len):
@@ -64,6 +75,7 @@ def test_noalloc_matches_workspace_decode_twice():
         assert torch.equal(ln, rl)
         assert torch.equal(tok, rt)
         assert (sc - rs).abs().max().item() <= SCORE_TOL
+        assert noalloc_status() == 0
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
