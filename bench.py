@@ -47,7 +47,7 @@ DESCR = {
     "char": "char: B=16 T=1000 V=29 beam=128 nbest=128 offline, paged (page 16, max_seq_len 400), "
             "logits N(0,1.5) +3 on blank, held labels +2",
     "skip": "skip: B=256 T=2000 V=1024 beam=16 nbest=16 offline, blank threshold 0.999",
-    "stream": "stream (decoded offline): B=128 T=1600 V=5000 beam=10 nbest=10, peaky logits",
+    "stream": "stream: 128 streams x 1600 frames, V=5000 beam=10 nbest=10, 16-frame chunks, offsets U[0,160)",
 }
 L2_BYTES = 129 * 1024 * 1024
 
@@ -61,6 +61,9 @@ def args_():
     p.add_argument("--workload", default="bpe", choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the compact record of the other workloads (default run: recorded after the headline)")
+    p.add_argument("--workload-steps", type=int, default=5)
     return p.parse_args()
 
 
@@ -122,26 +125,27 @@ class Clocks:
 
 # ------------------------------------------------------------------ bytes
 
-def algorithmic_bytes(w, lp, lens, kept, L):
-    """Bytes each stage must move (per benchmark step).
+def algorithmic_bytes(w, lens, kept, out_lengths=None):
+    """The decode's algorithmic bytes per benchmark step, as the survey's
+    measurement rule counts them.
 
-    rank:   every kept frame row read once (4V) and its ranked list written
-            (ids + log-probs + a 32-byte header).
-    select: one 32-byte sector per valid frame for the blank test.
-    steps:  per decoded frame, its ranked list read back, lp[t][x] for the
-            beam's last labels and the listed labels, and the beam state
-            (pb, pnb, score, last, len) read and written per hypothesis.
-    decode: the log-probabilities read plus the beam state traffic.
+    rank:    every kept frame's row of log-probabilities read once (4V).
+    select:  one 32-byte sector per skipped valid frame (its blank test; a
+             kept frame's blank log-prob is part of its row).
+    state:   per decoded frame and row, the beam state: beam x 20 bytes (pb,
+             pnb, last, len and the token), plus the final N-best tokens
+             (4 bytes per output label).
+    decode:  all three.  The ranked lists the pre-pass writes and the steps
+             read back are an intermediate of this design, not counted.
     """
     V, beam = w.V, w.beam
-    n_kept = int(kept.sum())
+    n_kept = int(np.asarray(kept).sum())
     n_valid = int(np.minimum(lens, w.T).sum())
-    rec = 32 + 8 * L
-    rank = n_kept * (4 * V + rec)
-    select = 0 if w.blank_threshold >= 1.0 else n_valid * 32
-    state = n_kept * beam * 40
-    steps = n_kept * (rec + 4 * (beam + L)) + state
-    return dict(rank=rank, select=select, steps=steps, decode=n_kept * 4 * V + select + state)
+    rank = n_kept * 4 * V
+    select = (n_valid - n_kept) * 32
+    final = 0 if out_lengths is None else int(np.asarray(out_lengths).sum()) * 4
+    state = n_kept * beam * 20 + final
+    return dict(rank=rank, select=select, state=state, steps=state, decode=rank + select + state)
 
 
 def traffic_record(kernel: str, workload: str):
@@ -194,8 +198,7 @@ def run_reference(a, w, rank, world):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "frames/s", "n_gpus": a.gpus,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B={w.B} T={w.T} V={w.V} beam={w.beam} nbest={w.nbest} offline",
-                   "l2": "n/a (host)"},
+        "config": {"workload": DESCR.get(w.name, w.name), "l2": "n/a (host)"},
         "cpu_baseline": {"value": v, "unit": "frames/s", "cores": cores, "kind": "oracle",
                          "sample": f"whole {w.name} batch per step on {cores} host threads"},
         "e2e": {"value": v, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -227,9 +230,10 @@ def job_frames(world: int, B: int, T: int) -> int:
 
 # ------------------------------------------------------------------ streaming (config 3)
 
-def run_stream(a, w, torch, D, dev):
+def measure_stream(w, steps, warmup, torch, D, dev, clocks=None, cpu_sample=False):
     """One step = one streaming session: stream_init, then every 16-frame tick of
-    the 128 staggered streams through stream_step_chunk, ticks resident in HBM."""
+    the 128 staggered streams through stream_step_chunk, ticks resident in HBM.
+    Returns the session's figures (device time, end to end, bytes)."""
     offsets = synth.stream_offsets(w)
     nt = synth.n_ticks(w, offsets)
     cache = {}
@@ -248,13 +252,13 @@ def run_stream(a, w, torch, D, dev):
         for c, nf in ticks:
             st.step_chunk(c, nf)
 
-    for _ in range(max(3, a.warmup)):
+    for _ in range(max(3, warmup)):
         session()
     torch.cuda.synchronize(dev)
     fused = D.read_counters(st.buf)["fused"] > 0
     ts = []
-    with Clocks(0, enabled=not a.no_clocks) as clk:
-        for _ in range(a.steps):
+    with (clocks if clocks is not None else Clocks(0, enabled=False)) as clk:
+        for _ in range(steps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             session()
@@ -297,7 +301,7 @@ def run_stream(a, w, torch, D, dev):
         session_host()
     torch.cuda.synchronize(dev)
     te = []
-    for _ in range(a.steps):
+    for _ in range(steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         session_host()
@@ -307,10 +311,11 @@ def run_stream(a, w, torch, D, dev):
     e2e_ms = statistics.mean(te)
     h2d = sum(hc.numel() * 4 + hn.numel() * 4 for hc, hn in host_ticks)
     d2h = sum(r.numel() * r.element_size() for r in res_host)
+    valid = np.full(w.B, w.T)
+    by = algorithmic_bytes(w, valid, valid, res_host[1].numpy())
 
-    # the oracle on the host cores: a bounded sample of whole streams decoded offline
     cpu = None
-    if not a.no_cpu_baseline:
+    if cpu_sample:  # the oracle on the host cores: a bounded sample of whole streams decoded offline
         import oracle as O
         O.lib()
         ns = min(w.B, 16)
@@ -322,27 +327,116 @@ def run_stream(a, w, torch, D, dev):
         dt = time.perf_counter() - t0
         cpu = {"value": ns * w.T / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
                "sample": f"{ns} whole streams of {w.T} frames decoded offline, {cores} threads, {dt:.2f} s"}
+    return dict(ms=ms, ticks=nt, fused=fused, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, bytes=by, frames=w.B * w.T,
+                cpu=cpu, clocks=clk.summary() if clocks is not None else None, launches=steps * (1 + nt))
 
-    frames = w.B * w.T
-    tick_bytes = w.B * w.chunk * w.V * 4
-    gbs = nt * tick_bytes / (ms / 1e3) / 1e9
+
+def run_stream(a, w, torch, D, dev):
+    m = measure_stream(w, a.steps, a.warmup, torch, D, dev, clocks=Clocks(0, enabled=not a.no_clocks),
+                       cpu_sample=not a.no_cpu_baseline)
+    ms, nt = m["ms"], m["ticks"]
+    gbs = m["bytes"]["decode"] / (ms / 1e3) / 1e9
     peak, peak_kind = peaks()
     print(json.dumps({
-        "metric": METRIC, "value": frames / (ms / 1e3), "unit": "frames/s", "n_gpus": 1, "steps": a.steps,
+        "metric": METRIC, "value": m["frames"] / (ms / 1e3), "unit": "frames/s", "n_gpus": 1, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"stream: {w.B} streams x {w.T} frames, V={w.V}, beam={w.beam}, chunks of {w.chunk} "
                                f"frames over {nt} ticks, offsets U[0,160)",
                    "l2": "inputs (4.5 GB of ticks) larger than L2"},
-        "ms_per_tick": ms / nt, "fused": fused,
-        "roofline": {"kernel": "k_fused" if fused else "k_step_warp", "bound": "hbm", "achieved": gbs, "peak": peak,
-                     "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_kind": peak_kind},
-        "e2e": {"value": frames / (e2e_ms / 1e3), "unit": "frames/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "cpu_baseline": cpu,
-        "gpu_launches": a.steps * (1 + nt),
-        "clocks": clk.summary(),
+        "ms_per_tick": ms / nt, "fused": m["fused"],
+        "roofline": {"kernel": "k_fused" if m["fused"] else "k_step_warp", "bound": "hbm", "achieved": gbs,
+                     "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_kind": peak_kind,
+                     "bytes_per_step": m["bytes"]["decode"]},
+        "e2e": {"value": m["frames"] / (m["e2e_ms"] / 1e3), "unit": "frames/s", "h2d_bytes_per_step": m["h2d"],
+                "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"]},
+        "cpu_baseline": m["cpu"],
+        "gpu_launches": m["launches"],
+        "clocks": m["clocks"],
     }), flush=True)
+
+
+def measure_offline_compact(w, steps, warmup, torch, D, dev):
+    """A whole offline decode of workload w (inputs resident, L2 flushed between
+    steps) and the same through the host-buffer call: the figures of the
+    compact per-workload record."""
+    lp_np, lens_np = synth.gen_batch(w, pad="zero")
+    Bn, T, V = lp_np.shape
+    cfg = D.Config(beam=w.beam, nbest=w.nbest, blank_id=w.blank_id, max_seq_len=w.max_seq_len,
+                   blank_threshold=w.blank_threshold, paged=bool(w.paged), page_size=w.page_size)
+    lp_host = torch.from_numpy(lp_np).pin_memory()
+    lens_host = torch.from_numpy(lens_np).pin_memory()
+    lp, lens = lp_host.to(dev), lens_host.to(dev)
+    ws = torch.empty(D.workspace_size(cfg, Bn, T, V), dtype=torch.uint8, device=dev)
+    out_len = min(w.max_seq_len, T) if w.max_seq_len > 0 else T
+    outs = (torch.empty((Bn, w.nbest, out_len), dtype=torch.int32, device=dev),
+            torch.empty((Bn, w.nbest), dtype=torch.int32, device=dev),
+            torch.empty((Bn, w.nbest), dtype=torch.float32, device=dev))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def decode():
+        D.decode_offline(cfg, lp, lens, workspace=ws, outputs=outs, out_len=out_len)
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return statistics.mean(ts)
+
+    for _ in range(max(3, warmup)):
+        decode()
+    ms = timed(decode, steps)
+    fused = D.read_counters(ws)["fused"] > 0
+    _, nsel = D.select_frames(cfg, lp, lens)
+    kept = nsel.cpu().numpy()
+    by = algorithmic_bytes(w, lens_np, kept, outs[1].cpu().numpy())
+    out_host = tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs)
+    ws_host = torch.empty(D.host_workspace_size(cfg, Bn, T, V, out_len), dtype=torch.uint8, device=dev)
+
+    def decode_host():
+        D.decode_offline_host(cfg, lp_host, lens_host, workspace=ws_host, out_len=out_len, outputs=out_host,
+                              device=dev, synchronize=False)
+
+    for _ in range(2):
+        decode_host()
+    e2e_ms = timed(decode_host, steps)
+    h2d = int(np.clip(lens_np, 0, T).sum()) * V * 4 + lens_host.numel() * 4
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    return dict(ms=ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, bytes=by, frames=Bn * T,
+                valid=int(np.minimum(lens_np, T).sum()), kept=int(kept.sum()), fused=fused)
+
+
+def workloads_record(names, steps, warmup, torch, D, dev):
+    """Compact figures of the other workloads, measured after the headline
+    timed region: device ms per step, B*T frames/s, the algorithmic bytes and
+    their fraction of the measured HBM bandwidth, and end to end through host
+    buffers."""
+    peak, peak_kind = peaks()
+    out = {}
+    for n in names:
+        w = synth.WORKLOADS[n]
+        m = (measure_stream(w, steps, warmup, torch, D, dev) if w.streaming
+             else measure_offline_compact(w, steps, warmup, torch, D, dev))
+        gbs = m["bytes"]["decode"] / (m["ms"] / 1e3) / 1e9
+        rec = {"workload": DESCR.get(n, n), "ms_per_step": m["ms"], "frames_per_s": m["frames"] / (m["ms"] / 1e3),
+               "bytes_per_step": m["bytes"]["decode"], "achieved_gbs": gbs, "frac": gbs / peak,
+               "peak_kind": peak_kind, "path": "k_fused" if m["fused"] else "two kernels",
+               "e2e": {"frames_per_s": m["frames"] / (m["e2e_ms"] / 1e3), "ms_per_step": m["e2e_ms"],
+                       "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"]}}
+        if w.streaming:
+            rec["ms_per_tick"] = m["ms"] / m["ticks"]
+        else:
+            rec["valid_frames_per_s"] = m["valid"] / (m["ms"] / 1e3)
+            rec["kept_frames"] = m["kept"]
+        out[n] = rec
+    return out
 
 
 # ------------------------------------------------------------------ our arm
@@ -484,11 +578,11 @@ def main():
     frames = job_frames(world, Bn, T)
     valid = world * int(np.minimum(lens_np, T).sum())
     peak, peak_kind = peaks()
-    by = algorithmic_bytes(w, lp_np, lens_np, kept, L)
+    by = algorithmic_bytes(w, lens_np, kept, outs[1].cpu().numpy())
     stage_ms = {n: statistics.mean(v) for n, v in per_stage.items()}
     dom = max(stage_ms, key=stage_ms.get)
-    dom_bytes = {"rank": by["rank"], "select": by["select"], "steps": by["steps"],
-                 "rank+steps": by["rank"] + by["steps"], "init": 0, "output": 0}[dom]
+    dom_bytes = {"rank": by["rank"], "select": by["select"], "steps": by["state"],
+                 "rank+steps": by["rank"] + by["state"], "init": 0, "output": 0}[dom]
     achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
     decode_gbs = by["decode"] / (ms / 1e3) / 1e9
     res = {
@@ -502,7 +596,7 @@ def main():
         "unfused_stage_ms": split_ms,
         "roofline": {"kernel": kernel_of[dom], "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_record(kernel_of[dom], w.name),
-                     "peak_kind": peak_kind},
+                     "peak_kind": peak_kind, "bytes_per_launch": dom_bytes},
         "decode_roofline": {"achieved": decode_gbs, "peak": peak, "unit": "GB/s", "frac": decode_gbs / peak,
                             "bytes_per_step": by["decode"], "peak_kind": peak_kind},
         "e2e": {"value": frames / (e2e / 1e3), "unit": "frames/s", "h2d_bytes_per_step": h2d,
@@ -532,6 +626,8 @@ def main():
         dt1 = time.perf_counter() - t0
         res["cpu_baseline_1thread"] = {"value": nr * T / dt1, "unit": "frames/s", "cores": 1, "kind": "oracle",
                                        "sample": f"first {nr} rows of the {w.name} batch, 1 thread, {dt1:.2f} s"}
+    if not a.no_workloads and world == 1 and w.name == "bpe":
+        res["workloads"] = workloads_record(["tiny", "char", "skip", "stream"], a.workload_steps, 3, torch, D, dev)
     print(json.dumps(res), flush=True)
     if dist is not None:
         dist.destroy_process_group()

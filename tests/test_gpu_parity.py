@@ -4,6 +4,8 @@ Bars: token sequences and lengths bit-exact; scores within 1e-4 absolute (the
 decoder's contract) and, by construction, bit-identical (both sides evaluate
 the same float32 operations in the same order).
 """
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -186,17 +188,18 @@ def test_paged_equals_flat():
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
-# ------------------------------------------------------------ full-size workloads, sampled rows
+# ------------------------------------------------------------ full-size workloads, every row
 
-@pytest.mark.parametrize("name,rows", [("tiny", [0]), ("bpe", [0, 7, 31]), ("char", [0, 15]),
-                                       ("skip", [0, 100, 255])])
-def test_full_size_sampled_rows(name, rows):
+@pytest.mark.parametrize("name", ["tiny", "bpe", "char", "skip"])
+def test_full_size_every_row(name):
+    """Each offline workload at its full size, in the launch configuration the
+    benchmark times, compared with the oracle on every row."""
     w = synth.WORKLOADS[name]
     lp, lens = synth.gen_batch(w, pad="nan")
     cfg = cfg_of(w)
     g = gpu_offline(cfg, lp, lens)
-    o = oracle_offline(cfg, lp, lens, rows=rows)
-    assert_same(tuple(x[rows] for x in g), o, f"{name} rows {rows}")
+    o = oracle_offline(cfg, lp, lens)
+    assert_same(g, o, f"{name}: all {w.B} rows")
 
 
 # ------------------------------------------------------------ streaming
@@ -278,20 +281,45 @@ def test_streaming_partial_chunks_and_resume():
     assert all(np.array_equal(x, y) for x, y in zip(got, got2))
 
 
-def test_stream_workload_sampled_streams():
-    """The streaming workload's tick schedule on a subset of streams."""
-    w = synth.workload("stream", B=12, T=400)
-    offs = synth.stream_offsets(synth.WORKLOADS["stream"])[:12]
+def test_stream_workload_full():
+    """The streaming workload exactly as the benchmark runs it: 128 streams x
+    1,600 frames, staggered offsets, one stream_step_chunk call per 16-frame
+    global tick with per-stream n_frames; every stream against the oracle's
+    offline decode of its frames ("GPU CTC Prefix Beam Search Decoder",
+    sections 3.4.9 and 8)."""
+    w = synth.WORKLOADS["stream"]
+    offs = synth.stream_offsets(w)
+    full = np.empty((w.B, w.T, w.V), np.float32)
+    with ThreadPoolExecutor(8) as ex:
+        for i, x in enumerate(ex.map(lambda i: synth.gen_stream(w, i), range(w.B))):
+            full[i] = x
     cfg = cfg_of(w)
     st = D.StreamState(cfg, w.B, w.V)
-    cache = {}
-    for k in range(synth.n_ticks(w, offs)):
-        chunk, nf = synth.stream_tick(w, k, offs, cache)
+    ticks = synth.n_ticks(w, offs)
+    for k in range(ticks):
+        chunk, nf = tick_from_streams(full, offs, k, w.chunk)
+        if k in (0, ticks // 2):  # the same bytes as the generator's own tick
+            ref_chunk, ref_nf = synth.stream_tick(w, k, offs, {})
+            assert np.array_equal(nf, ref_nf) and np.array_equal(chunk, ref_chunk, equal_nan=True)
         st.step_chunk(torch.from_numpy(chunk).cuda(), torch.from_numpy(nf).cuda())
     got = tuple(v.cpu().numpy() for v in st.read(out_len=w.T))
-    full = np.stack([synth.gen_stream(w, i) for i in range(w.B)])
+    assert st.status() == 0
     ref = oracle_offline(cfg, full, None, out_len=w.T)
-    assert_same(got, ref, "stream workload")
+    assert_same(got, ref, "stream workload, all 128 streams")
+
+
+def tick_from_streams(full, offs, k, C):
+    """Tick k's chunk: stream i's local frames that fall in global frames
+    [C k, C k + C), packed at the chunk's first rows, NaN after them."""
+    B, T, V = full.shape
+    chunk = np.full((B, C, V), np.nan, np.float32)
+    nf = np.zeros(B, np.int32)
+    for i in range(B):
+        a, e = max(C * k, int(offs[i])), min(C * k + C, int(offs[i]) + T)
+        if e > a:
+            chunk[i, :e - a] = full[i, a - int(offs[i]):e - int(offs[i])]
+            nf[i] = e - a
+    return chunk, nf
 
 
 def test_state_header_mismatch_sets_status():

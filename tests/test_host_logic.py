@@ -117,3 +117,18 @@ def test_caller_buffers_are_validated():
         D._check_buf(ws[::2], 100, cpu, "workspace")
     with pytest.raises(ValueError):
         D._cuda_device("cpu")
+
+
+def test_algorithmic_bytes_follow_the_measurement_rule():
+    """Kept rows read once (4V), one 32-byte sector per skipped valid frame,
+    beam x 20 bytes of state per decoded frame and row, 4 bytes per output label;
+    the ranked lists of the pre-pass are not counted."""
+    import bench
+    w = synth.workload("skip", B=3, T=10, V=8, beam=2, nbest=2)
+    lens = np.array([10, 4, 0], np.int32)
+    kept = np.array([7, 4, 0])
+    by = bench.algorithmic_bytes(w, lens, kept, np.array([[3, 2], [1, 0], [0, 0]]))
+    assert by["rank"] == 11 * 4 * 8
+    assert by["select"] == 3 * 32
+    assert by["state"] == 11 * 2 * 20 + 6 * 4
+    assert by["decode"] == by["rank"] + by["select"] + by["state"]
