@@ -131,6 +131,17 @@ def _stream(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _row_strides(x: torch.Tensor):
+    """(batch, time) element strides of a [B, T, V] tensor as the library takes
+    them.  A dimension of extent 1 is never stepped over, and torch and NumPy
+    leave its stride arbitrary (often 0: an expanded or inserted axis), so it
+    is given a valid one instead."""
+    B, T, V = x.shape[0], x.shape[1], x.shape[2]
+    st = x.stride(1) if T > 1 else V
+    sb = x.stride(0) if B > 1 else st * max(T, 1)
+    return sb, st
+
+
 def _f32_3d(lp: torch.Tensor) -> torch.Tensor:
     if lp.dtype != torch.float32 or lp.dim() != 3 or not lp.is_cuda:
         raise ValueError("log_prob must be a CUDA float32 tensor [B, T, V]")
@@ -276,14 +287,14 @@ def decode_offline(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[to
             raise ValueError("a boosted decode runs every stage")
         tables = boost_tables(boost, B, dev)
         rc = _call(dev, lib().ctcpb_decode_offline_boosted, ctypes.byref(c), ctypes.byref(_boost_arg(tables)),
-                   _ptr(lp), lp.stride(0), lp.stride(1), _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes,
+                   _ptr(lp), *_row_strides(lp), _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes,
                    _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
     elif stages == STAGE_ALL:
-        rc = _call(dev, lib().ctcpb_decode_offline, ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
+        rc = _call(dev, lib().ctcpb_decode_offline, ctypes.byref(c), _ptr(lp), *_row_strides(lp),
                    _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln), _ptr(sc), out_len,
                    _stream(dev))
     else:
-        rc = _call(dev, lib().ctcpb_decode_offline_staged, ctypes.byref(c), _ptr(lp), lp.stride(0), lp.stride(1),
+        rc = _call(dev, lib().ctcpb_decode_offline_staged, ctypes.byref(c), _ptr(lp), *_row_strides(lp),
                    _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln), _ptr(sc), out_len,
                    stages, _stream(dev))
     _check(rc, "decode_offline")
@@ -332,11 +343,11 @@ def decode_offline_host(cfg: Config, log_prob: torch.Tensor, seq_lengths: Option
     if boost is not None:
         tables = boost_tables(boost, B, dev)
         rc = _call(dev, lib().ctcpb_decode_offline_host_boosted, ctypes.byref(c), ctypes.byref(_boost_arg(tables)),
-                   _ptr(log_prob), log_prob.stride(0), log_prob.stride(1), _ptr(seq_lengths), B, T, V,
+                   _ptr(log_prob), *_row_strides(log_prob), _ptr(seq_lengths), B, T, V,
                    _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln), _ptr(sc), out_len, _stream(dev))
     else:
-        rc = _call(dev, lib().ctcpb_decode_offline_host, ctypes.byref(c), _ptr(log_prob), log_prob.stride(0),
-                   log_prob.stride(1), _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln),
+        rc = _call(dev, lib().ctcpb_decode_offline_host, ctypes.byref(c), _ptr(log_prob),
+                   *_row_strides(log_prob), _ptr(seq_lengths), B, T, V, _ptr(workspace), ws_bytes, _ptr(tok), _ptr(ln),
                    _ptr(sc), out_len, _stream(dev))
     _check(rc, "decode_offline_host")
     if synchronize:
@@ -395,11 +406,11 @@ class StreamState:
                 raise ValueError("is_speech must be a uint8 tensor [B, >= chunk_T] with unit column stride")
             self._on(is_speech, dev, "is_speech")
             _check(_call(dev, lib().ctcpb_stream_step_chunk_masked, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb,
-                         self.B, self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames), _ptr(is_speech),
+                         self.B, self.V, _ptr(lp), *_row_strides(lp), _ptr(n_frames), _ptr(is_speech),
                          is_speech.stride(0), lp.shape[1], _stream(dev)), "stream_step_chunk_masked")
             return
         _check(_call(dev, lib().ctcpb_stream_step_chunk, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb, self.B,
-                     self.V, _ptr(lp), lp.stride(0), lp.stride(1), _ptr(n_frames), lp.shape[1], _stream(dev)),
+                     self.V, _ptr(lp), *_row_strides(lp), _ptr(n_frames), lp.shape[1], _stream(dev)),
                "stream_step_chunk")
 
     def step(self, lp_frame: torch.Tensor, is_speech: Optional[torch.Tensor] = None):
@@ -418,7 +429,8 @@ class StreamState:
             self._on(is_speech, dev, "is_speech")
             is_speech = is_speech.contiguous()
         _check(_call(dev, lib().ctcpb_stream_step, ctypes.byref(self.cfg.c()), _ptr(self.buf), nb, self.B, self.V,
-                     _ptr(lp), lp.stride(0), _ptr(is_speech), _stream(dev)), "stream_step")
+                     _ptr(lp), lp.stride(0) if self.B > 1 else self.V, _ptr(is_speech), _stream(dev)),
+               "stream_step")
 
     def read(self, out_len: Optional[int] = None, outputs=None):
         """The current N best of every stream; the state is not modified."""
@@ -471,7 +483,7 @@ def select_frames(cfg: Config, log_prob: torch.Tensor, seq_lengths: Optional[tor
         seq_lengths = seq_lengths.contiguous()
     sel = torch.empty((B, T), dtype=torch.int32, device=dev)
     nsel = torch.empty((B,), dtype=torch.int32, device=dev)
-    _check(_call(dev, lib().ctcpb_select_frames, ctypes.byref(cfg.c()), _ptr(lp), lp.stride(0), lp.stride(1),
+    _check(_call(dev, lib().ctcpb_select_frames, ctypes.byref(cfg.c()), _ptr(lp), *_row_strides(lp),
                  _ptr(seq_lengths), B, T, V, _ptr(sel), _ptr(nsel), _stream(dev)), "select_frames")
     return sel, nsel
 

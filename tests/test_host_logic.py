@@ -132,3 +132,15 @@ def test_algorithmic_bytes_follow_the_measurement_rule():
     assert by["select"] == 3 * 32
     assert by["state"] == 11 * 2 * 20 + 6 * 4
     assert by["decode"] == by["rank"] + by["select"] + by["state"]
+
+
+def test_row_strides_of_extent_one_dimensions():
+    """An inserted batch axis has stride 0 (NumPy's x[None]); the library is
+    given a valid stride for it instead, and real strides pass unchanged."""
+    x = torch.from_numpy(np.zeros((3, 8), np.float32)[None])
+    assert x.stride(0) == 0
+    assert D._row_strides(x) == (24, 8)
+    y = torch.zeros((2, 1, 8))[:, :, :]
+    assert D._row_strides(y) == (8, 8)
+    z = torch.zeros((4, 6, 8))
+    assert D._row_strides(z) == (48, 8)
