@@ -121,6 +121,14 @@ const char* ctcpb_status_string(int s) {
   }
 }
 
+int ctcpb_lse_table(float* out, int n) {
+  static constexpr FCoef kTable = make_fcoef();
+  if (n < 0) return CTCPB_EINVAL;
+  if (n > 0 && !out) return CTCPB_ENULL;
+  for (int i = 0; i < n && i < kFCoef; ++i) out[i] = kTable.c[i];
+  return kFCoef;
+}
+
 int ctcpb_list_len(const ctcpb_config* cfg, int V) {
   int rc = check_cfg(cfg, V);
   if (rc) return rc;

@@ -202,64 +202,97 @@ __host__ __device__ inline float* rec_lps(char* r, int Lpad) { return (float*)(r
 // The decoder's float32 log-semiring ("GPU CTC Prefix Beam Search Decoder",
 // section 3: logsumexp(a,b) = max + log(1 + exp(-|a-b|)), NEG_INF = -FLT_MAX),
 // written with explicit round-to-nearest intrinsics so nothing is contracted.
-//   dexp(x)   exp(x) for x <= 0: x = n*ln2 + r by Cody-Waite reduction
-//             (ln2 = HI + LO, HI with 16 significant bits so n*HI is exact),
-//             e^r by its degree-7 Taylor polynomial, times 2^n; 0 below -87.
-//   dlog1p(x) log(1+x) for x in [0,1] as 2*atanh(s), s = x/(2+x), through
-//             the odd series to s^13; above sqrt(2)-1 it evaluates
-//             ln2 + 2*atanh((x-1)/(x+3)) instead.
-//   dlse      max(a,b) + dlog1p(dexp(-|a-b|)).
+//   dF(d)     log(1 + e^-d) for d >= 0: on each of 96 segments [k/4, (k+1)/4)
+//             the degree-5 Taylor polynomial of the function about the
+//             segment's midpoint d_k = k/4 + 1/8, in u = d - d_k, by Horner's
+//             rule; 0 for d >= 24 (where it is below 4e-11).
+//   dlse      max(a,b) + dF(|a-b|).
 //   dadd      max(a+b, NEG): a product of probabilities, clamped to NEG.
+// The coefficients are the float32 roundings of F^(n)(d_k) / n!.  They are
+// computed at compile time (make_fcoef) in double: F' = -s with s =
+// 1/(1 + e^d) and ds/dd = s^2 - s, so each derivative is a polynomial in s;
+// exp and log1p come from their series (cx_exp, cx_log1p).  The kernels copy
+// the table into shared memory and pass it to dlse.
 #define CTCPB_NEG (-FLT_MAX)
 
-__device__ __forceinline__ float dexp(float x) {
-  const float LN2_HI = 0.693145751953125f;
-  const float LN2_LO = 1.42860682030941723212e-6f;
-  const float LOG2E = 1.44269504088896340736f;
-  // branch-free: the reduction runs on a clamped argument, the result is selected
-  const bool under = !(x >= -87.0f);
-  x = under ? -87.0f : x;
-  float n = rintf(__fmul_rn(x, LOG2E));
-  float r = __fmaf_rn(n, -LN2_HI, x);
-  r = __fmaf_rn(n, -LN2_LO, r);
-  float p = (float)(1.0 / 5040.0);
-  p = __fmaf_rn(p, r, (float)(1.0 / 720.0));
-  p = __fmaf_rn(p, r, (float)(1.0 / 120.0));
-  p = __fmaf_rn(p, r, (float)(1.0 / 24.0));
-  p = __fmaf_rn(p, r, (float)(1.0 / 6.0));
-  p = __fmaf_rn(p, r, 0.5f);
-  p = __fmaf_rn(p, r, 1.0f);
-  p = __fmaf_rn(p, r, 1.0f);
-  int ni = (int)n;
-  return under ? 0.0f : __fmul_rn(p, __uint_as_float((unsigned)(ni + 127) << 23));
+constexpr int kFSeg = 96, kFDeg = 5, kFCoef = kFSeg * (kFDeg + 1);
+struct FCoef {
+  float c[kFCoef];  // segment-major: c[6k + n]
+};
+
+// e^x for |x| <= 25: x = n ln2 + r, |r| <= ln2/2, the Taylor series of e^r to
+// r^24, times 2^n.
+constexpr double cx_exp(double x) {
+  const double ln2 = 0.693147180559945309417232121458;
+  const double t = x / ln2;
+  const int n = (int)(t >= 0.0 ? t + 0.5 : t - 0.5);
+  const double r = x - n * ln2;
+  double term = 1.0, sum = 1.0;
+  for (int i = 1; i <= 24; ++i) {
+    term = term * r / i;
+    sum += term;
+  }
+  double p = 1.0;
+  for (int i = 0; i < (n >= 0 ? n : -n); ++i) p *= 2.0;
+  return n >= 0 ? sum * p : sum / p;
 }
 
-__device__ __forceinline__ float dlog1p(float x) {
-  const float LN2_HI = 0.693145751953125f;
-  const float LN2_LO = 1.42860682030941723212e-6f;
-  const bool lo_half = x <= 0.41421356237309504880f;
-  float num = lo_half ? x : __fsub_rn(x, 1.0f);
-  float den = lo_half ? __fadd_rn(2.0f, x) : __fadd_rn(x, 3.0f);
-  float hi = lo_half ? 0.0f : LN2_HI;
-  float lo = lo_half ? 0.0f : LN2_LO;
-  float s = __fdiv_rn(num, den);
-  float z = __fmul_rn(s, s);
-  float q = (float)(1.0 / 13.0);
-  q = __fmaf_rn(q, z, (float)(1.0 / 11.0));
-  q = __fmaf_rn(q, z, (float)(1.0 / 9.0));
-  q = __fmaf_rn(q, z, (float)(1.0 / 7.0));
-  q = __fmaf_rn(q, z, (float)(1.0 / 5.0));
-  q = __fmaf_rn(q, z, (float)(1.0 / 3.0));
-  float w = __fmul_rn(z, q);
-  float t2 = __fadd_rn(s, s);
-  float r = __fmaf_rn(t2, w, t2);
-  return __fadd_rn(__fadd_rn(r, lo), hi);
+// log(1 + y) for y in [0, 1]: 2 atanh(t), t = y / (2 + y) <= 1/3, the odd
+// series to t^49 (stopping once a term is below 1e-60 of the first, which
+// also keeps the compile-time evaluation clear of underflow).
+constexpr double cx_log1p(double y) {
+  const double t = y / (2.0 + y), t2 = t * t;
+  double pw = t, sum = 0.0;
+  for (int j = 0; j < 25 && pw > t * 1e-60; ++j) {
+    sum += pw / (2 * j + 1);
+    pw *= t2;
+  }
+  return 2.0 * sum;
 }
 
-__device__ __forceinline__ float dlse(float a, float b) {
+constexpr FCoef make_fcoef() {
+  FCoef f{};
+  for (int k = 0; k < kFSeg; ++k) {
+    const double d0 = k * 0.25 + 0.125;
+    const double s = 1.0 / (1.0 + cx_exp(d0));
+    f.c[6 * k] = (float)cx_log1p(cx_exp(-d0));
+    double P[kFDeg + 2] = {0.0, -1.0, 0.0, 0.0, 0.0, 0.0, 0.0};  // F' = -s, coefficients of s^i
+    double fact = 1.0;
+    for (int n = 1; n <= kFDeg; ++n) {
+      double v = 0.0;
+      for (int i = kFDeg + 1; i >= 0; --i) v = v * s + P[i];
+      fact *= n;
+      f.c[6 * k + n] = (float)(v / fact);
+      double Q[kFDeg + 2] = {0.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0};  // d/dd P(s) = P'(s) (s^2 - s)
+      for (int i = 1; i <= kFDeg; ++i) {
+        Q[i + 1] += i * P[i];
+        Q[i] -= i * P[i];
+      }
+      for (int i = 0; i < kFDeg + 2; ++i) P[i] = Q[i];
+    }
+  }
+  return f;
+}
+
+__device__ __forceinline__ float dF(const float* __restrict__ fc, float d) {
+  const bool far = !(d < 24.0f);  // NaN too
+  const int k = far ? 0 : (int)__fmul_rn(d, 4.0f);
+  const float u = __fsub_rn(d, __fadd_rn(__fmul_rn((float)k, 0.25f), 0.125f));
+  const float* c = fc + 6 * k;
+  float p = c[5];
+  p = __fmaf_rn(p, u, c[4]);
+  p = __fmaf_rn(p, u, c[3]);
+  p = __fmaf_rn(p, u, c[2]);
+  p = __fmaf_rn(p, u, c[1]);
+  p = __fmaf_rn(p, u, c[0]);
+  return far ? 0.0f : p;
+}
+
+// fc: the coefficient table (shared memory).
+__device__ __forceinline__ float dlse(const float* __restrict__ fc, float a, float b) {
   float m = fmaxf(a, b);
   float d = fabsf(__fsub_rn(a, b));
-  return __fadd_rn(m, dlog1p(dexp(-d)));
+  return __fadd_rn(m, dF(fc, d));
 }
 
 __device__ __forceinline__ float dadd(float a, float b) { return fmaxf(__fadd_rn(a, b), CTCPB_NEG); }

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(32) k_select_tile(View st, const uint8_t* __re
 // buffer (flat rows or pages).
 template <int NT>
 struct StepSmem {
+  float fc[kFCoef];  // the coefficients of log(1 + e^-d) (dlse)
   // current hypotheses, slot order
   float pb[NT], pnb[NT], sc[NT];
   int last[NT], len[NT];
@@ -351,6 +352,8 @@ struct StepSmem {
   int nw, npairs, nxu, nkeys, ndfree, nuc;
   int ptop, pnext;  // the row's page pool: LIFO top and bump pointer (paged)
 };
+
+__device__ const FCoef g_fcoef = make_fcoef();
 
 template <int NT>
 size_t step_smem_bytes(int sortcap) {
@@ -631,6 +634,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
     S.pnext = st.pnext()[b];
   }
   for (int i = tid; i < S.kLpos; i += NT) S.lpkey[i] = 0ull;
+  for (int i = tid; i < kFCoef; i += NT) S.fc[i] = g_fcoef.c[i];
   gsync<NT>();
 
   // Asynchronous copies that step s waits for at its start: its record into
@@ -720,10 +724,10 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
       for (int k = tid; k < nlive; k += NT) {
         float pb = S.pb[k], pnb = S.pnb[k];
         if (gap) {
-          pb = dlse(pb, pnb);
+          pb = dlse(S.fc, pb, pnb);
           pnb = NEG;
         }
-        const float A = dlse(pb, pnb);
+        const float A = dlse(S.fc, pb, pnb);
         const int L = S.len[k];
         const float lpl = L > 0 ? rdlp(lplf[k]) : NEG;
         // the last label emitted again (the repeat path, a merge fold) carries its bonus
@@ -774,7 +778,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
         const bool same = S.len[i] > 0 && S.last[i] == c;  // the folded candidate is i's (i, last) entry
         const bool rep_i = same && c != space;
         const float ext = rep_i ? dadd(S.lple[j], S.pbg[i]) : dadd(S.lple[j], S.A[i]);
-        S.bpnb[j] = dlse(S.bpnb[j], ext);
+        S.bpnb[j] = dlse(S.fc, S.bpnb[j], ext);
         if (same) {
           S.repdead[i] = 1;
         } else {
@@ -815,7 +819,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
       // is at most the beam-th largest key of the step (those are distinct
       // candidates), so the winners are among the candidates >= tau.
       auto blank_key = [&](int k) -> u64 {
-        const float sc = dlse(S.bpb[k], S.bpnb[k]);
+        const float sc = dlse(S.fc, S.bpb[k], S.bpnb[k]);
         return sc > NEG ? cand_key(sc, k, blank) : 0ull;
       };
       auto rep_key = [&](int k) -> u64 {
@@ -973,7 +977,7 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
           u64 key = 0ull;
           const int L = S.len[k];
           if (r == 0) {
-            const float sc = dlse(S.bpb[k], S.bpnb[k]);
+            const float sc = dlse(S.fc, S.bpb[k], S.bpnb[k]);
             if (sc > NEG) key = cand_key(sc, k, blank);
           } else if (r == 1) {
             if (L > 0 && L < cap && !S.repdead[k] && S.rep[k] > NEG) key = cand_key(S.rep[k], k, S.last[k]);

@@ -423,6 +423,140 @@ __device__ void rank_finish(const u64* cand, int n, int L, float lpb, int lane, 
   __syncwarp();
 }
 
+// The lean ranking of one staged row for lists of K = L + 1 <= 64 labels
+// (used up to kLeanK)
+// (all lanes).  Every step is a short, mostly independent instruction stream,
+// so a warp ranks a row in a few hundred cycles:
+//   1. each lane takes the maxima of two disjoint halves of its labels (the
+//      x,y and the z,w components of its float4 slices): 64 maxima of 64
+//      distinct labels;
+//   2. tau = the K-th largest of them, by counting: every lane reads the 64
+//      maxima from shared memory (broadcast) and keeps its maxima that have at
+//      least K maxima >= them; the largest such is tau.  At least K labels
+//      score >= tau, so the top K all do;
+//   3. each lane appends its own labels >= tau to a column of `cand` (at most
+//      kLaneHits each, no cross-lane traffic), then one scan packs the columns
+//      into a contiguous list;
+//   4. each packed key's rank = how many packed keys are larger (keys are
+//      distinct: they hold the label); ranks below L fill the list, rank L is
+//      the front.
+// Returns false, having written nothing, when a lane collects more than
+// kLaneHits labels (near-constant rows); the caller then ranks the row the
+// general way.
+constexpr int kLaneHits = 8;
+// The lean ranking serves lists of K = L + 1 <= 32 labels; with longer lists
+// more labels pass tau and counting every pair costs more than a sort.
+constexpr int kLeanK = 32;
+__device__ __forceinline__ bool rank_lean(const float* __restrict__ row, int V, int L, u64* cand, float lpb,
+                                          int lane, const RankDst& d) {
+  const int K = L + 1;
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const int V4 = V >> 2;
+  // 1. two maxima per lane, four independent chains
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+  int q = lane;
+  for (; q + 32 < V4; q += 64) {
+    const float4 x = r4[q], y = r4[q + 32];
+    m0 = fmaxf(m0, fmaxf(x.x, x.y));
+    m1 = fmaxf(m1, fmaxf(x.z, x.w));
+    m2 = fmaxf(m2, fmaxf(y.x, y.y));
+    m3 = fmaxf(m3, fmaxf(y.z, y.w));
+  }
+  if (q < V4) {
+    const float4 x = r4[q];
+    m0 = fmaxf(m0, fmaxf(x.x, x.y));
+    m1 = fmaxf(m1, fmaxf(x.z, x.w));
+  }
+  const float a = fmaxf(m0, m2) + 0.0f, b = fmaxf(m1, m3) + 0.0f;
+  const u32 ka = a > CTCPB_NEG ? fkey(a) : 0u, kb = b > CTCPB_NEG ? fkey(b) : 0u;
+  // 2. tau by counting (the pool lives in the packed-list half of cand)
+  u32* pool = reinterpret_cast<u32*>(cand + 32 * kLaneHits);
+  pool[lane] = ka;
+  pool[32 + lane] = kb;
+  __syncwarp();
+  int ga0 = 0, ga1 = 0, gb0 = 0, gb1 = 0;
+  const uint4* p4 = reinterpret_cast<const uint4*>(pool);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint4 v = p4[i];
+    ga0 += (int)(v.x >= ka) + (int)(v.y >= ka);
+    ga1 += (int)(v.z >= ka) + (int)(v.w >= ka);
+    gb0 += (int)(v.x >= kb) + (int)(v.y >= kb);
+    gb1 += (int)(v.z >= kb) + (int)(v.w >= kb);
+  }
+  u32 mine = 0u;
+  if (ka != 0u && ga0 + ga1 >= K) mine = ka;
+  if (kb != 0u && gb0 + gb1 >= K && kb > mine) mine = kb;
+  const u32 tk = __reduce_max_sync(RFULL, mine);
+  const float tauf = tk != 0u ? fkey_inv(tk) : -FLT_MAX;  // fewer than K live maxima: every live label
+  // 3. this lane's labels >= tau into its column of cand
+  int h = 0;
+  auto take = [&](float v, int c) {
+    if (v >= tauf && v > CTCPB_NEG) {
+      if (h < kLaneHits) cand[32 * h + lane] = lab_key(v + 0.0f, c);
+      ++h;
+    }
+  };
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int q0 = lane; q0 < V4; q0 += 128) {
+    float4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = q0 + 32 * u < V4 ? r4[q0 + 32 * u] : ninf;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)) >= tauf) {
+        const int c = (q0 + 32 * u) << 2;
+        take(x[u].x, c);
+        take(x[u].y, c + 1);
+        take(x[u].z, c + 2);
+        take(x[u].w, c + 3);
+      }
+    }
+  }
+  if (__any_sync(RFULL, h > kLaneHits)) return false;
+  int incl = h;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(RFULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int n = __shfl_sync(RFULL, incl, 31);
+  u64* packed = cand + 32 * kLaneHits;
+  __syncwarp();  // the pool is read by every lane before it is overwritten
+  for (int j = 0, pos = incl - h; j < h; ++j, ++pos) packed[pos] = cand[32 * j + lane];
+  __syncwarp();
+  // 4. rank by counting; ranks 0..L-1 form the list, rank L is the front
+  for (int i = lane; i < n; i += 32) {
+    const u64 me = packed[i];
+    int r0 = 0, r1 = 0;
+    const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(packed);
+    int j = 0;
+    for (; j + 1 < n; j += 2) {
+      const ulonglong2 v = k2[j >> 1];
+      r0 += (int)(v.x > me);
+      r1 += (int)(v.y > me);
+    }
+    if (j < n) r0 += (int)(packed[j] > me);
+    put_ranked(me, r0 + r1, L, d);
+  }
+  const int cnt = n < L ? n : L;
+  for (int i = cnt + lane; i < L; i += 32) {
+    d.ids[i] = -1;
+    d.lps[i] = CTCPB_NEG;
+  }
+  if (lane == 0) {
+    *d.cnt = cnt;
+    *d.lpb = lpb;
+    if (n <= L) {
+      *d.flp = CTCPB_NEG;
+      *d.fid = -1;
+    }
+    if (d.tout) *d.tout = d.t;
+  }
+  __syncwarp();
+  return true;
+}
+
 __host__ __device__ inline size_t rank_tma_per_warp(int V) {
   return align_up((size_t)V * 4, 128) + (size_t)kCandCap * 8 + 16;
 }
@@ -508,7 +642,10 @@ __device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int b
       }
     }
     __syncwarp();
-    const int n = rank_gather<E>(buf, V, L, cand, lane);
+    // lists up to 31 labels: the lean ranking, which has written the record
+    // when it succeeds; otherwise (and for longer lists) the general one
+    const bool lean = E == 2 && L + 1 <= kLeanK && rank_lean(buf, V, L, cand, lpb, lane, dc);
+    const int n = lean ? 0 : rank_gather<E>(buf, V, L, cand, lane);
     if (n < 0) {  // constant or near-constant row: plain ranking of the staged row
       if (lane == 0) buf[blank] = rawb;
       __syncwarp();
@@ -522,7 +659,7 @@ __device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int b
       mbar_arrive_tx(bar, bytes);
       bulk_g2s(buf, row, bytes, bar);
     }
-    if (n >= 0) rank_finish<E>(cand, n, L, lpb, lane, dc);
+    if (!lean && n >= 0) rank_finish<E>(cand, n, L, lpb, lane, dc);
     if (dc.flag) {  // publish the record: every lane's stores, then the flag
       __threadfence();
       __syncwarp();

@@ -12,7 +12,8 @@
 //     candidates are ranked by counting;
 //   * the ranking is PROVEN exact when every candidate left out scores below
 //     the beam-th kept one: hypothesis k's left-out labels score at most
-//     add(lp[next listed label], A_k), its unlisted ones add(front, A_k);
+//     add(lp[next listed label], A_k), its unlisted ones add(front, A_k), so
+//     it suffices that `beam` candidates score above the largest such bound;
 //   * round 2 (the proof failed): the beam-th kept score tau is a lower bound
 //     of the true one, so the candidates that matter are exactly those scoring
 //     >= tau; each hypothesis counts its listed labels >= tau (the list is
@@ -67,6 +68,7 @@ constexpr int kGath = 128;            // gathered log-probs per frame (beam + L 
 constexpr int kMaxRec = 32 + 8 * 68;  // record bytes for lists of L <= 66 labels
 constexpr u32 kH32 = 2166136261u;     // prefix hash of the empty prefix
 constexpr u32 kGold = 0x9e3779b9u;
+constexpr int kBlankWin = 1 << 30;    // flag bit of a blank winner in its slot's gained-label count
 
 struct __align__(16) WarpSmem {
   u64 keys[kGenCap];
@@ -77,14 +79,17 @@ struct __align__(16) WarpSmem {
   int bw[32];
   int fold_i[32], fold_c[32];
   int nfold, nkeys;
-  int4 st[32][2];   // bookkeeping of hypothesis k, read by the candidates extending it
-  int4 nst[32][4];  // the new hypothesis of slot r, written by the candidate ranked r
+  // Both tables are word-major ([word][slot]) so that 32 lanes writing or
+  // reading 16-byte words of different slots hit different banks.
+  int4 st[2][32];   // bookkeeping of hypothesis k, read by the candidates extending it
+  int4 nst[3][32];  // the new hypothesis of slot r, written by the candidate ranked r
   u32 fk[32];       // fold key of slot j: (i << 20 | last_j) when l_j = l_i + last_j
   u32 hk[32];       // prefix hash keys of the extension winners
   float gath[2][kGath];  // lp[t][slot] of the next step, slot = hypothesis or beam + list position
 };
 
 struct __align__(16) Tables {
+  float fc[kFCoef];             // the coefficients of log(1 + e^-d) (dlse)
   unsigned short qmap[33][32];  // nlive -> lane -> (hyp << 8 | list position), 0xffff: none
   unsigned char qcnt[33][32];  // nlive -> hyp -> listed labels of that hyp in the round-1 set
 };
@@ -150,6 +155,8 @@ __device__ __noinline__ void sort_keys(WarpSmem& W, int m, int lane) {
 // greedily by the smallest (k+1)(q_k+1).
 constexpr Tables make_tables() {
   Tables tb{};
+  const FCoef f = make_fcoef();
+  for (int i = 0; i < kFCoef; ++i) tb.fc[i] = f.c[i];
   for (int n = 0; n <= 32; ++n) {
     unsigned char q[32] = {};
     for (int k = 0; k < 32; ++k) tb.qmap[n][k] = 0xffff;
@@ -312,9 +319,16 @@ __device__ __noinline__ int warp_collect_select(WarpSmem& W, const char* rec, in
 // counting the larger score keys; equal scores among the kept ones (two kept
 // lanes with one rank) are resolved on the full key (score, source slot, token).
 __device__ __forceinline__ int warp_rank(u32 hi, u32 lo, bool live, int beam) {
-  int r = 0;
+  // four independent counts, so the compares do not form one dependent chain
+  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) r += (int)(__shfl_sync(WFULL, hi, j) > hi);
+  for (int j = 0; j < 32; j += 4) {
+    r0 += (int)(__shfl_sync(WFULL, hi, j) > hi);
+    r1 += (int)(__shfl_sync(WFULL, hi, j + 1) > hi);
+    r2 += (int)(__shfl_sync(WFULL, hi, j + 2) > hi);
+    r3 += (int)(__shfl_sync(WFULL, hi, j + 3) > hi);
+  }
+  int r = (r0 + r1) + (r2 + r3);
   const bool in = live && r < beam;
   const u32 orr = __reduce_or_sync(WFULL, in ? (1u << r) : 0u);
   if (__popc(orr) != __popc(__ballot_sync(WFULL, in))) {
@@ -484,17 +498,17 @@ __device__ __forceinline__ Cand make_cand(const WarpSmem& W, bool valid, int qk,
 // in ring row hrow.  nm: the new slot's merge source.
 __device__ __forceinline__ void commit_slot(WarpSmem& W, int r, const Cand& c, bool isb, float bpb, float bpnb,
                                             bool gap, int nm, int hrow) {
-  const int4 s0 = W.st[c.src][0], s1 = W.st[c.src][1];
+  const int4 s0 = W.st[0][c.src], s1 = W.st[1][c.src];
   float npb = isb ? bpb : CTCPB_NEG, npnb = isb ? bpnb : c.cs;
   if (gap) {
     npb = c.cs;
     npnb = CTCPB_NEG;
   }
   W.hist[hrow][r] = ((u32)c.src << 24) | ((u32)c.tok & 0xffffffu);
-  W.nst[r][0] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(c.cs), isb ? s0.x : c.tok);
-  W.nst[r][1] = make_int4(isb ? s0.y : s0.y + 1, isb ? s0.z : (int)h32((u32)s0.z, c.tok), isb ? s0.w : s0.z, s1.x);
-  W.nst[r][2] = make_int4(s1.y, s1.z + (isb ? 0 : 1), c.gl, nm);
-  W.nst[r][3] = make_int4(isb ? 1 : 0, 0, 0, 0);
+  W.nst[0][r] = make_int4(__float_as_int(npb), __float_as_int(npnb), __float_as_int(c.cs), isb ? s0.x : c.tok);
+  W.nst[1][r] = make_int4(isb ? s0.y : s0.y + 1, isb ? s0.z : (int)h32((u32)s0.z, c.tok), isb ? s0.w : s0.z, s1.x);
+  // the labels gained since the last token-store write, and bit 30: a blank winner
+  W.nst[2][r] = make_int4(s1.y, (s1.z + (isb ? 0 : 1)) | (isb ? kBlankWin : 0), c.gl, nm);
   // prefix key of an extension winner for the merge check (a blank winner's
   // dummy can only cause an extra exact comparison)
   W.hk[r] = isb ? 0xffffffffu : (h32((u32)s0.z, c.tok) ^ ((u32)(s0.y + 1) * kGold));
@@ -558,7 +572,7 @@ __device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const fl
     c.cs = ck_score(key);
     c.src = gsrc;
     c.tok = gtk;
-    const int4 s0 = W.st[gsrc][0], s1 = W.st[gsrc][1];
+    const int4 s0 = W.st[0][gsrc], s1 = W.st[1][gsrc];
     c.gl = (gisb || (s0.y > 0 && gtk == s0.x)) ? gsrc : -1;
     const int gm = gisb ? (s1.w >= 0 ? W.bw[s1.w] : -1) : W.bw[gsrc];
     commit_slot(W, lane, c, gisb, gisb ? W.bpb[gsrc] : CTCPB_NEG, gisb ? W.bpnb[gsrc] : CTCPB_NEG, gap, gm, hrow);
@@ -800,8 +814,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
       // (i, last) names the candidate this slot absorbs; a unique dummy otherwise
       const u32 foldk = mi >= 0 ? (((u32)mi << 20) | (u32)last) : (0x80000000u | (u32)lane);
       if (live) {
-        W.st[lane][0] = make_int4(last, len, (int)h, (int)hp);
-        W.st[lane][1] = make_int4(origin, lo, nnew, msrc);
+        W.st[0][lane] = make_int4(last, len, (int)h, (int)hp);
+        W.st[1][lane] = make_int4(origin, lo, nnew, msrc);
       }
       W.fk[lane] = foldk;
       __syncwarp();
@@ -843,8 +857,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
       const int n = nlive;
       // blank slot (3.4.1-3.4.3), branch-free so it overlaps the candidates below
       const bool anyfold = __any_sync(WFULL, mi >= 0);
-      const float bpnb = anyfold ? dlse(stay, mterm) : stay;  // dlse(stay, NEG) == stay
-      const float scB = live ? dlse(bpb, bpnb) : NEG;
+      const float bpnb = anyfold ? dlse(tb.fc, stay, mterm) : stay;  // dlse(stay, NEG) == stay
+      const float scB = live ? dlse(tb.fc, bpb, bpnb) : NEG;
       // proof bound of this hypothesis: what its best label outside the set scores
       float bnd = NEG;
       {
@@ -858,12 +872,19 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         }
       }
 
+      // the largest bound (0: none), for the proof below
+      const u32 bmax = __reduce_max_sync(WFULL, bnd > NEG ? fkey(bnd) : 0u);
       // ---- round 1: the staircase
       const unsigned short qm = lane >= n ? tb.qmap[n][lane] : (unsigned short)0xffff;
       const Cand c = make_cand<KB>(W, qm != 0xffff, qm == 0xffff ? 0 : (qm >> 8), qm == 0xffff ? 0 : (qm & 31), A,
                                    last, len, Rrep, my_id, my_lp, scB, n, cnt, cap, beam, blank, anyfold, lane);
       const bool clive = c.cs > NEG;
       const u32 hi = clive ? fkey(c.cs) : 0u;
+      // The ranking is proven exact when no hypothesis can reach the beam-th
+      // kept score with a label left out of the set: there is no bound, or at
+      // least `beam` live candidates score above the largest bound.  This
+      // needs only the scores, so it runs beside the ranking.
+      const bool proven = bmax == 0u || __popc(__ballot_sync(WFULL, clive && hi > bmax)) >= beam;
       const int r = warp_rank(hi, clive ? ~(((u32)c.src << 20) | (u32)c.tok) : 0u, clive, beam);
       const bool won = clive && r < beam;
       nw = __popc(__ballot_sync(WFULL, won));
@@ -875,11 +896,11 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         const int nm = __shfl_sync(WFULL, won ? r : -1, mq < 0 ? 0 : mq);
         if (won) commit_slot(W, r, c, lane < n, bpb, bpnb, gap, mq < 0 ? -1 : nm, s - win0);
       }
-      const unsigned lastm = __ballot_sync(WFULL, won && r == beam - 1);
-      const u32 sstar = __shfl_sync(WFULL, hi, lastm ? __ffs(lastm) - 1 : 0);
-      const bool proven = !__any_sync(WFULL, bnd > NEG && (nw < beam || fkey(bnd) >= sstar));
       PHASE_MARK(3);
       if (!proven) {
+        // the beam-th kept score: round 2's threshold
+        const unsigned lastm = __ballot_sync(WFULL, won && r == beam - 1);
+        const u32 sstar = __shfl_sync(WFULL, hi, lastm ? __ffs(lastm) - 1 : 0);
         // the record, for the slow selection, into shared memory
         const int4* rg = reinterpret_cast<const int4*>(rec_g + (size_t)s * rbytes);
         for (int i = lane; i < (int)(rbytes / 16); i += 32) reinterpret_cast<int4*>(W.rec1)[i] = __ldcg(rg + i);
@@ -894,7 +915,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
       __syncwarp();
       PHASE_MARK(4);
       if (lane < nw) {
-        const int4 n0 = W.nst[lane][0], n1 = W.nst[lane][1], n2 = W.nst[lane][2], n3 = W.nst[lane][3];
+        const int4 n0 = W.nst[0][lane], n1 = W.nst[1][lane], n2 = W.nst[2][lane];
         pb = __int_as_float(n0.x);
         pnb = __int_as_float(n0.y);
         sc = __int_as_float(n0.z);
@@ -904,10 +925,10 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
         hp = (u32)n1.z;
         origin = n1.w;
         lo = n2.x;
-        nnew = n2.y;
+        nnew = n2.y & ~kBlankWin;
         gl = n2.z;
         msrc = n2.w;
-        isb_w = n3.x != 0;
+        isb_w = (n2.y & kBlankWin) != 0;
       } else {
         msrc = -1;
       }

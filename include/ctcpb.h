@@ -49,6 +49,18 @@ typedef struct CUstream_st* ctcpb_stream_t;
 #define CTCPB_ESIZE (-4)    /* workspace/state buffer smaller than the size query */
 #define CTCPB_ECUDA (-5)    /* a CUDA launch failed (the runtime error is pending) */
 
+/*
+ * The coefficient table of the library's logsumexp ("GPU CTC Prefix Beam
+ * Search Decoder", section 3: logsumexp(a, b) = max + log(1 + exp(-|a - b|))).
+ * log(1 + e^-d) is evaluated on 96 segments [k/4, (k+1)/4) by the degree-5
+ * Taylor polynomial about the segment midpoint k/4 + 1/8 (zero for d >= 24);
+ * entry 6k + n is the n-th coefficient of segment k, the float32 rounding of
+ * the n-th derivative over n!.  Writes the first min(n, 576) entries to the
+ * HOST buffer `out` and returns 576 (the table's size), so callers and tests
+ * can check the arithmetic the kernels use; negative on a bad argument.
+ */
+int ctcpb_lse_table(float* out, int n);
+
 /* Device-side status bits (ctcpb_read_status). */
 #define CTCPB_DEV_HEADER 0x1u   /* state header does not match the call's dims/config: call skipped */
 #define CTCPB_DEV_PAGES 0x2u    /* paged token pool exhausted: the beam kept its prefix (section 13) */

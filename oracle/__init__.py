@@ -48,9 +48,9 @@ def lib():
             L = ctypes.CDLL(build())
             f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
             i32p = np.ctypeslib.ndpointer(np.int32, flags="C_CONTIGUOUS")
-            for n in ("E", "L"):
-                fn = getattr(L, f"ctcpb_oracle_{n}")
-                fn.restype, fn.argtypes = ctypes.c_float, [ctypes.c_float]
+            L.ctcpb_oracle_F.restype, L.ctcpb_oracle_F.argtypes = ctypes.c_float, [ctypes.c_float]
+            L.ctcpb_oracle_F_coefficients.restype = None
+            L.ctcpb_oracle_F_coefficients.argtypes = [f32p]
             for n in ("lse", "add"):
                 fn = getattr(L, f"ctcpb_oracle_{n}")
                 fn.restype, fn.argtypes = ctypes.c_float, [ctypes.c_float, ctypes.c_float]
@@ -80,19 +80,18 @@ def _f32(x):
     return np.array(x, dtype=np.float32, order="C", copy=True)
 
 
-def E(x):
-    """exp(x) for x <= 0 (Cody-Waite + Taylor), elementwise."""
-    a = _f32(x)
+def F(d):
+    """log(1 + e^-d) for d >= 0 (piecewise Taylor polynomial), elementwise."""
+    a = _f32(d)
     out = np.empty_like(a)
     lib().ctcpb_oracle_map(0, a.ravel(), a.ravel(), out.ravel(), a.size)
     return out
 
 
-def L(x):
-    """log(1 + x) for x in [0, 1] (atanh series), elementwise."""
-    a = _f32(x)
-    out = np.empty_like(a)
-    lib().ctcpb_oracle_map(1, a.ravel(), a.ravel(), out.ravel(), a.size)
+def F_coefficients() -> np.ndarray:
+    """F's coefficient table: [96 segments, 6] float32, c[k][n] ~ F^(n)(k/4 + 1/8) / n!."""
+    out = np.empty((96, 6), np.float32)
+    lib().ctcpb_oracle_F_coefficients(out.ravel())
     return out
 
 

@@ -16,13 +16,16 @@
 //   NEG          = -FLT_MAX, the additive identity of the log semiring
 //                  (section 3, the logsumexp definition).
 //   add(a, b)    = max(a + b, NEG)          -- a product of probabilities
-//   lse(a, b)    = max(a,b) + L(E(-|a-b|))  -- section 3's logsumexp
-//   E(x)         = exp(x) for x <= 0: Cody-Waite reduction x = n ln2 + r with
-//                  |r| <= ln2/2, degree-7 Taylor polynomial of e^r, times 2^n;
-//                  E(x) = 0 for x < -87 (below the smallest normal result).
-//   L(x)         = log(1 + x) for x in [0, 1] through the series
-//                  log(1+x) = 2 atanh(s), s = x/(2+x), summed to s^13; for
-//                  x > sqrt(2)-1 it uses log(1+x) = ln2 + 2 atanh((x-1)/(x+3)).
+//   lse(a, b)    = max(a,b) + F(|a-b|)      -- section 3's logsumexp
+//   F(d)         = log(1 + e^-d) for d >= 0, piecewise: on each of 96
+//                  segments [k/4, (k+1)/4), k = 0..95, the degree-5 Taylor
+//                  polynomial of F about the segment's midpoint d_k = k/4 +
+//                  1/8, in u = d - d_k, evaluated by Horner's rule with fmaf;
+//                  F(d) = 0 for d >= 24 (F(24) < 4e-11).  Its coefficients are
+//                  the float32 roundings of F^(n)(d_k) / n!, computed once in
+//                  double from libm's exp and log1p: F' = -s with s =
+//                  1/(1 + e^d), and ds/dd = s^2 - s, so every derivative is a
+//                  polynomial in s.
 //   lp read      = max(raw, NEG) + 0.0f (clamps -inf/NaN to NEG, -0 to +0).
 //
 // Decoding follows section 3 of the page:
@@ -83,66 +86,60 @@ namespace {
 
 constexpr float NEG = -FLT_MAX;
 
-// ln 2 split for Cody-Waite: HI keeps the top 16 significant bits of ln 2, so
-// n * HI is exact for |n| <= 127; LO = ln2 - HI rounded to float.
-constexpr float LN2_HI = 0.693145751953125f;
-constexpr float LN2_LO = 1.42860682030941723212e-6f;
-constexpr float LOG2E = 1.44269504088896340736f;
-constexpr float SQRT2_M1 = 0.41421356237309504880f;
+// The coefficient table of F: c[k][n] = F^(n)(d_k) / n! rounded to float.
+constexpr int kSeg = 96, kDeg = 5;
+constexpr float kFMax = 24.0f;
 
-float from_bits(uint32_t u) {
-  float f;
-  std::memcpy(&f, &u, 4);
-  return f;
+struct FTable {
+  float c[kSeg][kDeg + 1];
+  FTable() {
+    for (int k = 0; k < kSeg; ++k) {
+      const double d0 = k * 0.25 + 0.125;
+      const double s = 1.0 / (1.0 + std::exp(d0));
+      c[k][0] = (float)std::log1p(std::exp(-d0));
+      // P[i]: coefficient of s^i in the current derivative, starting at F' = -s
+      double P[kDeg + 2] = {0.0, -1.0};
+      double fact = 1.0;
+      for (int n = 1; n <= kDeg; ++n) {
+        double v = 0.0;
+        for (int i = kDeg + 1; i >= 0; --i) v = v * s + P[i];
+        fact *= n;
+        c[k][n] = (float)(v / fact);
+        // d/dd P(s) = P'(s) (s^2 - s)
+        double Q[kDeg + 2] = {};
+        for (int i = 1; i <= kDeg; ++i) {
+          Q[i + 1] += i * P[i];
+          Q[i] -= i * P[i];
+        }
+        for (int i = 0; i <= kDeg + 1; ++i) P[i] = Q[i];
+      }
+    }
+  }
+};
+const FTable& ftable() {
+  static const FTable t;
+  return t;
 }
 
-// exp(x) for x <= 0.
-float fE(float x) {
-  if (!(x >= -87.0f)) return 0.0f;
-  float t = x * LOG2E;
-  float n = std::rint(t);
-  float r = std::fmaf(n, -LN2_HI, x);
-  r = std::fmaf(n, -LN2_LO, r);
-  // Taylor series of e^r: sum_{k=0..7} r^k / k!
-  float p = (float)(1.0 / 5040.0);
-  p = std::fmaf(p, r, (float)(1.0 / 720.0));
-  p = std::fmaf(p, r, (float)(1.0 / 120.0));
-  p = std::fmaf(p, r, (float)(1.0 / 24.0));
-  p = std::fmaf(p, r, (float)(1.0 / 6.0));
-  p = std::fmaf(p, r, 0.5f);
-  p = std::fmaf(p, r, 1.0f);
-  p = std::fmaf(p, r, 1.0f);
-  int ni = (int)n;  // in [-126, 0]
-  float scale = from_bits((uint32_t)(ni + 127) << 23);
-  return p * scale;
-}
-
-// log(1 + x) for x in [0, 1].
-float fL(float x) {
-  const bool lo_half = x <= SQRT2_M1;
-  float num = lo_half ? x : x - 1.0f;
-  float den = lo_half ? 2.0f + x : x + 3.0f;
-  float hi = lo_half ? 0.0f : LN2_HI;
-  float lo = lo_half ? 0.0f : LN2_LO;
-  float s = num / den;
-  float z = s * s;
-  // 2 atanh(s) = 2s (1 + z/3 + z^2/5 + ... + z^6/13)
-  float q = (float)(1.0 / 13.0);
-  q = std::fmaf(q, z, (float)(1.0 / 11.0));
-  q = std::fmaf(q, z, (float)(1.0 / 9.0));
-  q = std::fmaf(q, z, (float)(1.0 / 7.0));
-  q = std::fmaf(q, z, (float)(1.0 / 5.0));
-  q = std::fmaf(q, z, (float)(1.0 / 3.0));
-  float w = z * q;
-  float t2 = s + s;
-  float r = std::fmaf(t2, w, t2);
-  return (r + lo) + hi;
+// log(1 + e^-d) for d >= 0.
+float fF(float d) {
+  if (!(d < kFMax)) return 0.0f;
+  const int k = (int)(d * 4.0f);
+  const float u = d - ((float)k * 0.25f + 0.125f);
+  const float* c = ftable().c[k];
+  float p = c[5];
+  p = std::fmaf(p, u, c[4]);
+  p = std::fmaf(p, u, c[3]);
+  p = std::fmaf(p, u, c[2]);
+  p = std::fmaf(p, u, c[1]);
+  p = std::fmaf(p, u, c[0]);
+  return p;
 }
 
 float lse(float a, float b) {
   float m = std::fmax(a, b);
   float d = std::fabs(a - b);
-  return m + fL(fE(-d));
+  return m + fF(d);
 }
 
 float add(float a, float b) { return std::fmax(a + b, NEG); }
@@ -383,8 +380,12 @@ void for_rows(int B, int threads, const std::function<void(int)>& fn) {
 
 extern "C" {
 
-float ctcpb_oracle_E(float x) { return fE(x); }
-float ctcpb_oracle_L(float x) { return fL(x); }
+float ctcpb_oracle_F(float d) { return fF(d); }
+// The 96 x 6 coefficients of F, segment-major.
+void ctcpb_oracle_F_coefficients(float* out) {
+  for (int k = 0; k < kSeg; ++k)
+    for (int n = 0; n <= kDeg; ++n) out[k * (kDeg + 1) + n] = ftable().c[k][n];
+}
 float ctcpb_oracle_lse(float a, float b) { return lse(a, b); }
 float ctcpb_oracle_add(float a, float b) { return add(a, b); }
 float ctcpb_oracle_log_threshold(float thr) { return log_threshold(thr); }
@@ -392,8 +393,7 @@ float ctcpb_oracle_log_threshold(float thr) { return log_threshold(thr); }
 void ctcpb_oracle_map(int which, const float* a, const float* b, float* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) {
     switch (which) {
-      case 0: out[i] = fE(a[i]); break;
-      case 1: out[i] = fL(a[i]); break;
+      case 0: out[i] = fF(a[i]); break;
       case 2: out[i] = lse(a[i], b[i]); break;
       default: out[i] = add(a[i], b[i]); break;
     }

@@ -187,3 +187,21 @@ def test_host_decode_sizes_and_validation(lib):
                                          ctypes.c_void_p(512), 1024, *outs) == D.ESIZE
     assert lib.ctcpb_decode_offline_host(ctypes.byref(cc), big, 50000, 5000, NULL, 2, 10, 5000,
                                          ctypes.c_void_p(260), 1 << 40, *outs) == D.EALIGN
+
+
+def test_lse_table_equals_the_oracle_and_mpmath(lib):
+    """The library's logsumexp coefficients (computed at compile time by its
+    own series) equal the oracle's (computed by its own code from libm) and the
+    Taylor coefficients mpmath computes to 40 digits, bit for bit."""
+    import numpy as np
+    import oracle as O
+    out = np.empty(576, np.float32)
+    fn = lib.ctcpb_lse_table
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    assert fn(out.ctypes.data, 576) == 576
+    assert fn(None, 0) == 576 and fn(None, -1) < 0
+    ours = out.reshape(96, 6)
+    assert np.array_equal(ours.view(np.int32), O.F_coefficients().view(np.int32))
+    from test_oracle_math import exact_coefficients
+    assert np.array_equal(ours.view(np.int32), exact_coefficients().view(np.int32))

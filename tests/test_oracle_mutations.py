@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes.  Each case plants one mistake
 in a copy of oracle/ctcpb_oracle.cpp (a dropped term, a wrong path, a wrong
 coefficient, an off-by-one, a reversed tie-break), compiles it into a temporary library, and runs
-the independent pins on it: exp/log1p/lse against float64, and the unpruned
+the independent pins on it: F = log(1 + e^-d) and its coefficients against
+float64 and mpmath, lse against float64, and the unpruned
 decode against the float64 enumeration of every alignment, plain and with a
 cap, frame skipping, a word-boundary label and label bonuses ("GPU CTC Prefix
 Beam Search Decoder", sections 3.1-3.5), and the hand-derived tie cases of
@@ -53,15 +54,14 @@ def unpruned_matches(lp, exact, **kw):
 def pins_hold():
     """Every independent pin, as one boolean per pin."""
     res = {}
-    # float32 exp / log1p / lse against float64, within 2 ulp (lse: 4)
-    xs = np.concatenate([-np.logspace(-6, np.log10(87.0), 200), [0.0, -0.5, -1.0, -20.0]]).astype(np.float32)
-    e = O.E(xs).astype(np.float64)
-    ref = np.exp(xs.astype(np.float64))
-    res["E"] = bool(np.all(np.abs(e - ref) <= 2 * np.spacing(ref.astype(np.float32)).astype(np.float64)))
-    us = np.linspace(0.0, 1.0, 201).astype(np.float32)
-    l = O.L(us).astype(np.float64)
-    ref = np.log1p(us.astype(np.float64))
-    res["L"] = bool(np.all(np.abs(l - ref) <= 2 * np.spacing(np.maximum(ref, 1e-30).astype(np.float32))))
+    # F = log(1 + e^-d) within 2 ulp of float64 on every segment, its
+    # coefficients against mpmath's Taylor coefficients, lse within 4 ulp
+    ds = np.concatenate([np.linspace(0.0, 23.99, 4001), [1e-6, 23.9999]]).astype(np.float32)
+    f = O.F(ds).astype(np.float64)
+    ref = np.log1p(np.exp(-ds.astype(np.float64)))
+    res["F"] = bool(np.all(np.abs(f - ref) <= 2 * np.spacing(ref.astype(np.float32)).astype(np.float64)))
+    from test_oracle_math import exact_coefficients
+    res["F coefficients"] = bool(np.array_equal(O.F_coefficients(), exact_coefficients()))
     rng = np.random.default_rng(3)
     a = rng.uniform(-30, 0, 300).astype(np.float32)
     b = rng.uniform(-30, 0, 300).astype(np.float32)
@@ -114,11 +114,12 @@ MUTATIONS = {
     "space label repeats like any label": (
         "float ext = (!empty && c == last && c != space) ? add(v, pb[k]) : add(v, A[k]);",
         "float ext = (!empty && c == last) ? add(v, pb[k]) : add(v, A[k]);"),
-    "exp: wrong Taylor coefficient": ("p = std::fmaf(p, r, (float)(1.0 / 6.0));",
-                                      "p = std::fmaf(p, r, (float)(1.0 / 5.0));"),
-    "log1p: wrong series coefficient": ("q = std::fmaf(q, z, (float)(1.0 / 3.0));",
-                                        "q = std::fmaf(q, z, (float)(1.0 / 4.0));"),
-    "lse: signed difference": ("float d = std::fabs(a - b);", "float d = a - b;"),
+    "F: Taylor polynomial about the segment start": ("const float u = d - ((float)k * 0.25f + 0.125f);",
+                                                     "const float u = d - ((float)k * 0.25f);"),
+    "F: the degree-5 term dropped": ("float p = c[5];", "float p = 0.0f * c[5];"),
+    "F: wrong derivative recurrence": ("Q[i] -= i * P[i];", "Q[i] += i * P[i];"),
+    "F: wrong factorial": ("fact *= n;", "fact *= n + 1;"),
+    "lse: the smaller argument as the base": ("float m = std::fmax(a, b);", "float m = std::fmin(a, b);"),
     "ties: source slot descending": ("if (x.src != y.src) return x.src < y.src;",
                                      "if (x.src != y.src) return x.src > y.src;"),
     "ties: token descending": ("return x.tok < y.tok;", "return x.tok > y.tok;"),
