@@ -434,9 +434,11 @@ __device__ void rank_finish(const u64* cand, int n, int L, float lpb, int lane, 
 //      maxima from shared memory (broadcast) and keeps its maxima that have at
 //      least K maxima >= them; the largest such is tau.  At least K labels
 //      score >= tau, so the top K all do;
-//   3. each lane appends its own labels >= tau to a column of `cand` (at most
-//      kLaneHits each, no cross-lane traffic), then one scan packs the columns
-//      into a contiguous list;
+//   3. each lane tests its float4 slices by their maxima against tau (one
+//      compare each, no branch) into a bit mask, then reads the few slices
+//      with a hit again and appends their labels >= tau to its own column of
+//      `cand` (at most kLaneHits each, no cross-lane traffic); one scan packs
+//      the columns into a contiguous list;
 //   4. each packed key's rank = how many packed keys are larger (keys are
 //      distinct: they hold the label); ranks below L fill the list, rank L is
 //      the front.
@@ -491,26 +493,38 @@ __device__ __forceinline__ bool rank_lean(const float* __restrict__ row, int V, 
   const float tauf = tk != 0u ? fkey_inv(tk) : -FLT_MAX;  // fewer than K live maxima: every live label
   // 3. this lane's labels >= tau into its column of cand
   int h = 0;
-  auto take = [&](float v, int c) {
-    if (v >= tauf && v > CTCPB_NEG) {
-      if (h < kLaneHits) cand[32 * h + lane] = lab_key(v + 0.0f, c);
-      ++h;
-    }
-  };
   const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  for (int q0 = lane; q0 < V4; q0 += 128) {
+  // a label is taken iff v >= t2: t2 = tau, or the least float above NEG when
+  // tau is NEG (fewer than K live maxima), so dead labels and NaN never pass
+  const float t2 = fmaxf(tauf, __int_as_float(0xff7ffffe));
+  // Each round tests four of the lane's float4 slices by their maxima (one
+  // compare each) into a bit mask; every eighth round (and the last) the few
+  // slices with a hit are read again and their labels taken.
+  const int nrounds = (V4 + 127) >> 7;
+  u32 fm = 0u;
+  int r0 = 0;  // round of mask bit 0
+  for (int r = 0; r < nrounds; ++r) {
+    const int q0 = lane + 128 * r;
     float4 x[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) x[u] = q0 + 32 * u < V4 ? r4[q0 + 32 * u] : ninf;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)) >= tauf) {
-        const int c = (q0 + 32 * u) << 2;
-        take(x[u].x, c);
-        take(x[u].y, c + 1);
-        take(x[u].z, c + 2);
-        take(x[u].w, c + 3);
+    for (int u = 0; u < 4; ++u)
+      fm |= (u32)(fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w)) >= t2) << (4 * (r - r0) + u);
+    if (r - r0 == 7 || r == nrounds - 1) {
+      for (; fm; fm &= fm - 1u) {
+        const int bit = __ffs(fm) - 1;
+        const int q = lane + 128 * (r0 + (bit >> 2)) + 32 * (bit & 3);
+        const float4 y = r4[q];
+        const float v[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          if (v[cc] >= t2) {
+            if (h < kLaneHits) cand[32 * h + lane] = lab_key(v[cc] + 0.0f, 4 * q + cc);
+            ++h;
+          }
       }
+      r0 = r + 1;
     }
   }
   if (__any_sync(RFULL, h > kLaneHits)) return false;
