@@ -25,7 +25,7 @@ constexpr int kMaxBoost = 4096;               // boosted labels per row
 constexpr float kMaxBonus = 1e6f;             // largest bonus magnitude
 constexpr int kStreamDefaultCap = 4096;       // section 11: STREAMING_MAX_SEQ_LEN
 constexpr u32 kMagic = 0x42504354u;           // "TCPB"
-constexpr u32 kVersion = 2u;
+constexpr u32 kVersion = 3u;
 
 // ---------------------------------------------------------------- layout
 //
@@ -51,7 +51,11 @@ struct RowHdr {
   int32_t t_prev;  // frame index of the last decoded step (-1 before the first)
   int32_t nlive;   // live hypotheses in slots [0, nlive)
   int32_t parity;  // token buffer holding the current hypotheses
-  int32_t pad[3];
+  // flat storage: 1 when each slot k's first plo[k] labels are still in the
+  // other buffer, at row porg[k] (the warp step kernel leaves them there at
+  // the end of a call and copies them at the start of the next)
+  int32_t pending;
+  int32_t pad[2];
 };
 
 struct Layout {
@@ -64,7 +68,7 @@ struct Layout {
   int max_boost, hcap;  // boosted labels per row and hash slots per row (a power of two, 0: no boosting)
   size_t rec_bytes;
   size_t o_rows, o_pb, o_pnb, o_sc, o_last, o_len, o_h, o_hp, o_msrc;
-  size_t o_clist, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;
+  size_t o_clist, o_porg, o_plo, o_pages, o_btab, o_refc, o_pool, o_ptop, o_pnext;
   size_t o_recs, o_rflag, o_sel, o_nsel, o_bkey, o_bval, total;
 };
 
@@ -118,6 +122,8 @@ inline Layout make_layout(int B, int V, int beam, int cap, int paged, int page_s
   o.o_msrc = take(4 * nb);
   if (!paged) {
     o.o_clist = take(4 * 2 * nb * (size_t)o.ldseq);
+    o.o_porg = take(4 * nb);
+    o.o_plo = take(4 * nb);
   } else {
     o.o_pages = take(4 * (size_t)B * o.ppr * (size_t)page_size);
     o.o_btab = take(4 * 2 * nb * (size_t)o.max_lp);
@@ -159,6 +165,9 @@ struct View {
   __host__ __device__ int* clist(int par, int b, int k) const {
     return (int*)(base + lay.o_clist) + (((size_t)par * lay.B + b) * lay.beam + k) * (size_t)lay.ldseq;
   }
+  // flat: a pending prefix's row in the other buffer and its length, [B][beam]
+  __host__ __device__ int* porg() const { return (int*)(base + lay.o_porg); }
+  __host__ __device__ int* plo() const { return (int*)(base + lay.o_plo); }
   // paged storage, per-row partitions of ppr pages
   __host__ __device__ int* page(int b, int phys) const {
     return (int*)(base + lay.o_pages) + ((size_t)b * lay.ppr + phys) * (size_t)lay.page_size;

@@ -145,8 +145,8 @@ __global__ void k_init(View st) {
   }
   for (size_t b = tid; b < (size_t)L.B; b += nthr) {
     RowHdr r;
-    r.step = 0; r.tcount = 0; r.t_prev = -1; r.nlive = 0; r.parity = 0;
-    r.pad[0] = r.pad[1] = r.pad[2] = 0;
+    r.step = 0; r.tcount = 0; r.t_prev = -1; r.nlive = 0; r.parity = 0; r.pending = 0;
+    r.pad[0] = r.pad[1] = 0;
     st.rows()[b] = r;
     if (L.paged) {
       st.ptop()[b] = 0;
@@ -1304,13 +1304,19 @@ __global__ void __launch_bounds__(128) k_output(View st, int nbest, int* __restr
   }
   __syncthreads();
   TokenStore tok{st, b};
+  // flat storage left by the warp kernel: a slot's first plo labels may still
+  // be in the other buffer (row porg)
+  const bool pend = !Ly.paged && rh.pending != 0;
   for (int n = 0; n < nbest; ++n) {
     const size_t o = (size_t)b * nbest + n;
     int* dst = out_tokens + o * (size_t)out_len;
     if (n < nlive) {
       const int k = order[n];
       const int L = st.len()[(size_t)b * beam + k];
-      for (int x = tid; x < out_len; x += blockDim.x) dst[x] = x < L ? tok.get(rh.parity, k, x) : -1;
+      const int plo = pend ? st.plo()[(size_t)b * beam + k] : 0;
+      const int* pre = plo > 0 ? st.clist(rh.parity ^ 1, b, st.porg()[(size_t)b * beam + k]) : nullptr;
+      for (int x = tid; x < out_len; x += blockDim.x)
+        dst[x] = x < L ? (x < plo ? pre[x] : tok.get(rh.parity, k, x)) : -1;
       if (tid == 0) {
         out_lengths[o] = L;
         out_scores[o] = scs[k];

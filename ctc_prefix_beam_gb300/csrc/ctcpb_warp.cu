@@ -406,9 +406,11 @@ __device__ __noinline__ int round2_plan(float A, int len, bool live, float my_lp
 // Materialise the history ring (steps win0..s_last) into the other parity of
 // the flat rows: each hypothesis' row = its origin row's first lo labels + the
 // nnew labels it gained in the window.  rows[p]: this row's hypotheses in
-// parity p, ldseq labels apart.
+// parity p, ldseq labels apart.  prefixes = false writes only the gained
+// labels and leaves the prefixes in the old parity (a pending prefix, copied
+// later by a call with an empty window and prefixes = true).
 __device__ __noinline__ void flush_rows(WarpSmem& W, int* rows0, int* rows1, int ldseq, int lane, int nlive, int blank,
-                                        int par, int win0, int s_last, int origin, int lo, int nnew) {
+                                        int par, int win0, int s_last, int origin, int lo, int nnew, bool prefixes) {
   int* const from_rows = par ? rows1 : rows0;
   int* const to_rows = par ? rows0 : rows1;
   int slot = lane, rem = nnew;
@@ -422,7 +424,7 @@ __device__ __noinline__ void flush_rows(WarpSmem& W, int* rows0, int* rows1, int
     slot = (int)(e >> 24);
   }
   // origin prefixes, four rows at a time with every load issued before the stores
-  for (int w0 = 0; w0 < nlive; w0 += 4) {
+  for (int w0 = 0; prefixes && w0 < nlive; w0 += 4) {
     int4 v[4][2];
     int nv[4], o[4];
 #pragma unroll
@@ -725,7 +727,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   int* const rows0 = st.clist(0, b, 0);
   int* const rows1 = st.clist(1, b, 0);
   auto flush = [&](int s_last) {
-    flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par, win0, s_last, origin, lo, nnew);
+    flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par, win0, s_last, origin, lo, nnew, true);
     par ^= 1;
     origin = lane;
     lo = len;
@@ -733,6 +735,13 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     win0 = s_last + 1;
   };
 
+  // The previous call left each slot's prefix in the other parity: copy it
+  // now, while the first records are still being ranked.
+  if (rh0.pending) {
+    const int po = lane < nlive ? st.porg()[rb + lane] : -1;
+    const int pl = lane < nlive ? st.plo()[rb + lane] : 0;
+    flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par ^ 1, 0, -1, po, pl, 0, true);
+  }
   if (!await_records(nsteps < 2 ? nsteps : 2)) {
     bail();
     return;
@@ -977,7 +986,14 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   }
   cp_wait_all();
   __syncwarp();
-  flush(nsteps - 1);
+  // the gained labels only; the prefixes stay pending in the old parity (the
+  // next call or the N-best gather reads them from there)
+  flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par, win0, nsteps - 1, origin, lo, nnew, false);
+  if (lane < nlive) {
+    st.porg()[rb + lane] = origin;
+    st.plo()[rb + lane] = lo;
+  }
+  par ^= 1;
 
   if (lane < beam) {
     st.pb()[rb + lane] = pb;
@@ -1004,6 +1020,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     rr.t_prev = t_prev;
     rr.nlive = nlive;
     rr.parity = par;
+    rr.pending = 1;
     st.rows()[b] = rr;
   }
 }
