@@ -600,14 +600,37 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   Tables& tb = *reinterpret_cast<Tables*>(smem);
   const int wid = threadIdx.x >> 5;
   WarpSmem& W = reinterpret_cast<WarpSmem*>(smem + align_up(sizeof(Tables), 16))[wid < kWPC ? wid : 0];
+  // per step warp: its row's pending prefixes are in place (set by a helper warp)
+  volatile int* pend_done = reinterpret_cast<int*>(smem + align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem));
   const int lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < (int)(sizeof(Tables) / 16); i += blockDim.x)
     reinterpret_cast<int4*>(&tb)[i] = reinterpret_cast<const int4*>(&g_tables)[i];
+  if (threadIdx.x < kWPC) pend_done[threadIdx.x] = 0;
   __syncthreads();
 
   const Layout& Ly = st.lay;
+  if (wid >= kWPC) {
+    // A helper warp: the prefixes that the previous call left in the other
+    // parity of the row of step warp wid - kWPC, copied while that warp waits
+    // for its first ranked records.  (Repeating the copy is harmless, so it
+    // does not matter whether the step warp decodes anything in this call.)
+    const int hw = wid - kWPC, hb = row_block * kWPC + hw;
+    if (hw < kWPC && hb < Ly.B) {
+      const RowHdr rh = st.rows()[hb];
+      if (rh.pending && (mode == 0 || header_matches(st))) {
+        const size_t hrb = (size_t)hb * Ly.beam;
+        const int po = lane < rh.nlive ? st.porg()[hrb + lane] : -1;
+        const int pl = lane < rh.nlive ? st.plo()[hrb + lane] : 0;
+        flush_rows(W, st.clist(0, hb, 0), st.clist(1, hb, 0), Ly.ldseq, lane, rh.nlive, Ly.blank, rh.parity ^ 1, 0,
+                   -1, po, pl, 0, true);
+      }
+      __threadfence_block();
+      if (lane == 0) pend_done[hw] = 1;
+    }
+    return;
+  }
   const int b = row_block * kWPC + wid;
-  if (wid >= kWPC || b >= Ly.B) return;
+  if (b >= Ly.B) return;
   // the row's label-boost table (keys null: no boosting; BOOST instantiations only)
   const BoostTab bt{BOOST ? st.bkey(b) : nullptr, BOOST ? st.bval(b) : nullptr, Ly.hcap - 1};
   const int beam = Ly.beam, cap = Ly.cap, blank = Ly.blank, V = Ly.V, Lpad = Ly.Lpad;
@@ -726,7 +749,30 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   // Materialise the ring into the other parity of the flat rows.
   int* const rows0 = st.clist(0, b, 0);
   int* const rows1 = st.clist(1, b, 0);
+  // Before the rows are first written or compared: the helper warp has put
+  // the previous call's pending prefixes in place (a bounded wait).  Blocks
+  // without helper warps (the stand-alone step kernel) copy them here.
+  const bool helpers = (int)blockDim.x >= 64 * kWPC;
+  if (rh0.pending && !helpers) {
+    const int po = lane < nlive ? st.porg()[rb + lane] : -1;
+    const int pl = lane < nlive ? st.plo()[rb + lane] : 0;
+    flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par ^ 1, 0, -1, po, pl, 0, true);
+  }
+  bool pend_wait = rh0.pending != 0 && helpers;
+  auto wait_pending = [&]() {
+    if (!pend_wait) return;
+    pend_wait = false;
+    long long spin = 0;
+    while (pend_done[wid] == 0 && spin < kFlagSpins) {
+      __nanosleep(64);
+      ++spin;
+    }
+    if (spin >= kFlagSpins && lane == 0) atomicOr(&st.hdr()->status, CTCPB_DEV_TIMEOUT);
+    __threadfence_block();
+    __syncwarp();
+  };
   auto flush = [&](int s_last) {
+    wait_pending();
     flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par, win0, s_last, origin, lo, nnew, true);
     par ^= 1;
     origin = lane;
@@ -735,13 +781,6 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     win0 = s_last + 1;
   };
 
-  // The previous call left each slot's prefix in the other parity: copy it
-  // now, while the first records are still being ranked.
-  if (rh0.pending) {
-    const int po = lane < nlive ? st.porg()[rb + lane] : -1;
-    const int pl = lane < nlive ? st.plo()[rb + lane] : 0;
-    flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par ^ 1, 0, -1, po, pl, 0, true);
-  }
   if (!await_records(nsteps < 2 ? nsteps : 2)) {
     bail();
     return;
@@ -988,6 +1027,7 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
   __syncwarp();
   // the gained labels only; the prefixes stay pending in the old parity (the
   // next call or the N-best gather reads them from there)
+  wait_pending();
   flush_rows(W, rows0, rows1, Ly.ldseq, lane, nlive, blank, par, win0, nsteps - 1, origin, lo, nnew, false);
   if (lane < nlive) {
     st.porg()[rb + lane] = origin;
@@ -1061,7 +1101,7 @@ bool step_warp_fits(const Layout& lay) {
   return lay.beam <= 16 && !lay.paged && lay.rec_bytes <= (size_t)kMaxRec;
 }
 
-size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem); }
+size_t step_warp_smem_bytes() { return align_up(sizeof(Tables), 16) + kWPC * sizeof(WarpSmem) + 16 * kWPC; }
 
 template <int KB, bool BOOST>
 static cudaError_t launch_kb(const View& st, const float* lp, long long sb, long long stt, int mode,
