@@ -989,8 +989,8 @@ __device__ __forceinline__ void step_warp_body(const View& st, const float* __re
     {
       const bool wl = lane < nw;
       const bool want = wl && step > 0 && isb_w && msrc < 0 && len >= 1;
-      if (__any_sync(WFULL, want)) {
-        const unsigned match = want ? smem_match<KB>(W.hk, hp ^ ((u32)(len - 1) * kGold), nw) : 0u;
+      {
+        const unsigned match = smem_match<KB>(W.hk, hp ^ ((u32)(len - 1) * kGold), nw);
         const bool cand = want && match != 0u;
         if (__any_sync(WFULL, cand)) {
           ++c_hash;
