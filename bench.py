@@ -69,6 +69,8 @@ def args_():
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the compact record of the other workloads (default run: recorded after the headline)")
     p.add_argument("--workload-steps", type=int, default=5)
+    p.add_argument("--stream-ticks", type=int, default=0,
+                   help="stream workload: decode only the first N ticks of the session (profiling); 0: all")
     return p.parse_args()
 
 
@@ -235,12 +237,15 @@ def job_frames(world: int, B: int, T: int) -> int:
 
 # ------------------------------------------------------------------ streaming (config 3)
 
-def measure_stream(w, steps, warmup, torch, D, dev, clocks=None, cpu_sample=False):
+def measure_stream(w, steps, warmup, torch, D, dev, clocks=None, cpu_sample=False, max_ticks=0):
     """One step = one streaming session: stream_init, then every 16-frame tick of
     the 128 staggered streams through stream_step_chunk, ticks resident in HBM.
-    Returns the session's figures (device time, end to end, bytes)."""
+    Returns the session's figures (device time, end to end, bytes).  max_ticks >
+    0 keeps only the session's first ticks (a bounded case for profiling)."""
     offsets = synth.stream_offsets(w)
     nt = synth.n_ticks(w, offsets)
+    if max_ticks > 0:
+        nt = min(nt, max_ticks)
     cache = {}
     ticks, host_ticks = [], []
     for k in range(nt):
@@ -317,7 +322,7 @@ def measure_stream(w, steps, warmup, torch, D, dev, clocks=None, cpu_sample=Fals
     e2e_ms = statistics.mean(te)
     h2d = sum(hc.numel() * 4 + hn.numel() * 4 for hc, hn in host_ticks)
     d2h = sum(r.numel() * r.element_size() for r in res_host)
-    valid = np.full(w.B, w.T)
+    valid = np.sum([hn.numpy() for _, hn in host_ticks], axis=0)  # frames each stream decoded
     by = algorithmic_bytes(w, valid, valid, res_host[1].numpy())
 
     cpu = None
@@ -333,13 +338,13 @@ def measure_stream(w, steps, warmup, torch, D, dev, clocks=None, cpu_sample=Fals
         dt = time.perf_counter() - t0
         cpu = {"value": ns * w.T / dt, "unit": "frames/s", "cores": cores, "kind": "oracle",
                "sample": f"{ns} whole streams of {w.T} frames decoded offline, {cores} threads, {dt:.2f} s"}
-    return dict(ms=ms, ticks=nt, fused=fused, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, bytes=by, frames=w.B * w.T,
+    return dict(ms=ms, ticks=nt, fused=fused, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, bytes=by, frames=int(valid.sum()),
                 cpu=cpu, clocks=clk.summary() if clocks is not None else None, launches=steps * (1 + nt))
 
 
 def run_stream(a, w, torch, D, dev):
     m = measure_stream(w, a.steps, a.warmup, torch, D, dev, clocks=Clocks(0, enabled=not a.no_clocks),
-                       cpu_sample=not a.no_cpu_baseline)
+                       cpu_sample=not a.no_cpu_baseline, max_ticks=a.stream_ticks)
     ms, nt = m["ms"], m["ticks"]
     gbs = m["bytes"]["decode"] / (ms / 1e3) / 1e9
     peak, peak_kind = peaks()
