@@ -663,10 +663,10 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
     const int srow = srow_next;  // batch or chunk row
     const int t = mode == 0 ? srow : (mode == 1 ? tcount + s : tcount + srow - tile_start);
     const float* row = lp + (long long)b * sb + (long long)srow * stt;
-    if (s + 1 < nsteps) srow_next = srow_of(s + 1);  // used at the winners: its load has time
     cp_wait_all();
     gsync<NT>();
     if (s + 1 < nsteps) prefetch_rec(s + 1);  // rec[(s+1) & 1] was step s-1's, done
+    if (s + 1 < nsteps) srow_next = srow_of(s + 1);  // used at the winners: its load has time
     BPHASE(0);
     const unsigned char* rbuf = S.rec[s & 1];
     const RecHdr& rhd = *reinterpret_cast<const RecHdr*>(rbuf);

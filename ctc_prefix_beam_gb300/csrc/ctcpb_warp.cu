@@ -516,6 +516,102 @@ __device__ __forceinline__ void commit_slot(WarpSmem& W, int r, const Cand& c, b
   W.hk[r] = isb ? 0xffffffffu : (h32((u32)s0.z, c.tok) ^ ((u32)(s0.y + 1) * kGold));
 }
 
+// The exhaustive selection when the frame's list bounds every unlisted label:
+// the candidates scoring at least thr (blank slots, repeats, listed
+// extensions) are compacted into W.keys with the running count in a register,
+// then each lane ranks its keys by counting the larger ones (the keys are
+// distinct: no two candidates share a source slot and a token).  Leaves the
+// winners in order in W.keys[0 .. nw) and returns nw, or -1 when
+// warp_collect_select must run instead: more than kFastKeys candidates, or an
+// unlisted label that could still reach the beam.
+constexpr int kFastKeys = 128;
+__device__ __noinline__ int fast_exhaustive(WarpSmem& W, const char* rec, int Lpad, u64 thr, float A, int last,
+                                               int len, bool live, float Rrep, float scB, int mi, int n, int cap,
+                                               int beam, int blank, int lane) {
+  const RecHdr* h = (const RecHdr*)rec;
+  const int cnt = h->cnt;
+  const int* ids = (const int*)(rec + 32);
+  const float* lps = (const float*)(rec + 32 + 4 * Lpad);
+  const unsigned lt = (1u << lane) - 1u;
+  int base = 0;  // keys written so far (the same in every lane)
+  // slot j absorbs the extension (mi_j, last_j): it is not a candidate of its own
+  const unsigned folds = __ballot_sync(WFULL, live && mi >= 0);
+  bool rep_folded = false;
+  for (unsigned f = folds; f; f &= f - 1u) {
+    const int j = __ffs(f) - 1;
+    const int ij = __shfl_sync(WFULL, mi, j), cj = __shfl_sync(WFULL, last, j);  // every lane shuffles
+    rep_folded |= ij == lane && cj == last;
+  }
+  {
+    const u64 kb = (live && scB > CTCPB_NEG) ? cand_key(scB, lane, blank) : 0ull;
+    const u64 kr = (live && Rrep > CTCPB_NEG && !rep_folded) ? cand_key(Rrep, lane, last) : 0ull;
+    const bool tb = kb != 0ull && kb >= thr, tr = kr != 0ull && kr >= thr;
+    const unsigned mb = __ballot_sync(WFULL, tb), mr = __ballot_sync(WFULL, tr);
+    if (tb) W.keys[__popc(mb & lt)] = kb;
+    if (tr) W.keys[__popc(mb) + __popc(mr & lt)] = kr;
+    base = __popc(mb) + __popc(mr);
+  }
+  for (int p0 = 0; p0 < cnt; p0 += 32) {
+    const int p = p0 + lane;
+    const bool pv = p < cnt;
+    const int c = pv ? ids[p] : -1;
+    const float v = pv ? lps[p] : CTCPB_NEG;
+    unsigned fk = 0u;  // hypotheses whose extension by c a fold absorbs
+    for (unsigned f = folds; f; f &= f - 1u) {
+      const int j = __ffs(f) - 1;
+      const int ij = __shfl_sync(WFULL, mi, j), cj = __shfl_sync(WFULL, last, j);
+      if (cj == c) fk |= 1u << ij;
+    }
+    for (int k = 0; k < n; ++k) {
+      const float a = __shfl_sync(WFULL, A, k);
+      const int lk = __shfl_sync(WFULL, len, k), tk = __shfl_sync(WFULL, last, k);
+      const float sc = dadd(v, a);
+      const bool ok = pv && lk < cap && !(lk > 0 && c == tk) && ((fk >> k) & 1u) == 0u && sc > CTCPB_NEG;
+      const u64 key = ok ? cand_key(sc, k, c) : 0ull;
+      const bool take = ok && key >= thr;
+      const unsigned m = __ballot_sync(WFULL, take);
+      const int at = base + __popc(m & lt);
+      if (take && at < kFastKeys) W.keys[at] = key;
+      base += __popc(m);
+    }
+  }
+  if (base > kFastKeys) return -1;
+  __syncwarp();
+  const int m = base;
+  u64 x[kFastKeys / 32];
+  int r[kFastKeys / 32];
+#pragma unroll
+  for (int i = 0; i < kFastKeys / 32; ++i) {
+    const int q = lane + 32 * i;
+    x[i] = q < m ? W.keys[q] : 0ull;
+    r[i] = 0;
+  }
+  for (int t = 0; t < m; ++t) {
+    const u64 y = W.keys[t];
+#pragma unroll
+    for (int i = 0; i < kFastKeys / 32; ++i) r[i] += (int)(y > x[i]);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < kFastKeys / 32; ++i)
+    if (x[i] != 0ull && r[i] < beam) W.keys[r[i]] = x[i];
+  __syncwarp();
+  const int nw = m < beam ? m : beam;
+  // an unlisted label scores at most front_lp: it must stay below the beam-th key
+  const float front_lp = h->front_lp;
+  if (front_lp > CTCPB_NEG) {
+    u64 t2 = thr;
+    if (nw == beam && W.keys[beam - 1] > t2) t2 = W.keys[beam - 1] & 0xffffffff00000000ull;
+    bool bad = false;
+    if (live && len < cap) {
+      const float u = dadd(front_lp, A);
+      bad = u > CTCPB_NEG && ((u64)fkey(u) << 32) >= t2;
+    }
+    if (__any_sync(WFULL, bad)) return -1;
+  }
+  return nw;
+}
+
 // The selection when the first candidate set did not prove it: round 2 (every
 // listed candidate scoring >= sstar, when they fit the warp), else the
 // exhaustive selection.  Writes the winners' new slots like the fast path.
@@ -562,7 +658,8 @@ __device__ __forceinline__ int slow_select(WarpSmem& W, const char* Rc, const fl
   W.bw[lane] = -1;
   __syncwarp();
   const u64 thr = nw1 == beam ? ((u64)sstar << 32) : 0ull;
-  const int res = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr, bt);
+  int res = fast_exhaustive(W, Rc, Lpad, thr, A, last, len, live, Rrep, scB, mi, n, cap, beam, blank, lane);
+  if (res < 0) res = warp_collect_select(W, Rc, Lpad, n, beam, cap, blank, V, row, lane, thr, bt);
   const int nw = res & 0xffff;
   const u64 key = lane < nw ? W.keys[lane] : 0ull;
   const int gsrc = ck_src(key), gtk = ck_tok(key);
