@@ -449,8 +449,9 @@ constexpr int kLaneHits = 8;
 // The lean ranking serves lists of K = L + 1 <= 32 labels; with longer lists
 // more labels pass tau and counting every pair costs more than a sort.
 constexpr int kLeanK = 32;
+template <class Release>
 __device__ __forceinline__ bool rank_lean(const float* __restrict__ row, int V, int L, u64* cand, float lpb,
-                                          int lane, const RankDst& d) {
+                                          int lane, const RankDst& d, Release&& release_row) {
   const int K = L + 1;
   const float4* r4 = reinterpret_cast<const float4*>(row);
   const int V4 = V >> 2;
@@ -528,6 +529,7 @@ __device__ __forceinline__ bool rank_lean(const float* __restrict__ row, int V, 
     }
   }
   if (__any_sync(RFULL, h > kLaneHits)) return false;
+  release_row();  // the row buffer is not read again: its next row may start arriving
   int incl = h;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -656,9 +658,22 @@ __device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int b
       }
     }
     __syncwarp();
-    // lists up to 31 labels: the lean ranking, which has written the record
-    // when it succeeds; otherwise (and for longer lists) the general one
-    const bool lean = E == 2 && L + 1 <= kLeanK && rank_lean(buf, V, L, cand, lpb, lane, dc);
+    // the next row's bulk copy, issued once every lane is done reading the buffer
+    bool issued = false;
+    auto next_copy = [&]() {
+      __syncwarp();
+      have = advance(&it, &row, &t);
+      if (have && lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        mbar_arrive_tx(bar, bytes);
+        bulk_g2s(buf, row, bytes, bar);
+      }
+      issued = true;
+    };
+    // lists up to 31 labels: the lean ranking, which issues the next copy as
+    // soon as its passes over the row are done and has written the record when
+    // it succeeds; otherwise (and for longer lists) the general one
+    const bool lean = E == 2 && L + 1 <= kLeanK && rank_lean(buf, V, L, cand, lpb, lane, dc, next_copy);
     const int n = lean ? 0 : rank_gather<E>(buf, V, L, cand, lane);
     if (n < 0) {  // constant or near-constant row: plain ranking of the staged row
       if (lane == 0) buf[blank] = rawb;
@@ -666,13 +681,7 @@ __device__ __forceinline__ void rank_tma_body_e(const Items& items, int V, int b
       rank_row(buf, V, blank, L, cand, lane, dc.ids, dc.lps, dc.cnt, dc.lpb, dc.flp, dc.fid);
       if (dc.tout && lane == 0) *dc.tout = dc.t;
     }
-    __syncwarp();  // every lane is done reading the buffer
-    have = advance(&it, &row, &t);
-    if (have && lane == 0) {
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      mbar_arrive_tx(bar, bytes);
-      bulk_g2s(buf, row, bytes, bar);
-    }
+    if (!issued) next_copy();
     if (!lean && n >= 0) rank_finish<E>(cand, n, L, lpb, lane, dc);
     if (dc.flag) {  // publish the record: every lane's stores, then the flag
       __threadfence();
