@@ -567,7 +567,7 @@ def main():
             torch.cuda.synchronize(dev)
             sp["rank"].append(ev[0].elapsed_time(ev[1]))
             sp["steps"].append(ev[1].elapsed_time(ev[2]))
-        split_ms = {k: statistics.mean(v) for k, v in sp.items()}
+        split_ms = {k: statistics.median(v) for k, v in sp.items()}  # medians: one cold run would skew a mean of ten
 
     # end to end through the public host-buffer call (ctcpb_decode_offline_host):
     # every step copies the valid frames and the lengths from page-locked host
@@ -604,7 +604,7 @@ def main():
     valid = world * int(np.minimum(lens_np, T).sum())
     peak, peak_kind = peaks()
     by = algorithmic_bytes(w, lens_np, kept, outs[1].cpu().numpy())
-    stage_ms = {n: statistics.mean(v) for n, v in per_stage.items()}
+    stage_ms = {n: statistics.median(v) for n, v in per_stage.items()}  # medians, like the split above
     dom = max(stage_ms, key=stage_ms.get)
     dom_bytes = {"rank": by["rank"], "select": by["select"], "steps": by["state"],
                  "rank+steps": by["rank"] + by["state"], "init": 0, "output": 0}[dom]

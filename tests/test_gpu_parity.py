@@ -167,6 +167,37 @@ def test_block_kernel_frame_scans_match_oracle(beam, V, paged, cap):
     assert cnt["frame_scans"] > 0, cnt
 
 
+@pytest.mark.parametrize("beam,V,list_len,flat", [(16, 3000, 0, "tie"), (8, 1024, 0, "tie"),
+                                                   (16, 400, 66, "near"), (12, 200, 40, "near")])
+def test_warp_kernel_exhaustive_paths_match_oracle(beam, V, list_len, flat):
+    """The warp-per-row kernel's slow selections.  "tie": every other frame
+    gives all non-blank labels one log-prob, so the first unlisted label ties
+    with the listed ones and the exhaustive selection must scan the frame.
+    "near": frames close to uniform with a long list, so that more candidates
+    reach the beam-th kept score than the compacting selection takes and the
+    general one runs."""
+    rng = np.random.default_rng(beam * V + list_len)
+    B, T = 4, 40
+    x = rng.normal(0.0, 1.0 if flat == "tie" else 0.05, size=(B, T, V))
+    x[:, :, 0] += 1.0 if flat == "tie" else 0.5
+    lp = log_softmax(x)
+    if flat == "tie":
+        lp[:, 1::2, 1:] = lp[:, 1::2, 1:].mean(-1, keepdims=True)
+    lens = np.array([40, 23, 1, 39], np.int32)
+    cfg = D.Config(beam=beam, nbest=beam, list_len=list_len)
+    dev = torch.device("cuda")
+    ws = torch.empty(D.workspace_size(cfg, B, T, V), dtype=torch.uint8, device=dev)
+    tok, ln, sc = D.decode_offline(cfg, torch.from_numpy(lp).to(dev), torch.from_numpy(lens).to(dev), workspace=ws)
+    torch.cuda.synchronize()
+    g = (tok.cpu().numpy(), ln.cpu().numpy(), sc.cpu().numpy())
+    assert_same(g, oracle_offline(cfg, lp, lens), f"beam {beam} V {V} L {list_len} {flat}")
+    cnt = D.read_counters(ws)
+    assert cnt["steps"] == int(lens.sum())
+    assert cnt["exhaustive"] > 0, cnt
+    if flat == "tie":
+        assert cnt["frame_scans"] > 0, cnt
+
+
 def test_ties_and_dead_labels_match_oracle():
     rng = np.random.default_rng(77)
     B, T, V = 4, 40, 9
