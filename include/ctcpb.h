@@ -25,8 +25,9 @@
  *   - Workspace and state buffers must be 256-byte aligned.
  *
  * Arithmetic: float32 with a fixed operation order and the library's own
- * exp/log1p (Cody-Waite reduction + Taylor series; atanh series), so results
- * are reproducible bit for bit on any launch shape.
+ * logsumexp, max(a, b) + F(|a - b|) with F(d) = log(1 + e^-d) evaluated from a
+ * table of degree-5 Taylor polynomials (96 segments of width 1/4; F = 0 from
+ * d = 24 on), so results are reproducible bit for bit on any launch shape.
  */
 #ifndef CTCPB_H
 #define CTCPB_H
@@ -247,9 +248,8 @@ int ctcpb_decode_offline_host_boosted(const ctcpb_config* cfg, const ctcpb_boost
  *     exceeds CTCPB_NOALLOC_SCRATCH_BYTES; nothing is launched then.
  *   - Calls no allocator.  The first call on each device looks up the array's
  *     device address (cudaGetSymbolAddress) with that device current, and
- *     keeps it for the process; make that first call before any stream
- *     capture.  The kept address does not survive cudaDeviceReset: do not use
- *     this call on a device after resetting it.
+ *     keeps it for the process.  The kept address does not survive
+ *     cudaDeviceReset: do not use this call on a device after resetting it.
  *   - All calls on a device share the one array, which keeps the last call's
  *     contents (each call resets what it reads before reading it).  Calls
  *     whose work overlaps on the GPU (different streams, or several host
