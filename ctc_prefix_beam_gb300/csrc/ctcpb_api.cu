@@ -165,15 +165,19 @@ int decode_offline_impl(const ctcpb_config* cfg, const ctcpb_boost* boost, const
   if ((rc = check_buf(ws, ws_bytes, lay.total))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   View st{(char*)ws, lay};
-  if (stage_mask & CTCPB_STAGE_INIT) {
+  const float thr = cfg->blank_threshold;
+  const int mode = thr >= 1.0f ? 0 : (thr > 0.0f ? 1 : 2);
+  const float log_thr = mode == 1 ? (float)std::log((double)thr) : 0.0f;
+  // the reset and the selection share a launch when both run
+  const bool init_select = (stage_mask & CTCPB_STAGE_INIT) && (stage_mask & CTCPB_STAGE_SELECT) && T > 0;
+  if (init_select)
+    TRY(launch_init_select(st, log_prob, stride_b, stride_t, seq_lengths, T, mode, log_thr, st.sel(), st.nsel(), s));
+  else if (stage_mask & CTCPB_STAGE_INIT)
     TRY(launch_init(st, s));
-    if (boost) TRY(launch_boost_build(st, boost->row_ptr, boost->tokens, boost->bonus, s));
-  }
+  if ((stage_mask & CTCPB_STAGE_INIT) && boost)
+    TRY(launch_boost_build(st, boost->row_ptr, boost->tokens, boost->bonus, s));
   if (T > 0) {
-    const float thr = cfg->blank_threshold;
-    const int mode = thr >= 1.0f ? 0 : (thr > 0.0f ? 1 : 2);
-    const float log_thr = mode == 1 ? (float)std::log((double)thr) : 0.0f;
-    if (stage_mask & CTCPB_STAGE_SELECT)
+    if ((stage_mask & CTCPB_STAGE_SELECT) && !init_select)
       TRY(launch_select(st, log_prob, stride_b, stride_t, seq_lengths, T, mode, log_thr, st.sel(), st.nsel(), s));
     const bool both = (stage_mask & CTCPB_STAGE_RANK) && (stage_mask & CTCPB_STAGE_STEPS);
     const int fused = both ? try_fused(st, log_prob, stride_b, stride_t, 0, nullptr, 0, 0, T, s) : 0;

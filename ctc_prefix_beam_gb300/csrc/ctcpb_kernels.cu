@@ -127,7 +127,8 @@ __device__ __forceinline__ void set_status(const View& st, u32 bit) { atomicOr(&
 
 // ------------------------------------------------------------------ init
 
-__global__ void k_init(View st) {
+// The reset, spread over the launch's threads.
+__device__ __forceinline__ void init_body(const View& st) {
   const Layout& L = st.lay;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t nthr = (size_t)gridDim.x * blockDim.x;
@@ -172,6 +173,8 @@ __global__ void k_init(View st) {
     for (size_t i = tid; i < np; i += nthr) rc[i] = 0;
   }
 }
+
+__global__ void k_init(View st) { init_body(st); }
 
 // ------------------------------------------------------------------ label boosts
 // Row b's label-boost hash table from entries [row_ptr[b], row_ptr[b+1]) of
@@ -233,12 +236,13 @@ __global__ void k_host_plan(const int* __restrict__ lens, int B, int T, int F, i
 // ------------------------------------------------------------------ select
 // Section 3.5: keep t < len_b iff lp[b,t,blank] < log_thr (mode 1), all
 // frames (mode 0) or none (mode 2); ordered compaction with warp ballots.
-__global__ void __launch_bounds__(256) k_select(View st, const float* __restrict__ lp, long long sb, long long stt,
-                                                const int* __restrict__ lens, int T, int mode, float log_thr,
-                                                int* __restrict__ sel, int* __restrict__ nsel) {
+// Row b's selection by one block of 256 threads.
+__device__ __forceinline__ void select_row(const View& st, int b, const float* __restrict__ lp, long long sb,
+                                           long long stt, const int* __restrict__ lens, int T, int mode,
+                                           float log_thr, int* __restrict__ sel, int* __restrict__ nsel) {
   __shared__ int wcount[8];
   __shared__ int base_s;
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int len_b = lens ? lens[b] : T;
   len_b = len_b < 0 ? 0 : (len_b > T ? T : len_b);
   const int blank = st.lay.blank;
@@ -270,6 +274,21 @@ __global__ void __launch_bounds__(256) k_select(View st, const float* __restrict
   const int n = base_s;
   for (int i = n + tid; i < T; i += 256) sel[(size_t)b * T + i] = -1;
   if (tid == 0) nsel[b] = n;
+}
+
+__global__ void __launch_bounds__(256) k_select(View st, const float* __restrict__ lp, long long sb, long long stt,
+                                                const int* __restrict__ lens, int T, int mode, float log_thr,
+                                                int* __restrict__ sel, int* __restrict__ nsel) {
+  select_row(st, blockIdx.x, lp, sb, stt, lens, T, mode, log_thr, sel, nsel);
+}
+
+// The reset and the selection in one launch (they touch disjoint memory):
+// blocks b < B also select row b.
+__global__ void __launch_bounds__(256) k_init_select(View st, const float* __restrict__ lp, long long sb,
+                                                     long long stt, const int* __restrict__ lens, int T, int mode,
+                                                     float log_thr, int* __restrict__ sel, int* __restrict__ nsel) {
+  init_body(st);
+  if ((int)blockIdx.x < st.lay.B) select_row(st, blockIdx.x, lp, sb, stt, lens, T, mode, log_thr, sel, nsel);
 }
 
 // Speech-masked streaming: the chunk rows of tile [tile_start, tile_start +
@@ -1282,53 +1301,53 @@ __global__ void __launch_bounds__(NT, 1) k_step(View st, const float* __restrict
 }
 
 // ------------------------------------------------------------------ output
-// Section 3.6: the first nbest hypotheses after a stable sort by score.
+// Section 3.6: the first nbest hypotheses after a stable sort by score.  Block
+// (b, n) writes row b's n-th: it finds the slot of rank n, then copies its
+// labels, so the rows' N best are written side by side.
 __global__ void __launch_bounds__(128) k_output(View st, int nbest, int* __restrict__ out_tokens,
                                                 int* __restrict__ out_lengths, float* __restrict__ out_scores,
                                                 int out_len) {
-  __shared__ int order[kMaxBeam];
   __shared__ float scs[kMaxBeam];
+  __shared__ int slot_n;
   const Layout& Ly = st.lay;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int b = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
   const RowHdr rh = st.rows()[b];
   const int beam = Ly.beam;
   const bool never = rh.step == 0;
   const int nlive = never ? 0 : rh.nlive;
+  const size_t o = (size_t)b * nbest + n;
+  int* dst = out_tokens + o * (size_t)out_len;
+  if (n >= nlive) {  // a dead slot (the whole block)
+    for (int x = tid; x < out_len; x += blockDim.x) dst[x] = -1;
+    if (tid == 0) {
+      const bool empty_row = never && n == 0;
+      out_lengths[o] = 0;
+      out_scores[o] = empty_row ? 0.0f : CTCPB_NEG;
+    }
+    return;
+  }
   for (int k = tid; k < nlive; k += blockDim.x) scs[k] = st.sc()[(size_t)b * beam + k];
   __syncthreads();
   for (int k = tid; k < nlive; k += blockDim.x) {
     int r = 0;
     const float v = scs[k];
     for (int j = 0; j < nlive; ++j) r += (scs[j] > v) || (scs[j] == v && j < k);
-    order[r] = k;
+    if (r == n) slot_n = k;  // ranks are a permutation: exactly one slot
   }
   __syncthreads();
+  const int k = slot_n;
   TokenStore tok{st, b};
   // flat storage left by the warp kernel: a slot's first plo labels may still
   // be in the other buffer (row porg)
   const bool pend = !Ly.paged && rh.pending != 0;
-  for (int n = 0; n < nbest; ++n) {
-    const size_t o = (size_t)b * nbest + n;
-    int* dst = out_tokens + o * (size_t)out_len;
-    if (n < nlive) {
-      const int k = order[n];
-      const int L = st.len()[(size_t)b * beam + k];
-      const int plo = pend ? st.plo()[(size_t)b * beam + k] : 0;
-      const int* pre = plo > 0 ? st.clist(rh.parity ^ 1, b, st.porg()[(size_t)b * beam + k]) : nullptr;
-      for (int x = tid; x < out_len; x += blockDim.x)
-        dst[x] = x < L ? (x < plo ? pre[x] : tok.get(rh.parity, k, x)) : -1;
-      if (tid == 0) {
-        out_lengths[o] = L;
-        out_scores[o] = scs[k];
-      }
-    } else {
-      for (int x = tid; x < out_len; x += blockDim.x) dst[x] = -1;
-      if (tid == 0) {
-        const bool empty_row = never && n == 0;
-        out_lengths[o] = 0;
-        out_scores[o] = empty_row ? 0.0f : CTCPB_NEG;
-      }
-    }
+  const int L = st.len()[(size_t)b * beam + k];
+  const int plo = pend ? st.plo()[(size_t)b * beam + k] : 0;
+  const int org = pend ? st.porg()[(size_t)b * beam + k] : 0;
+  const int* pre = plo > 0 ? st.clist(rh.parity ^ 1, b, org) : nullptr;
+  for (int x = tid; x < out_len; x += blockDim.x) dst[x] = x < L ? (x < plo ? pre[x] : tok.get(rh.parity, k, x)) : -1;
+  if (tid == 0) {
+    out_lengths[o] = L;
+    out_scores[o] = scs[k];
   }
 }
 
@@ -1354,6 +1373,14 @@ cudaError_t launch_boost_build(const View& st, const int* row_ptr, const int* to
                                cudaStream_t s) {
   if (st.lay.B == 0 || st.lay.hcap == 0) return cudaSuccess;
   k_boost_build<<<(st.lay.B + 63) / 64, 64, 0, s>>>(st, row_ptr, tokens, bonus);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_init_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
+                               int mode, float log_thr, int* sel, int* nsel, cudaStream_t s) {
+  const int gi = grid_for((long long)st.lay.B * st.lay.beam * 2 + 1, 8);
+  const int grid = st.lay.B > gi ? st.lay.B : gi;
+  k_init_select<<<grid, 256, 0, s>>>(st, lp, sb, stt, lens, T, mode, log_thr, sel, nsel);
   return cudaGetLastError();
 }
 
@@ -1416,7 +1443,9 @@ cudaError_t launch_host_plan(const int* lens, int B, int T, int F, int nchunks, 
 cudaError_t launch_output(const View& st, int nbest, int* out_tokens, int* out_lengths, float* out_scores,
                           int out_len, cudaStream_t s) {
   if (st.lay.B == 0) return cudaSuccess;
-  k_output<<<st.lay.B, 128, 0, s>>>(st, nbest, out_tokens, out_lengths, out_scores, out_len);
+  if (nbest <= 0) return cudaSuccess;
+  k_output<<<dim3((unsigned)st.lay.B, (unsigned)nbest), 128, 0, s>>>(st, nbest, out_tokens, out_lengths, out_scores,
+                                                                      out_len);
   return cudaGetLastError();
 }
 

@@ -39,6 +39,8 @@ cudaError_t launch_select_tile_thr(const View& st, const float* lp, long long sb
                                    const int* nframes, int chunk_T, int tile_start, int tile_len, cudaStream_t s);
 // Frames of each row in each chunk of F frames, for the host-buffer decode: plan [nchunks][B].
 cudaError_t launch_host_plan(const int* lens, int B, int T, int F, int nchunks, int* plan, cudaStream_t s);
+cudaError_t launch_init_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
+                               int mode, float log_thr, int* sel, int* nsel, cudaStream_t s);
 cudaError_t launch_select(const View& st, const float* lp, long long sb, long long stt, const int* lens, int T,
                           int mode, float log_thr, int* sel, int* nsel, cudaStream_t s);
 cudaError_t launch_prepass(const View& st, const float* lp, long long sb, long long stt, int mode,
