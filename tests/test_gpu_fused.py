@@ -22,7 +22,10 @@ def _run(cfg, lp, lens, split):
     outs = (torch.empty((B, cfg.nbest, out_len), dtype=torch.int32, device=dev),
             torch.empty((B, cfg.nbest), dtype=torch.int32, device=dev),
             torch.empty((B, cfg.nbest), dtype=torch.float32, device=dev))
-    if split:  # the pre-pass and the steps in two calls: two kernels
+    if split == "stages":  # every stage in a call of its own: the reset and the selection apart too
+        for stage in (D.STAGE_INIT, D.STAGE_SELECT, D.STAGE_RANK, D.STAGE_STEPS, D.STAGE_OUTPUT):
+            D.decode_offline(cfg, x, ln, workspace=ws, outputs=outs, out_len=out_len, stages=stage)
+    elif split:  # the pre-pass and the steps in two calls: two kernels
         D.decode_offline(cfg, x, ln, workspace=ws, outputs=outs, out_len=out_len,
                          stages=D.STAGE_INIT | D.STAGE_SELECT | D.STAGE_RANK)
         D.decode_offline(cfg, x, ln, workspace=ws, outputs=outs, out_len=out_len,
@@ -42,10 +45,11 @@ def test_fused_equals_two_kernels_and_oracle(name, over):
     cfg = cfg_of(w)
     fused, cf = _run(cfg, lp, lens, split=False)
     split, cs = _run(cfg, lp, lens, split=True)
-    assert cf["fused"] == 1 and cs["fused"] == 0
-    for a, b in zip(fused, split):
-        assert np.array_equal(a, b)
-    assert cf["steps"] == cs["steps"]
+    staged, cg = _run(cfg, lp, lens, split="stages")
+    assert cf["fused"] == 1 and cs["fused"] == 0 and cg["fused"] == 0
+    for a, b, c in zip(fused, split, staged):
+        assert np.array_equal(a, b) and np.array_equal(a, c)
+    assert cf["steps"] == cs["steps"] == cg["steps"]
     assert_same(fused, oracle_offline(cfg, lp, lens), f"{name}{over}")
 
 
