@@ -181,3 +181,40 @@ def test_random_long_utterances_match_oracle(seed):
                    space=cfg.space_id, boost=boost)
     assert_same(tuple(v.cpu().numpy() for v in out), ref, f"seed {seed}")
     assert st.status() == 0
+
+
+def draw_slow(seed):
+    """A warp-kernel configuration (beam <= 16, flat storage) with near-flat,
+    tied or quantised frames, so that many steps are unproven, exhaustive or
+    scan the frame."""
+    rng = np.random.default_rng(50_000 + seed)
+    V = int(rng.choice([8, 16, 40, 100, 256, 1000, 3000]))
+    beam = int(rng.integers(2, 17))
+    B, T = int(rng.integers(1, 5)), int(rng.integers(2, 80))
+    L = int(rng.choice([0, 0, 1, 3, 8, 22, 40, 66]))
+    cfg = D.Config(beam=beam, nbest=int(rng.integers(1, beam + 1)), list_len=L,
+                   max_seq_len=int(rng.integers(2, 30)) if rng.random() < 0.2 else 0,
+                   space_id=int(rng.integers(1, V)) if rng.random() < 0.2 else -1)
+    x = rng.normal(0.0, float(rng.choice([0.02, 0.1, 0.5, 1.0])), size=(B, T, V))
+    x[:, :, 0] += float(rng.choice([0.0, 0.5, 2.0]))
+    lp = x - x.max(-1, keepdims=True)
+    lp = (lp - np.log(np.exp(lp).sum(-1, keepdims=True))).astype(np.float32)
+    if rng.random() < 0.5:  # tied frames: every non-blank label one log-prob
+        fr = rng.random(T) < 0.4
+        lp[:, fr, 1:] = lp[:, fr, 1:].mean(-1, keepdims=True)
+    if rng.random() < 0.3:  # quantised log-probs: many exact ties
+        lp = np.round(lp, 1).astype(np.float32)
+    lens = rng.integers(0, T + 1, size=B).astype(np.int32)
+    return cfg, lp, lens
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_slow_selections_match_oracle(seed):
+    cfg, lp, lens = draw_slow(seed)
+    B, T, V = lp.shape
+    dev = torch.device("cuda")
+    ws = torch.empty(D.workspace_size(cfg, B, T, V), dtype=torch.uint8, device=dev)
+    out = D.decode_offline(cfg, torch.from_numpy(lp).to(dev), torch.from_numpy(lens).to(dev), workspace=ws)
+    torch.cuda.synchronize()
+    assert_same(tuple(o.cpu().numpy() for o in out), oracle_offline(cfg, lp, lens), f"seed {seed}: {cfg}")
+    assert D.read_status(ws) == 0
