@@ -33,7 +33,8 @@ static int grid_for(long long items_per_warp_units, int warps_per_block) {
 }
 }  // namespace
 
-// Warps (one 16-byte aligned row buffer each) that fit 200 KB of shared memory.
+// Warps (one 16-byte aligned row buffer each) that fit 200 KB of shared memory
+// (the fused launch; the stand-alone pre-pass takes what the device allows).
 int rank_tma_warps(int V) {
   int w = (int)((200u * 1024u) / rank_tma_per_warp(V));
   return w > 16 ? 16 : w;
@@ -111,6 +112,14 @@ cudaError_t launch_rank_tma(const Items& items, long long nitems, int V, int bla
                             cudaStream_t s) {
   const int E = L + 1 <= 64 ? 2 : (L + 1 <= 128 ? 4 : (L + 1 <= 256 ? 8 : 16));
   int wpb = rank_tma_warps(V);
+  {  // as many row buffers as the device's largest block allocation holds
+    int dev = 0, maxsm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess) {
+      const int w = (int)((size_t)maxsm / rank_tma_per_warp(V));
+      if (w > wpb) wpb = w > 16 ? 16 : w;
+    }
+  }
   if (E > 2 && wpb > 8) wpb = 8;
   const size_t smem = rank_tma_per_warp(V) * wpb;
   const void* fn = E == 2    ? (const void*)k_rank_tma<Items>
